@@ -1,0 +1,200 @@
+/*
+ * ia.h -- C ABI of the INT8-QK attention library (libia.so) for NVIDIA GB300 (sm_103a).
+ *
+ * Forward softmax attention with symmetric INT8 Q/K, an optional per-key
+ * additive bias, an optional tile-64 block-sparse key mask, a 16-bit P.V
+ * accumulated in FP32, an optional per-(head, channel) V scale and an optional
+ * natural-log LSE output, plus the quantisation pass in front of it and the
+ * exact two-partial merge behind it.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers on the current CUDA device unless stated.
+ *     The caller owns every buffer; the library allocates nothing on the
+ *     device, keeps no per-call state and never synchronises: each call only
+ *     enqueues kernels on `stream` (a cudaStream_t passed as void*; NULL is the
+ *     legacy default stream) and returns.
+ *   - Tensors are [B, H, S, D] ("BHSD") with the last dimension contiguous.
+ *     Strides are in ELEMENTS of the tensor's own type, ordered (b, h, s).
+ *   - Errors in the arguments are detected on the host before anything is
+ *     enqueued and returned as IA_ERR_INVALID_ARG / IA_ERR_UNSUPPORTED; a
+ *     failed launch returns IA_ERR_CUDA. ia_last_error_message() then holds a
+ *     one-line description (thread-local).
+ *   - Device-side waits inside the attention kernel are bounded. If one runs
+ *     out, the kernel records IA_ERR_TIMEOUT in a device status word and
+ *     returns instead of hanging; ia_device_status() reads and clears it.
+ *   - Only sm_103 devices are supported (IA_ERR_UNSUPPORTED otherwise).
+ */
+#ifndef IA_H_
+#define IA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define IA_API __attribute__((visibility("default")))
+#else
+#define IA_API
+#endif
+
+typedef enum ia_status {
+  IA_OK = 0,
+  IA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad shape or stride */
+  IA_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+  IA_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a launch failed */
+  IA_ERR_TIMEOUT = 4      /* a bounded device-side wait ran out */
+} ia_status;
+
+typedef enum ia_dtype { IA_BF16 = 0, IA_FP16 = 1 } ia_dtype;
+
+/* One fp32 scale per row ("per token") or per 64-row block of a head. */
+typedef enum ia_granularity { IA_PER_TOKEN = 0, IA_PER_BLOCK64 = 1 } ia_granularity;
+
+/*
+ * ia_quantize_qk -- K mean-centring and symmetric INT8 quantisation of Q and K.
+ *
+ * Defined by: "minimax_h3_sparse_int8" (FastVideo API page), module
+ * description and the source of sparse_sm89_attention (per-token scales; K
+ * centred by its mean over the sequence, a softmax-invariant shift; the mean is
+ * the sum over the sequence divided by the number of valid rows; int8 codes
+ * [B,H,S,D] and fp32 scales [B,H,S]); "Feature Request: Direct int8 Q/K
+ * passthrough between Comfy Kitchen and SageAttention", sections 2.1 and 3.1
+ * (mean_seq + quant_qk_int8; per-block scales); "[attention-int8] Multiple
+ * build issues and numerical accuracy problem", maintainer's point 1
+ * (symmetric range [-127, 127]).
+ *
+ * For each row (IA_PER_TOKEN) or 64-row block (IA_PER_BLOCK64) of a head:
+ *   x'    = fp32(x - mu)                 (K only, when centring; Q never)
+ *   amax  = max |x'|
+ *   scale = fp32(amax / 127)             (0 when amax == 0)
+ *   code  = round_half_even(fp32(x' * fp32(127 / amax))), clamped to +-127
+ * mu[b,h,d] = fp32(fp64(sum_s k[b,h,s,d]) / n_valid): the sum is accumulated
+ * with error-free transformations, exact whenever the float64 sum is.
+ *
+ *   q, k        16-bit inputs of type in_dtype, [B,H,Sq,D] and [B,H,Sk,D],
+ *               strides q_strides / k_strides (b,h,s in elements, d contiguous),
+ *               16-byte aligned rows. Either may be NULL to skip it.
+ *   D           64 or 128.
+ *   center_k    nonzero: subtract mu from K (mu from k_mean_in if non-NULL,
+ *               else computed). Ignored when k is NULL.
+ *   kv_valid    optional int32 [ceil(Sk/64)]: valid rows of each 64-row tile.
+ *               Requires Sk % 64 == 0. Rows past it get code 0 and, per
+ *               token, scale 0; they are left out of the mean's count and of
+ *               block maxima. When Sq == Sk it applies to Q as well.
+ *   k_mean_in   optional fp32 [B,H,D] mean to use instead of computing one
+ *               (so that separate calls share one centring frame).
+ *   q_i8, k_i8  outputs, int8 contiguous [B,H,Sq,D] / [B,H,Sk,D].
+ *   q_scale, k_scale  outputs, fp32 contiguous [B,H,Sq] / [B,H,Sk] per token,
+ *               [B,H,ceil(S/64)] per block.
+ *   k_mean_out  optional fp32 [B,H,D] output of the mean that was used.
+ */
+IA_API ia_status ia_quantize_qk(const void* q, const void* k, ia_dtype in_dtype, int B, int H,
+                                int Sq, int Sk, int D, const int64_t q_strides[3],
+                                const int64_t k_strides[3], ia_granularity granularity,
+                                int center_k, const int32_t* kv_valid, const float* k_mean_in,
+                                int8_t* q_i8, int8_t* k_i8, float* q_scale, float* k_scale,
+                                float* k_mean_out, void* stream);
+
+/* Shapes, strides and options of one attention call. */
+typedef struct ia_attn_params {
+  int B, H, Sq, Sk, D;          /* D is 64 or 128; Sq, Sk >= 0 */
+  float sm_scale;               /* softmax scale; NaN selects D^-1/2 */
+  ia_granularity granularity;   /* layout of q_scale / k_scale */
+  ia_dtype v_dtype;             /* element type of V, of P and of the output */
+  int64_t q_strides[3];         /* q_i8 (b,h,s), elements; rows 16-byte aligned */
+  int64_t k_strides[3];         /* k_i8 (b,h,s) */
+  int64_t qs_strides[2];        /* q_scale (b,h); s or block index contiguous */
+  int64_t ks_strides[2];        /* k_scale (b,h) */
+  int64_t v_strides[3];         /* v (b,h,s) */
+  int64_t o_strides[3];         /* out (b,h,s) */
+  int64_t lse_strides[2];       /* lse (b,h); query index contiguous */
+  const float* v_scale;         /* optional fp32 [H, D], applied once to the output */
+  const int32_t* kv_valid;      /* optional int32 [Sk/64] valid keys per 64-key tile */
+} ia_attn_params;
+
+/* Fill p with contiguous BHSD strides for the given shape (no pointers set). */
+IA_API void ia_attn_params_init(ia_attn_params* p, int B, int H, int Sq, int Sk, int D,
+                                ia_granularity granularity, ia_dtype v_dtype);
+
+/*
+ * ia_attention_fwd -- forward attention on INT8 Q/K with a 16-bit P.V.
+ *
+ * Defined by: "minimax_h3_sparse_int8" (FastVideo API page), module
+ * description (INT8 QK with per-token scales, FP32 accumulation, PV in BF16,
+ * V scale per head and channel applied once in the epilogue, tile-64 key
+ * selection with partial key tiles masked) and sparse_sm89_attention (mask
+ * [B,H,S/64,S/64], one validity entry per 64-key tile); "int8_attention:
+ * masked path costs ~1.8x unmasked, and a request for optional return_lse",
+ * opening paragraph (one fp32 additive bias per key, [1,1,1,K], shared by all
+ * heads and queries) and Question 2 (LSE so partial calls merge exactly);
+ * "Add optional forward LSE output" (FlyDSL), Summary and Public API
+ * (LSE = sm_scale*m + ln l, natural log, fp32 [B,H,Sq], -inf for fully masked
+ * rows).
+ *
+ *   s_ij = sm_scale * q_scale_i * k_scale_j * sum_d q_i8[i,d] * k_i8[j,d] + bias_j
+ *   s_ij = -inf where block_mask[b,h,i/64,j/64] == 0 or key j is past kv_valid
+ *   O_i  = v_scale[h,:] * sum_j softmax_j(s_i.) v_j       (output dtype = v_dtype)
+ *   LSE_i = ln sum_j e^{s_ij}; a row with no visible key gives O = 0, LSE = -inf.
+ * Query rows past kv_valid (when Sq == Sk) are padding: O = 0, LSE = -inf.
+ *
+ *   q_i8, k_i8          int8 codes (from ia_quantize_qk or a caller's GEMM epilogue).
+ *   q_scale, k_scale    fp32 scales laid out per p->granularity.
+ *   v                   [B,H,Sk,D] of p->v_dtype, strides p->v_strides.
+ *   bias_or_null        fp32 [Sk], contiguous: broadcast over B, H and queries.
+ *   block_mask_or_null  uint8/bool [B,H,ceil(Sq/64),ceil(Sk/64)], contiguous.
+ *   out                 [B,H,Sq,D] of p->v_dtype, strides p->o_strides.
+ *   lse_or_null         fp32 [B,H,Sq], strides p->lse_strides.
+ * A key sub-range [off, off+len) of larger tensors is a view: pass
+ * k_i8 + off*k_strides[2], k_scale + off (per token; off/64 per block, off a
+ * multiple of 64), v + off*v_strides[2], bias + off, and Sk = len.
+ * Alignment: q_i8, k_i8, v and out 16-byte aligned with 16-byte-multiple row,
+ * head and batch strides (in bytes).
+ */
+IA_API ia_status ia_attention_fwd(const int8_t* q_i8, const int8_t* k_i8, const float* q_scale,
+                                  const float* k_scale, const void* v, const float* bias_or_null,
+                                  const uint8_t* block_mask_or_null, void* out,
+                                  float* lse_or_null, const ia_attn_params* p, void* stream);
+
+/*
+ * ia_merge_lse -- exact merge of two partial attentions over disjoint key sets.
+ *
+ * Defined by: "int8_attention: masked path costs ~1.8x unmasked, ..." Question 2
+ * (a core call and a skirt call merged through their log-sum-exps) and "Add
+ * optional forward LSE output", Kernel implementation (split-K combine: LSE
+ * from the combined maximum and denominator).
+ *
+ *   M = max(L1, L2), w_k = e^{L_k - M}, L = M + ln(w1 + w2),
+ *   O = (w1 O1 + w2 O2) / (w1 + w2);  M = -inf gives O = 0, L = -inf.
+ * o1, o2, o_out: [B,H,Sq,D] contiguous of `dtype`; lse1, lse2, lse_out: fp32
+ * [B,H,Sq] contiguous. o_out may alias o1 or o2 and lse_out lse1 or lse2.
+ * lse_out may be NULL. All pointers 16-byte aligned; D is 64 or 128.
+ */
+IA_API ia_status ia_merge_lse(const void* o1, const float* lse1, const void* o2,
+                              const float* lse2, void* o_out, float* lse_out, int B, int H,
+                              int Sq, int D, ia_dtype dtype, void* stream);
+
+/* Static description of a status code. */
+IA_API const char* ia_status_string(ia_status s);
+
+/* Status and message of the last failed call on this host thread; IA_OK after a success. */
+IA_API ia_status ia_get_last_error(void);
+IA_API const char* ia_last_error_message(void);
+
+/*
+ * ia_device_status -- synchronise `stream`, then read and clear the device
+ * status word the attention kernel writes when a bounded wait runs out.
+ * Returns IA_OK, IA_ERR_TIMEOUT, or IA_ERR_CUDA if the synchronisation failed.
+ */
+IA_API ia_status ia_device_status(void* stream);
+
+/* Library version as "major.minor.patch". */
+IA_API const char* ia_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IA_H_ */

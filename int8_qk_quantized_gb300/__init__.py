@@ -1,0 +1,244 @@
+"""INT8-QK quantised attention for GB300 (sm_103a): Python binding of libia.so.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI in ``include/ia.h``. Torch is used for device memory
+and the current stream. If ``libia.so`` has not been built, the first call
+raises; there is no fallback implementation.
+
+    q8, qs, k8, ks = quantize_qk(q, k)                  # int8 codes + fp32 scales
+    out, lse = attention(q8, k8, qs, ks, v, bias=b, return_lse=True)
+    out, lse = merge_lse(o1, l1, o2, l2)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+__all__ = ["quantize_qk", "attention", "merge_lse", "device_status", "IAError", "lib_path",
+           "load_library", "AttnParams", "BF16", "FP16", "PER_TOKEN", "PER_BLOCK64"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "lib", "libia.so")
+_lib = None
+
+BF16, FP16 = 0, 1
+PER_TOKEN, PER_BLOCK64 = 0, 1
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "timeout"}
+
+
+class IAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class AttnParams(ctypes.Structure):
+    """Mirror of ``ia_attn_params``."""
+    _fields_ = [
+        ("B", ctypes.c_int), ("H", ctypes.c_int), ("Sq", ctypes.c_int), ("Sk", ctypes.c_int),
+        ("D", ctypes.c_int), ("sm_scale", ctypes.c_float), ("granularity", ctypes.c_int),
+        ("v_dtype", ctypes.c_int),
+        ("q_strides", ctypes.c_int64 * 3), ("k_strides", ctypes.c_int64 * 3),
+        ("qs_strides", ctypes.c_int64 * 2), ("ks_strides", ctypes.c_int64 * 2),
+        ("v_strides", ctypes.c_int64 * 3), ("o_strides", ctypes.c_int64 * 3),
+        ("lse_strides", ctypes.c_int64 * 2),
+        ("v_scale", ctypes.c_void_p), ("kv_valid", ctypes.c_void_p),
+    ]
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libia.so (built by ``build_lib.build()``) and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                           "int8_qk_quantized_gb300.build_lib.build() first")
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, i32, i64p = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int64)
+    L.ia_quantize_qk.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i64p, i64p, i32, i32,
+                                 vp, vp, vp, vp, vp, vp, vp, vp]
+    L.ia_quantize_qk.restype = i32
+    L.ia_attention_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                   ctypes.POINTER(AttnParams), vp]
+    L.ia_attention_fwd.restype = i32
+    L.ia_merge_lse.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
+    L.ia_merge_lse.restype = i32
+    L.ia_attn_params_init.argtypes = [ctypes.POINTER(AttnParams), i32, i32, i32, i32, i32, i32, i32]
+    L.ia_attn_params_init.restype = None
+    L.ia_device_status.argtypes = [vp]
+    L.ia_device_status.restype = i32
+    L.ia_status_string.argtypes = [i32]
+    L.ia_status_string.restype = ctypes.c_char_p
+    L.ia_last_error_message.argtypes = []
+    L.ia_last_error_message.restype = ctypes.c_char_p
+    L.ia_get_last_error.argtypes = []
+    L.ia_get_last_error.restype = i32
+    L.ia_version.argtypes = []
+    L.ia_version.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _check(status: int):
+    if status != 0:
+        msg = load_library().ia_last_error_message().decode(errors="replace")
+        raise IAError(status, msg)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(dt):
+    if dt == torch.bfloat16:
+        return BF16
+    if dt == torch.float16:
+        return FP16
+    raise TypeError(f"16-bit float tensors expected (bf16 or fp16), got {dt}")
+
+
+def _gran_code(g):
+    return {"token": PER_TOKEN, "block64": PER_BLOCK64}[g]
+
+
+def _strides3(t):
+    if t.dim() != 4 or t.stride(3) != 1:
+        raise ValueError("expected a [B,H,S,D] tensor with a contiguous last dimension")
+    return (ctypes.c_int64 * 3)(t.stride(0), t.stride(1), t.stride(2))
+
+
+def quantize_qk(q, k, granularity: str = "token", center_k: bool = True, kv_valid=None,
+                k_mean=None, return_mean: bool = False, stream=None):
+    """Quantise Q (may be None) and K to INT8 with symmetric fp32 scales.
+
+    Returns ``(q8, q_scale, k8, k_scale)`` (``None`` for a skipped input), plus
+    the K mean ``[B,H,D]`` that was used when ``return_mean``.
+    """
+    L = load_library()
+    ref = k if k is not None else q
+    B, H, _, D = ref.shape
+    dt = _dtype_code(ref.dtype)
+    g = _gran_code(granularity)
+    dev = ref.device
+
+    def nscale(S):
+        return S if g == PER_TOKEN else (S + 63) // 64
+
+    q8 = qs = k8 = ks = None
+    Sq = Sk = 0
+    if q is not None:
+        Sq = q.shape[2]
+        q8 = torch.empty((B, H, Sq, D), dtype=torch.int8, device=dev)
+        qs = torch.empty((B, H, nscale(Sq)), dtype=torch.float32, device=dev)
+    if k is not None:
+        Sk = k.shape[2]
+        k8 = torch.empty((B, H, Sk, D), dtype=torch.int8, device=dev)
+        ks = torch.empty((B, H, nscale(Sk)), dtype=torch.float32, device=dev)
+    mu = None
+    if return_mean and k is not None and center_k:
+        mu = torch.empty((B, H, D), dtype=torch.float32, device=dev)
+    if kv_valid is not None:
+        kv_valid = kv_valid.to(device=dev, dtype=torch.int32).contiguous()
+    if k_mean is not None:
+        k_mean = k_mean.to(device=dev, dtype=torch.float32).contiguous()
+    _check(L.ia_quantize_qk(
+        _ptr(q), _ptr(k), dt, B, H, Sq, Sk, D,
+        _strides3(q) if q is not None else None, _strides3(k) if k is not None else None,
+        g, 1 if center_k else 0, _ptr(kv_valid), _ptr(k_mean),
+        _ptr(q8), _ptr(k8), _ptr(qs), _ptr(ks), _ptr(mu), _stream(stream)))
+    res = (q8, qs, k8, ks)
+    return res + (mu,) if return_mean else res
+
+
+def attention(q8, k8, q_scale, k_scale, v, *, bias=None, block_mask=None, sm_scale=None,
+              v_scale=None, kv_valid=None, granularity: str = "token", return_lse: bool = False,
+              out=None, lse=None, stream=None):
+    """Forward attention on INT8 Q/K codes with a 16-bit P.V (see ``ia_attention_fwd``).
+
+    ``bias`` is fp32 ``[Sk]`` (any ``[1,1,1,Sk]`` view), ``block_mask`` bool
+    ``[B,H,ceil(Sq/64),ceil(Sk/64)]``, ``v_scale`` fp32 ``[H,D]``, ``kv_valid``
+    int32 ``[Sk/64]``. Returns ``out`` or ``(out, lse)``.
+    """
+    L = load_library()
+    B, H, Sq, D = q8.shape
+    Sk = k8.shape[2]
+    vd = _dtype_code(v.dtype)
+    p = AttnParams()
+    p.B, p.H, p.Sq, p.Sk, p.D = B, H, Sq, Sk, D
+    p.sm_scale = float("nan") if sm_scale is None else float(sm_scale)
+    p.granularity = _gran_code(granularity)
+    p.v_dtype = vd
+    if out is None:
+        out = torch.empty((B, H, Sq, D), dtype=v.dtype, device=v.device)
+    if return_lse and lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=v.device)
+    for name, t in (("q_strides", q8), ("k_strides", k8), ("v_strides", v), ("o_strides", out)):
+        s = _strides3(t)
+        getattr(p, name)[:] = list(s)
+    for name, t in (("qs_strides", q_scale), ("ks_strides", k_scale)):
+        if t.dim() != 3 or t.stride(2) != 1:
+            raise ValueError("scales must be [B,H,n] with a contiguous last dimension")
+        getattr(p, name)[:] = [t.stride(0), t.stride(1)]
+    if lse is not None:
+        if lse.dim() != 3 or lse.stride(2) != 1:
+            raise ValueError("lse must be [B,H,Sq] with a contiguous last dimension")
+        p.lse_strides[:] = [lse.stride(0), lse.stride(1)]
+    if bias is not None:
+        bias = bias.reshape(-1)
+        if bias.dtype != torch.float32 or bias.numel() != Sk or not bias.is_contiguous():
+            raise ValueError("bias must be a contiguous fp32 tensor with Sk elements")
+    if block_mask is not None:
+        if block_mask.dtype not in (torch.bool, torch.uint8) or not block_mask.is_contiguous():
+            raise ValueError("block_mask must be a contiguous bool/uint8 tensor")
+        if tuple(block_mask.shape) != (B, H, (Sq + 63) // 64, (Sk + 63) // 64):
+            raise ValueError("block_mask must be [B, H, ceil(Sq/64), ceil(Sk/64)]")
+    if v_scale is not None:
+        v_scale = v_scale.to(device=v.device, dtype=torch.float32).contiguous()
+        if v_scale.shape != (H, D):
+            raise ValueError("v_scale must be [H, D]")
+        p.v_scale = v_scale.data_ptr()
+    if kv_valid is not None:
+        kv_valid = kv_valid.to(device=v.device, dtype=torch.int32).contiguous()
+        p.kv_valid = kv_valid.data_ptr()
+    _check(L.ia_attention_fwd(_ptr(q8), _ptr(k8), _ptr(q_scale), _ptr(k_scale), _ptr(v),
+                              _ptr(bias), _ptr(block_mask), _ptr(out), _ptr(lse),
+                              ctypes.byref(p), _stream(stream)))
+    return (out, lse) if return_lse else out
+
+
+def merge_lse(o1, lse1, o2, lse2, out=None, lse_out=None, stream=None):
+    """Exact merge of two partial attentions through their LSEs (contiguous inputs)."""
+    L = load_library()
+    B, H, Sq, D = o1.shape
+    for t in (o1, o2, lse1, lse2):
+        if not t.is_contiguous():
+            raise ValueError("merge_lse expects contiguous inputs")
+    if out is None:
+        out = torch.empty_like(o1)
+    if lse_out is None:
+        lse_out = torch.empty_like(lse1)
+    _check(L.ia_merge_lse(_ptr(o1), _ptr(lse1), _ptr(o2), _ptr(lse2), _ptr(out), _ptr(lse_out),
+                          B, H, Sq, D, _dtype_code(o1.dtype), _stream(stream)))
+    return out, lse_out
+
+
+def device_status(stream=None):
+    """Synchronise the stream and raise if a bounded device wait ran out."""
+    _check(load_library().ia_device_status(_stream(stream)))
+
+
+def default_sm_scale(D: int) -> float:
+    return 1.0 / math.sqrt(D)

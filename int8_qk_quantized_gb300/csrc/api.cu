@@ -1,0 +1,275 @@
+// C ABI of libia.so: argument checking, status codes and dispatch to the
+// kernel launchers. Nothing here allocates device memory or synchronises
+// (except ia_device_status, which exists to synchronise).
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "launch.h"
+
+namespace {
+
+thread_local ia_status t_last = IA_OK;
+thread_local char t_msg[256] = "";
+
+ia_status fail(ia_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+ia_status fail(ia_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_msg, sizeof(t_msg), fmt, ap);
+  va_end(ap);
+  t_last = s;
+  return s;
+}
+
+ia_status ok() {
+  t_last = IA_OK;
+  t_msg[0] = '\0';
+  return IA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Current device must be sm_103; caches the SM count per device.
+ia_status check_device(int* num_sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(IA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  static thread_local int cached_dev = -1, cached_sms = 0, cached_ok = 0;
+  if (dev != cached_dev) {
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(IA_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+    cached_dev = dev;
+    cached_sms = sms;
+    cached_ok = (major == 10 && minor == 3) ? 1 : 0;
+    if (!cached_ok) {
+      cached_dev = -1;
+      return fail(IA_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", dev,
+                  major, minor);
+    }
+  }
+  *num_sms = cached_sms;
+  return IA_OK;
+}
+
+bool strides_ok(const int64_t* st, int n, int64_t esize) {
+  for (int i = 0; i < n; ++i)
+    if (st[i] < 0 || ((st[i] * esize) & 15) != 0) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+IA_API const char* ia_status_string(ia_status s) {
+  switch (s) {
+    case IA_OK: return "ok";
+    case IA_ERR_INVALID_ARG: return "invalid argument";
+    case IA_ERR_UNSUPPORTED: return "unsupported";
+    case IA_ERR_CUDA: return "CUDA error";
+    case IA_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+IA_API ia_status ia_get_last_error(void) { return t_last; }
+IA_API const char* ia_last_error_message(void) { return t_msg; }
+IA_API const char* ia_version(void) { return "0.1.0"; }
+
+IA_API void ia_attn_params_init(ia_attn_params* p, int B, int H, int Sq, int Sk, int D,
+                                ia_granularity granularity, ia_dtype v_dtype) {
+  if (p == nullptr) return;
+  std::memset(p, 0, sizeof(*p));
+  p->B = B;
+  p->H = H;
+  p->Sq = Sq;
+  p->Sk = Sk;
+  p->D = D;
+  p->sm_scale = NAN;
+  p->granularity = granularity;
+  p->v_dtype = v_dtype;
+  const int64_t hd = static_cast<int64_t>(D);
+  p->q_strides[0] = static_cast<int64_t>(H) * Sq * hd;
+  p->q_strides[1] = static_cast<int64_t>(Sq) * hd;
+  p->q_strides[2] = hd;
+  p->k_strides[0] = static_cast<int64_t>(H) * Sk * hd;
+  p->k_strides[1] = static_cast<int64_t>(Sk) * hd;
+  p->k_strides[2] = hd;
+  const int64_t nq = granularity == IA_PER_BLOCK64 ? (Sq + 63) / 64 : Sq;
+  const int64_t nk = granularity == IA_PER_BLOCK64 ? (Sk + 63) / 64 : Sk;
+  p->qs_strides[0] = static_cast<int64_t>(H) * nq;
+  p->qs_strides[1] = nq;
+  p->ks_strides[0] = static_cast<int64_t>(H) * nk;
+  p->ks_strides[1] = nk;
+  for (int i = 0; i < 3; ++i) p->v_strides[i] = p->k_strides[i];
+  for (int i = 0; i < 3; ++i) p->o_strides[i] = p->q_strides[i];
+  p->lse_strides[0] = static_cast<int64_t>(H) * Sq;
+  p->lse_strides[1] = Sq;
+}
+
+IA_API ia_status ia_quantize_qk(const void* q, const void* k, ia_dtype in_dtype, int B, int H,
+                                int Sq, int Sk, int D, const int64_t q_strides[3],
+                                const int64_t k_strides[3], ia_granularity granularity,
+                                int center_k, const int32_t* kv_valid, const float* k_mean_in,
+                                int8_t* q_i8, int8_t* k_i8, float* q_scale, float* k_scale,
+                                float* k_mean_out, void* stream) {
+  if (B < 0 || H < 0 || Sq < 0 || Sk < 0) return fail(IA_ERR_INVALID_ARG, "negative shape");
+  if (D != 64 && D != 128) return fail(IA_ERR_INVALID_ARG, "D must be 64 or 128 (got %d)", D);
+  if (in_dtype != IA_BF16 && in_dtype != IA_FP16) return fail(IA_ERR_INVALID_ARG, "in_dtype");
+  if (granularity != IA_PER_TOKEN && granularity != IA_PER_BLOCK64)
+    return fail(IA_ERR_INVALID_ARG, "granularity");
+  if (q == nullptr && k == nullptr) return fail(IA_ERR_INVALID_ARG, "q and k are both NULL");
+  if (q != nullptr) {
+    if (q_i8 == nullptr || q_scale == nullptr || q_strides == nullptr)
+      return fail(IA_ERR_INVALID_ARG, "q given without q_i8/q_scale/q_strides");
+    if (!aligned16(q) || !strides_ok(q_strides, 3, 2) || !aligned16(q_i8))
+      return fail(IA_ERR_INVALID_ARG, "q rows must be 16-byte aligned (base and b,h,s strides)");
+  }
+  if (k != nullptr) {
+    if (k_i8 == nullptr || k_scale == nullptr || k_strides == nullptr)
+      return fail(IA_ERR_INVALID_ARG, "k given without k_i8/k_scale/k_strides");
+    if (!aligned16(k) || !strides_ok(k_strides, 3, 2) || !aligned16(k_i8))
+      return fail(IA_ERR_INVALID_ARG, "k rows must be 16-byte aligned (base and b,h,s strides)");
+  }
+  if (kv_valid != nullptr && (Sk % 64) != 0)
+    return fail(IA_ERR_INVALID_ARG, "kv_valid requires Sk to be a multiple of 64 (Sk=%d)", Sk);
+  int sms = 0;
+  ia_status s = check_device(&sms);
+  if (s != IA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (q != nullptr) {
+    ia::QuantArgs a{};
+    a.x = q;
+    a.sb = q_strides[0];
+    a.sh = q_strides[1];
+    a.ss = q_strides[2];
+    a.B = B;
+    a.H = H;
+    a.S = Sq;
+    a.D = D;
+    a.dtype = in_dtype;
+    a.gran_block = granularity == IA_PER_BLOCK64;
+    a.center = 0;
+    a.valid = (kv_valid != nullptr && Sq == Sk) ? kv_valid : nullptr;
+    a.codes = q_i8;
+    a.scales = q_scale;
+    cudaError_t e = ia::launch_quantize(a, sms, st);
+    if (e != cudaSuccess) return fail(IA_ERR_CUDA, "quantize(q): %s", cudaGetErrorString(e));
+  }
+  if (k != nullptr) {
+    ia::QuantArgs a{};
+    a.x = k;
+    a.sb = k_strides[0];
+    a.sh = k_strides[1];
+    a.ss = k_strides[2];
+    a.B = B;
+    a.H = H;
+    a.S = Sk;
+    a.D = D;
+    a.dtype = in_dtype;
+    a.gran_block = granularity == IA_PER_BLOCK64;
+    a.center = center_k ? 1 : 0;
+    a.valid = kv_valid;
+    a.mean_in = center_k ? k_mean_in : nullptr;
+    a.mean_out = center_k ? k_mean_out : nullptr;
+    a.codes = k_i8;
+    a.scales = k_scale;
+    cudaError_t e = ia::launch_quantize(a, sms, st);
+    if (e != cudaSuccess) return fail(IA_ERR_CUDA, "quantize(k): %s", cudaGetErrorString(e));
+  }
+  return ok();
+}
+
+IA_API ia_status ia_attention_fwd(const int8_t* q_i8, const int8_t* k_i8, const float* q_scale,
+                                  const float* k_scale, const void* v, const float* bias_or_null,
+                                  const uint8_t* block_mask_or_null, void* out,
+                                  float* lse_or_null, const ia_attn_params* p, void* stream) {
+  if (p == nullptr) return fail(IA_ERR_INVALID_ARG, "params is NULL");
+  if (p->B < 0 || p->H < 0 || p->Sq < 0 || p->Sk < 0) return fail(IA_ERR_INVALID_ARG, "negative shape");
+  if (p->D != 64 && p->D != 128) return fail(IA_ERR_INVALID_ARG, "D must be 64 or 128 (got %d)", p->D);
+  if (p->v_dtype != IA_BF16 && p->v_dtype != IA_FP16) return fail(IA_ERR_INVALID_ARG, "v_dtype");
+  if (p->granularity != IA_PER_TOKEN && p->granularity != IA_PER_BLOCK64)
+    return fail(IA_ERR_INVALID_ARG, "granularity");
+  if (p->B == 0 || p->H == 0 || p->Sq == 0) return ok();
+  if (q_i8 == nullptr || k_i8 == nullptr || q_scale == nullptr || k_scale == nullptr ||
+      v == nullptr || out == nullptr)
+    return fail(IA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned16(q_i8) || !aligned16(k_i8) || !aligned16(v) || !aligned16(out))
+    return fail(IA_ERR_INVALID_ARG, "q_i8, k_i8, v and out must be 16-byte aligned");
+  if (!strides_ok(p->q_strides, 3, 1) || !strides_ok(p->k_strides, 3, 1) ||
+      !strides_ok(p->v_strides, 3, 2) || !strides_ok(p->o_strides, 3, 2))
+    return fail(IA_ERR_INVALID_ARG, "row/head/batch strides must be non-negative multiples of 16 bytes");
+  if ((p->q_strides[2] < p->D) || (p->k_strides[2] < p->D) || (p->v_strides[2] < p->D) ||
+      (p->o_strides[2] < p->D))
+    return fail(IA_ERR_INVALID_ARG, "row stride smaller than D");
+  if (p->kv_valid != nullptr && (p->Sk % 64) != 0)
+    return fail(IA_ERR_INVALID_ARG, "kv_valid requires Sk to be a multiple of 64 (Sk=%d)", p->Sk);
+  if (p->Sk > 65535 * 64)
+    return fail(IA_ERR_UNSUPPORTED, "Sk too large (%d)", p->Sk);
+  float sm = p->sm_scale;
+  if (std::isnan(sm)) sm = 1.0f / std::sqrt(static_cast<float>(p->D));
+  if (!std::isfinite(sm) || sm <= 0.f) return fail(IA_ERR_INVALID_ARG, "sm_scale must be positive");
+  int sms = 0;
+  ia_status s = check_device(&sms);
+  if (s != IA_OK) return s;
+  ia::AttnLaunch a{};
+  a.q = q_i8;
+  a.k = k_i8;
+  a.q_scale = q_scale;
+  a.k_scale = k_scale;
+  a.v = v;
+  a.bias = bias_or_null;
+  a.mask = block_mask_or_null;
+  a.out = out;
+  a.lse = lse_or_null;
+  a.p = *p;
+  a.sm_scale = sm;
+  const char* msg = "";
+  s = ia::launch_attention(a, sms, static_cast<cudaStream_t>(stream), &msg);
+  if (s != IA_OK) return fail(s, "attention: %s", msg);
+  return ok();
+}
+
+IA_API ia_status ia_merge_lse(const void* o1, const float* lse1, const void* o2,
+                              const float* lse2, void* o_out, float* lse_out, int B, int H,
+                              int Sq, int D, ia_dtype dtype, void* stream) {
+  if (B < 0 || H < 0 || Sq < 0) return fail(IA_ERR_INVALID_ARG, "negative shape");
+  if (D != 64 && D != 128) return fail(IA_ERR_INVALID_ARG, "D must be 64 or 128 (got %d)", D);
+  if (dtype != IA_BF16 && dtype != IA_FP16) return fail(IA_ERR_INVALID_ARG, "dtype");
+  if (static_cast<int64_t>(B) * H * Sq == 0) return ok();
+  if (o1 == nullptr || o2 == nullptr || lse1 == nullptr || lse2 == nullptr || o_out == nullptr)
+    return fail(IA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned16(o1) || !aligned16(o2) || !aligned16(o_out))
+    return fail(IA_ERR_INVALID_ARG, "outputs and inputs must be 16-byte aligned");
+  int sms = 0;
+  ia_status s = check_device(&sms);
+  if (s != IA_OK) return s;
+  ia::MergeArgs a{};
+  a.o1 = o1;
+  a.l1 = lse1;
+  a.o2 = o2;
+  a.l2 = lse2;
+  a.o = o_out;
+  a.l = lse_out;
+  a.rows = static_cast<int64_t>(B) * H * Sq;
+  a.D = D;
+  a.dtype = dtype;
+  cudaError_t e = ia::launch_merge(a, sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(IA_ERR_CUDA, "merge: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+IA_API ia_status ia_device_status(void* stream) {
+  unsigned int w = 0;
+  cudaError_t e = ia::attention_read_device_error(&w, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(IA_ERR_CUDA, "device status: %s", cudaGetErrorString(e));
+  if (w != 0) return fail(IA_ERR_TIMEOUT, "attention kernel status word 0x%x", w);
+  return ok();
+}
+
+}  // extern "C"

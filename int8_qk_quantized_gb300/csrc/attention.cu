@@ -1,0 +1,736 @@
+// Forward attention with INT8 Q/K and a 16-bit P.V on sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes ("minimax_h3_sparse_int8", FastVideo API page, module
+// description and sparse_sm89_attention; "int8_attention: masked path costs
+// ~1.8x unmasked, and a request for optional return_lse", opening paragraph;
+// "Add optional forward LSE output", Summary):
+//   s_ij = sm_scale * qs_i * ks_j * <q8_i, k8_j> + bias_j       (or -inf if masked)
+//   O_i  = v_scale (*) sum_j softmax_j(s_i.) v_j,   LSE_i = ln sum_j e^{s_ij}
+//
+// How, on GB300:
+//  * INT8 codes in [-127, 127] are exact in FP16, each product is exact in
+//    FP32 and every partial sum of a D <= 128 dot product stays below 2^24, so
+//    the QK^T MMA runs as tcgen05 kind::f16 on FP16-coded codes and yields the
+//    exact integer dot products in its FP32 accumulator (sm_103a has no
+//    kind::i8). The int8 tiles travel from HBM by TMA at one byte per element
+//    and two converter warps widen them in shared memory into the 128-byte
+//    swizzled K-major layout the MMA reads.
+//  * A CTA owns QS query stages of 128 rows. One thread issues the MMAs:
+//    S_s = Q_s K_j^T into TMEM, then O_s += P_s V_j with P_s read from TMEM.
+//    While the softmax warpgroup of one stage works on its S tile, the tensor
+//    core runs the other stage's MMAs.
+//  * Softmax warpgroups own one query row per thread (TMEM lane = row). They
+//    apply k_scale (and bias, masks) to the FP32 logits, keep a running
+//    maximum in log2 units, rescale O in TMEM only when the maximum grew by
+//    more than 8 (2^8 headroom in P), write P as bf16/f16 into the S columns
+//    and keep the row sum in FP32. The epilogue applies 1/l and the
+//    per-channel V scale once and writes the LSE in natural log.
+//  * The per-key bias and the k scales are loaded once per key tile into
+//    shared memory and read by all query rows (the [1,1,1,K] broadcast).
+//  * Block-sparse: one 128-row stage (two 64-row query tiles) walks the
+//    union of its tiles' kept key tiles (64 keys each); rows whose own query
+//    tile dropped a key tile see -inf there.
+//  * Every mbarrier wait is bounded. When one runs out the kernel records it
+//    in a device status word, stops issuing work, drains what is in flight,
+//    frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+#include <cstdio>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace ia {
+
+__device__ unsigned int g_attn_status;
+
+namespace {
+
+constexpr int kM = 128;              // query rows per stage (MMA M)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
+constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
+
+enum : unsigned {
+  kErrProducer = 1u,
+  kErrConverter = 2u,
+  kErrMma = 4u,
+  kErrSoftmax = 8u,
+  kErrDrain = 16u,
+  kErrSmemAlign = 32u,
+};
+
+struct Params {
+  const float* q_scale;
+  const float* k_scale;
+  const float* bias;
+  const uint8_t* mask;
+  const int32_t* kv_valid;
+  const float* v_scale;
+  void* out;
+  float* lse;
+  int H, Sq, Sk;
+  int n_tiles;   // key tiles (dense); mask width Tk (sparse)
+  int Tq, Tk;
+  float cq_mult;  // sm_scale * log2(e)
+  int gran_block;
+  int pad_query;
+  int64_t qs_sb, qs_sh, ks_sb, ks_sh;
+  int64_t o_sb, o_sh, o_ss;
+  int64_t l_sb, l_sh;
+  unsigned long long timeout_ns;
+};
+
+template <int D, int QS, int BN, bool SPARSE>
+struct Layout {
+  static constexpr int NKS = 2, NVS = 2, NRS = 2, NSC = 2;
+  static constexpr int QH = kM * D * 2;   // fp16 Q stage
+  static constexpr int KH = BN * D * 2;   // fp16 K tile
+  static constexpr int VB = BN * D * 2;   // 16-bit V tile
+  static constexpr int KR = BN * D;       // int8 K tile
+  static constexpr int QR = kM * D;       // int8 Q stage
+  static constexpr int SC = BN * 8 + 16;  // k scales, bias*log2e, flags
+  static constexpr int OFF_QH = 0;
+  static constexpr int OFF_KH = OFF_QH + QS * QH;
+  static constexpr int OFF_V = OFF_KH + NKS * KH;
+  static constexpr int OFF_KR = OFF_V + NVS * VB;
+  static constexpr int OFF_SC = OFF_KR + NRS * KR;
+  static constexpr int OFF_VS = OFF_SC + NSC * SC;
+  static constexpr int OFF_BAR = (OFF_VS + D * 4 + 7) / 8 * 8;
+  // barrier indices
+  static constexpr int B_QFULL = 0, B_QCONV = 1, B_KRF = 2, B_KRE = B_KRF + NRS,
+                       B_KCF = B_KRE + NRS, B_KCE = B_KCF + NKS, B_VF = B_KCE + NKS,
+                       B_VE = B_VF + NVS, B_SCF = B_VE + NVS, B_SCE = B_SCF + NSC,
+                       B_SF = B_SCE + NSC, B_PF = B_SF + QS, B_OF = B_PF + QS,
+                       B_DRAIN = B_OF + QS, NBAR = B_DRAIN + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;       // tmem base, abort, count, pad
+  static constexpr int OFF_LIST = OFF_MISC + 16 + 32;       // + warp counts for the list scan
+  static constexpr int SMEM_FIXED = OFF_LIST;
+  static constexpr int TMEM_NEED = QS * BN + QS * D;
+  static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64
+                                   : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
+  static constexpr int NWARPS = 4 * QS + 4;
+  static constexpr int W_PROD = 4 * QS, W_MMA = 4 * QS + 1, W_CONV = 4 * QS + 2;
+  static_assert(QS * QR <= VB, "raw Q is staged in the first V buffer");
+  static_assert(TMEM_NEED <= 512, "TMEM budget");
+  static_assert(OFF_QH % 1024 == 0 && OFF_KH % 1024 == 0 && OFF_V % 1024 == 0, "swizzle align");
+};
+
+struct Ctl {
+  volatile int* abort;
+  unsigned long long timeout;
+};
+
+// Bounded wait on an mbarrier phase. Returns false when the wait ran out here
+// (the status word and the CTA's abort flag are set) or another thread of
+// the CTA has already aborted.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c, unsigned code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*c.abort) return false;
+    if ((n & 15u) == 0 && *reinterpret_cast<volatile unsigned*>(&g_attn_status) != 0u) {
+      *c.abort = 1;  // another CTA already timed out: stop waiting as well
+      return false;
+    }
+    if ((n & 15u) == 0 && globaltimer_ns() - t0 > c.timeout) {
+      *c.abort = 1;
+      atomicOr(&g_attn_status, code);
+      return false;
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag: used to let copies and MMAs that
+// were already issued land before the CTA releases its shared memory and TMEM.
+__device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity, unsigned long long timeout) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 0;; ++n) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((n & 15u) == 15u && globaltimer_ns() - t0 > timeout) {
+      atomicOr(&g_attn_status, kErrDrain);
+      return;
+    }
+  }
+}
+
+// int8 tile [rows x D] row-major -> fp16 [rows x D] in 128-byte-swizzled
+// K-major blocks of 64 columns (block stride rows*128 bytes), as tcgen05 reads
+// with a SWIZZLE_128B descriptor. 64 threads.
+template <int D>
+__device__ __forceinline__ void widen_tile(const uint8_t* raw, uint8_t* dst, int rows, int ct) {
+  constexpr int CPR = D / 16;  // 16-byte int8 chunks per row
+  for (int idx = ct; idx < rows * CPR; idx += 64) {
+    const int r = idx / CPR, c = idx % CPR;
+    const uint4 w = *reinterpret_cast<const uint4*>(raw + r * D + c * 16);
+    uint32_t h[8];
+    i8x4_to_f16x4(w.x, h[0], h[1]);
+    i8x4_to_f16x4(w.y, h[2], h[3]);
+    i8x4_to_f16x4(w.z, h[4], h[5]);
+    i8x4_to_f16x4(w.w, h[6], h[7]);
+    const int blk = c >> 2;          // 64-column block
+    const int k0 = (c & 3) * 2;      // first 16-byte chunk within the 128-byte row
+    uint8_t* rowp = dst + blk * (rows * 128) + r * 128;
+    const int sw = r & 7;
+    *reinterpret_cast<uint4*>(rowp + ((k0 ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(rowp + (((k0 + 1) ^ sw) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
+template <int D, int QS, int BN, bool SPARSE, bool VBF16>
+__global__ void __launch_bounds__(32 * (4 * QS + 4), 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const Params a) {
+  using L = Layout<D, QS, BN, SPARSE>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int q0 = blockIdx.x * (kM * QS);
+
+  if ((smem_u32(smem) & 1023u) != 0) {  // swizzled operands need 1024-byte alignment
+    if (tid == 0) atomicOr(&g_attn_status, kErrSmemAlign);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  const Ctl ctl{abort_flag, a.timeout_ns};
+  auto bar = [&](int i) -> uint32_t { return smem_u32(bars + i); };
+
+  if (tid == 0) {
+    mbar_init(bar(L::B_QFULL), 1);
+    mbar_init(bar(L::B_QCONV), 64);
+    for (int i = 0; i < L::NRS; ++i) {
+      mbar_init(bar(L::B_KRF + i), 1);
+      mbar_init(bar(L::B_KRE + i), 64);
+    }
+    for (int i = 0; i < L::NKS; ++i) {
+      mbar_init(bar(L::B_KCF + i), 64);
+      mbar_init(bar(L::B_KCE + i), 1);
+    }
+    for (int i = 0; i < L::NVS; ++i) {
+      mbar_init(bar(L::B_VF + i), 1);
+      mbar_init(bar(L::B_VE + i), 1);
+    }
+    for (int i = 0; i < L::NSC; ++i) {
+      mbar_init(bar(L::B_SCF + i), 64);
+      mbar_init(bar(L::B_SCE + i), 4 * QS);
+    }
+    for (int s = 0; s < QS; ++s) {
+      mbar_init(bar(L::B_SF + s), 1);
+      mbar_init(bar(L::B_PF + s), kM);
+      mbar_init(bar(L::B_OF + s), 1);
+    }
+    mbar_init(bar(L::B_DRAIN), 1);
+    misc[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == L::W_MMA) {
+    tmem_alloc(smem_u32(misc), L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  float* vsc = reinterpret_cast<float*>(smem + L::OFF_VS);
+  for (int i = tid; i < D; i += blockDim.x) vsc[i] = a.v_scale ? __ldg(a.v_scale + h * D + i) : 1.f;
+
+  // Key tiles this CTA visits: all of them (dense) or the union of the kept
+  // tiles of its two 64-row query tiles, in ascending order (block-sparse).
+  uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::OFF_LIST);
+  int n_it;
+  const int qt0 = q0 / 64;
+  const int qt1 = qt0 + 1;
+  if constexpr (SPARSE) {
+    const uint8_t* m0 = a.mask + (static_cast<int64_t>(b * a.H + h) * a.Tq + qt0) * a.Tk;
+    const uint8_t* m1 = qt1 < a.Tq ? m0 + a.Tk : nullptr;
+    int* wcnt = reinterpret_cast<int*>(smem + L::OFF_MISC + 16);
+    int total = 0;
+    const int nw = blockDim.x >> 5;
+    for (int base = 0; base < a.Tk; base += blockDim.x) {
+      const int t = base + tid;
+      const bool keep = t < a.Tk && (m0[t] != 0 || (m1 != nullptr && m1[t] != 0));
+      const unsigned bal = __ballot_sync(0xffffffffu, keep);
+      if (lane == 0) wcnt[warp] = __popc(bal);
+      __syncthreads();
+      int before = total;
+      for (int w = 0; w < warp; ++w) before += wcnt[w];
+      if (keep) list[before + __popc(bal & ((1u << lane) - 1u))] = static_cast<uint16_t>(t);
+      for (int w = 0; w < nw; ++w) total += wcnt[w];
+      __syncthreads();
+    }
+    n_it = total;
+  } else {
+    n_it = a.n_tiles;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  const uint32_t sm_qh = smem_u32(smem + L::OFF_QH);
+  const uint32_t sm_kh = smem_u32(smem + L::OFF_KH);
+  const uint32_t sm_v = smem_u32(smem + L::OFF_V);
+  const uint32_t sm_kr = smem_u32(smem + L::OFF_KR);
+
+  if (warp == L::W_PROD) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      int kr_last[L::NRS], v_last[L::NVS];
+      for (int i = 0; i < L::NRS; ++i) kr_last[i] = -1;
+      for (int i = 0; i < L::NVS; ++i) v_last[i] = -1;
+      mbar_arrive_expect_tx(bar(L::B_QFULL), QS * kM * D);
+      for (int s = 0; s < QS; ++s)
+        tma_load_4d(sm_v + s * L::QR, &tm_q, bar(L::B_QFULL), 0, q0 + s * kM, h, b);
+      bool ok = true;
+      for (int it = 0; it < n_it; ++it) {
+        const int kt = SPARSE ? static_cast<int>(list[it]) : it;
+        const int rs = it % L::NRS;
+        if (it >= L::NRS) ok = wait_bar(bar(L::B_KRE + rs), ((it / L::NRS) - 1) & 1, ctl, kErrProducer);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(L::B_KRF + rs), BN * D);
+        tma_load_4d(sm_kr + rs * L::KR, &tm_k, bar(L::B_KRF + rs), 0, kt * BN, h, b);
+        kr_last[rs] = it;
+        const int vs = it % L::NVS;
+        if (it == 0)
+          ok = wait_bar(bar(L::B_QCONV), 0, ctl, kErrProducer);  // raw Q sits in V buffer 0
+        else if (it >= L::NVS)
+          ok = wait_bar(bar(L::B_VE + vs), ((it / L::NVS) - 1) & 1, ctl, kErrProducer);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(L::B_VF + vs), BN * D * 2);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(sm_v + vs * L::VB + c * BN * 128, &tm_v, bar(L::B_VF + vs), c * 64, kt * BN, h, b);
+        v_last[vs] = it;
+      }
+      if (!ok) {  // let issued copies land before the CTA's shared memory goes away
+        drain_bar(bar(L::B_QFULL), 0, a.timeout_ns);
+        for (int i = 0; i < L::NRS; ++i)
+          if (kr_last[i] >= 0) drain_bar(bar(L::B_KRF + i), (kr_last[i] / L::NRS) & 1, a.timeout_ns);
+        for (int i = 0; i < L::NVS; ++i)
+          if (v_last[i] >= 0) drain_bar(bar(L::B_VF + i), (v_last[i] / L::NVS) & 1, a.timeout_ns);
+      }
+    }
+  } else if (warp == L::W_MMA) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idq = idesc_f16(kM, BN, 0, 0, 0, 0);                  // f16 x f16, K-major
+      constexpr uint32_t idv = idesc_f16(kM, D, VBF16 ? 1 : 0, VBF16 ? 1 : 0, 0, 1);  // V MN-major
+      auto issue_qk = [&](int s, int kst) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(sm_qh + s * L::QH + (kk >> 2) * (kM * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sm_kh + kst * L::KH + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
+          mma_ss(tmem + s * BN, ad, bd, idq, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int s, int vs, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t bd = sdesc_sw128(sm_v + vs * L::VB + kk * 16 * 128, BN * 128, 1024);
+          mma_ts(tmem + QS * BN + s * D, tmem + s * BN + kk * 8, bd, idv, (first && kk == 0) ? 0u : 1u);
+        }
+      };
+      bool ok = wait_bar(bar(L::B_QCONV), 0, ctl, kErrMma);
+      tc_fence_after();
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int kst = it % L::NKS;
+        ok = wait_bar(bar(L::B_KCF + kst), (it / L::NKS) & 1, ctl, kErrMma);
+        if (!ok) break;
+        tc_fence_after();
+        const int pvs = (it + L::NVS - 1) % L::NVS;
+        if (it > 0) {
+          ok = wait_bar(bar(L::B_VF + pvs), ((it - 1) / L::NVS) & 1, ctl, kErrMma);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        for (int s = 0; s < QS && ok; ++s) {
+          if (it > 0) {
+            ok = wait_bar(bar(L::B_PF + s), (it - 1) & 1, ctl, kErrMma);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(s, pvs, it == 1);
+          }
+          issue_qk(s, kst);
+          mma_commit(bar(L::B_SF + s));
+        }
+        if (!ok) break;
+        mma_commit(bar(L::B_KCE + kst));
+        if (it > 0) mma_commit(bar(L::B_VE + pvs));
+      }
+      if (ok && n_it > 0) {
+        const int pvs = (n_it - 1) % L::NVS;
+        ok = wait_bar(bar(L::B_VF + pvs), ((n_it - 1) / L::NVS) & 1, ctl, kErrMma);
+        if (ok) tc_fence_after();
+        for (int s = 0; s < QS && ok; ++s) {
+          ok = wait_bar(bar(L::B_PF + s), (n_it - 1) & 1, ctl, kErrMma);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(s, pvs, n_it == 1);
+          mma_commit(bar(L::B_OF + s));
+        }
+      }
+      mma_commit(bar(L::B_DRAIN));  // every MMA issued above has completed once this arrives
+      drain_bar(bar(L::B_DRAIN), 0, a.timeout_ns);
+    }
+  } else if (warp >= L::W_CONV) {
+    // ---------------------------------------------- int8 -> fp16 converters
+    const int ct = tid - L::W_CONV * 32;
+    bool ok = wait_bar(bar(L::B_QFULL), 0, ctl, kErrConverter);
+    if (ok) {
+      for (int s = 0; s < QS; ++s)
+        widen_tile<D>(smem + L::OFF_V + s * L::QR, smem + L::OFF_QH + s * L::QH, kM, ct);
+      fence_proxy_async_smem();
+      mbar_arrive(bar(L::B_QCONV));
+    }
+    const uint8_t* mrow0 = nullptr;
+    const uint8_t* mrow1 = nullptr;
+    if (SPARSE) {
+      mrow0 = a.mask + (static_cast<int64_t>(b * a.H + h) * a.Tq + qt0) * a.Tk;
+      mrow1 = qt1 < a.Tq ? mrow0 + a.Tk : nullptr;
+    }
+    const float* ksb = a.k_scale + b * a.ks_sb + h * a.ks_sh;
+    for (int it = 0; it < n_it && ok; ++it) {
+      const int kt = SPARSE ? static_cast<int>(list[it]) : it;
+      // per-key softmax constants of this tile
+      const int ss = it % L::NSC;
+      if (it >= L::NSC) ok = wait_bar(bar(L::B_SCE + ss), ((it / L::NSC) - 1) & 1, ctl, kErrConverter);
+      if (!ok) break;
+      float* ksm = reinterpret_cast<float*>(smem + L::OFF_SC + ss * L::SC);
+      float* b2m = ksm + BN;
+      uint32_t* flg = reinterpret_cast<uint32_t*>(b2m + BN);
+      for (int c = ct; c < BN; c += 64) {
+        const int key = kt * BN + c;
+        const bool valid = key < a.Sk && (a.kv_valid == nullptr || (key & 63) < __ldg(a.kv_valid + (key >> 6)));
+        ksm[c] = valid ? __ldg(ksb + (a.gran_block ? (key >> 6) : key)) : 0.f;
+        b2m[c] = valid ? (a.bias ? __ldg(a.bias + key) * kLog2e : 0.f) : -INFINITY;
+      }
+      if (ct == 0) {
+        bool partial = kt * BN + BN > a.Sk;
+        if (a.kv_valid)
+          for (int t = (kt * BN) >> 6; t < ((kt + 1) * BN) >> 6 && t * 64 < a.Sk; ++t)
+            partial |= __ldg(a.kv_valid + t) < 64;
+        uint32_t f = (a.bias != nullptr || partial) ? 1u : 0u;
+        if (SPARSE) {
+          const uint32_t k0 = mrow0[kt] ? 1u : 0u;
+          const uint32_t k1 = (mrow1 != nullptr && mrow1[kt]) ? 1u : 0u;
+          f |= (k0 << 1) | (k1 << 2);
+          if (!(k0 && k1)) f |= 1u;
+        } else {
+          f |= 6u;
+        }
+        *flg = f;
+      }
+      mbar_arrive(bar(L::B_SCF + ss));
+      // K tile
+      const int rs = it % L::NRS, kst = it % L::NKS;
+      ok = wait_bar(bar(L::B_KRF + rs), (it / L::NRS) & 1, ctl, kErrConverter);
+      if (!ok) break;
+      if (it >= L::NKS) ok = wait_bar(bar(L::B_KCE + kst), ((it / L::NKS) - 1) & 1, ctl, kErrConverter);
+      if (!ok) break;
+      widen_tile<D>(smem + L::OFF_KR + rs * L::KR, smem + L::OFF_KH + kst * L::KH, BN, ct);
+      fence_proxy_async_smem();
+      mbar_arrive(bar(L::B_KCF + kst));
+      mbar_arrive(bar(L::B_KRE + rs));
+    }
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int s = warp >> 2;
+    const int r = tid & (kM - 1);
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + s * BN + lane_off;
+    const uint32_t tO = tmem + QS * BN + s * D + lane_off;
+    const int row = q0 + s * kM + r;
+    const bool row_ok = row < a.Sq;
+    float cq = 0.f;
+    if (row_ok)
+      cq = __ldg(a.q_scale + b * a.qs_sb + h * a.qs_sh + (a.gran_block ? (row >> 6) : row)) * a.cq_mult;
+    const int half = (r >= 64) ? 1 : 0;
+    float m = -INFINITY;  // reference maximum (log2 units) that P is relative to
+    float l = 0.f;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int ss = it % L::NSC;
+      bool w = wait_bar(bar(L::B_SF + s), it & 1, ctl, kErrSoftmax);
+      w = w && wait_bar(bar(L::B_SCF + ss), (it / L::NSC) & 1, ctl, kErrSoftmax);
+      ok = __all_sync(0xffffffffu, w);
+      if (!ok) break;
+      tc_fence_after();
+      const float* ksm = reinterpret_cast<const float*>(smem + L::OFF_SC + ss * L::SC);
+      const float* b2m = ksm + BN;
+      const uint32_t flags = *reinterpret_cast<const volatile uint32_t*>(b2m + BN);
+      float x[BN];
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(tS + c0, rr);
+        tmem_wait_ld(rr);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[c0 + i] = __uint_as_float(rr[i]);
+      }
+      const bool fast = (flags & 1u) == 0;
+      float tmax;
+      if (fast) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < BN; c += 2) {
+          const float2 k2 = *reinterpret_cast<const float2*>(ksm + c);
+          const uint64_t u = fmul2(pack2(x[c], x[c + 1]), pack2(k2.x, k2.y));
+          unpack2(u, x[c], x[c + 1]);
+          mx = fmax3(mx, x[c], x[c + 1]);
+        }
+        tmax = cq * mx;
+      } else {
+        const bool keep = SPARSE ? ((flags >> (1 + half)) & 1u) != 0 : true;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < BN; c += 2) {
+          const float2 k2 = *reinterpret_cast<const float2*>(ksm + c);
+          const float2 bb = *reinterpret_cast<const float2*>(b2m + c);
+          const uint64_t u = fmul2(pack2(x[c], x[c + 1]), pack2(k2.x, k2.y));
+          const uint64_t t = ffma2(u, pack2(cq, cq), pack2(bb.x, bb.y));
+          unpack2(t, x[c], x[c + 1]);
+          if (!keep) x[c] = x[c + 1] = -INFINITY;
+          mx = fmax3(mx, x[c], x[c + 1]);
+        }
+        tmax = mx;
+      }
+      const float m_new = fmaxf(m, tmax);
+      const bool need = m_new > m + kRescaleLog2;
+      if (__any_sync(0xffffffffu, need)) {
+        const float alpha = need ? ex2(m - m_new) : 1.f;
+        if (it > 0) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t rr[32];
+            tmem_ld32(tO + c0, rr);
+            tmem_wait_ld(rr);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+            tmem_st32(tO + c0, rr);
+          }
+        }
+        l *= alpha;
+        if (need) m = m_new;
+      }
+      const float mref = (m == -INFINITY) ? 0.f : m;
+      const float k1 = fast ? cq : 1.f;
+      const uint64_t k1v = pack2(k1, k1);
+      const uint64_t nm = pack2(-mref, -mref);
+      uint64_t lsum = pack2(0.f, 0.f);
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 64) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c = c0 + 2 * i;
+          float t0, t1;
+          unpack2(ffma2(pack2(x[c], x[c + 1]), k1v, nm), t0, t1);
+          const float p0 = ex2(t0), p1 = ex2(t1);
+          lsum = fadd2(lsum, pack2(p0, p1));
+          pk[i] = VBF16 ? cvt_bf16x2(p0, p1) : cvt_f16x2(p0, p1);
+        }
+        tmem_st32(tS + c0 / 2, pk);
+      }
+      float la, lb;
+      unpack2(lsum, la, lb);
+      l += la + lb;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(L::B_PF + s));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::B_SCE + ss));
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && n_it > 0) ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_OF + s), 0, ctl, kErrSoftmax));
+    if (ok) {
+      tc_fence_after();
+      bool pad = false;
+      if (a.pad_query && row_ok) pad = (row & 63) >= __ldg(a.kv_valid + (row >> 6));
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      char* orow = static_cast<char*>(a.out) +
+                   (b * a.o_sb + h * a.o_sh + static_cast<int64_t>(row) * a.o_ss) * 2;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t rr[32];
+        if (n_it > 0) {
+          tmem_ld32(tO + c0, rr);
+          tmem_wait_ld(rr);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) rr[i] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float o0 = __uint_as_float(rr[2 * i]) * inv_l * vsc[c0 + 2 * i];
+          float o1 = __uint_as_float(rr[2 * i + 1]) * inv_l * vsc[c0 + 2 * i + 1];
+          if (pad) o0 = o1 = 0.f;
+          pk[i] = VBF16 ? cvt_bf16x2(o0, o1) : cvt_f16x2(o0, o1);
+        }
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0 * 2);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+      if (row_ok && a.lse != nullptr) {
+        const float lse = (pad || !(l > 0.f)) ? -INFINITY : (m + log2f(l)) * kLn2;
+        a.lse[b * a.l_sb + h * a.l_sh + row] = lse;
+      }
+    }
+  }
+
+  // ------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == L::W_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 4-D map over [B][H][S][D] (innermost first), strides in bytes.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int esize, int D, int S,
+              int H, int B, int64_t ss, int64_t sh, int64_t sb, int box0, int box1,
+              CUtensorMapSwizzle sw) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const int64_t es = esize;
+  int64_t s1 = ss * es, s2 = sh * es, s3 = sb * es;
+  if (H <= 1) s2 = s1 * (S > 0 ? S : 1);
+  if (B <= 1) s3 = s2 * (H > 0 ? H : 1);
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S > 0 ? S : 1),
+                        static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(s1), static_cast<cuuint64_t>(s2),
+                           static_cast<cuuint64_t>(s3)};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(box0), static_cast<cuuint32_t>(box1), 1, 1};
+  cuuint32_t est[4] = {1, 1, 1, 1};
+  const CUresult r = enc(m, dt, 4, const_cast<void*>(base), dims, strides, box, est,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D, int QS, int BN, bool SPARSE, bool VBF16>
+ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** msg) {
+  using L = Layout<D, QS, BN, SPARSE>;
+  const ia_attn_params& p = A.p;
+  CUtensorMap tq, tk, tv;
+  const bool okq = make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, A.q, 1, D, p.Sq, p.H, p.B,
+                            p.q_strides[2], p.q_strides[1], p.q_strides[0], D, kM,
+                            CU_TENSOR_MAP_SWIZZLE_NONE);
+  const bool okk = make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, A.k, 1, D, p.Sk, p.H, p.B,
+                            p.k_strides[2], p.k_strides[1], p.k_strides[0], D, BN,
+                            CU_TENSOR_MAP_SWIZZLE_NONE);
+  const bool okv = make_map(&tv, VBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                            A.v, 2, D, p.Sk, p.H, p.B, p.v_strides[2], p.v_strides[1],
+                            p.v_strides[0], 64, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!(okq && okk && okv)) {
+    *msg = "cuTensorMapEncodeTiled rejected a Q/K/V layout (alignment or stride)";
+    return IA_ERR_INVALID_ARG;
+  }
+  Params a{};
+  a.q_scale = A.q_scale;
+  a.k_scale = A.k_scale;
+  a.bias = A.bias;
+  a.mask = A.mask;
+  a.kv_valid = p.kv_valid;
+  a.v_scale = p.v_scale;
+  a.out = A.out;
+  a.lse = A.lse;
+  a.H = p.H;
+  a.Sq = p.Sq;
+  a.Sk = p.Sk;
+  a.Tq = (p.Sq + 63) / 64;
+  a.Tk = (p.Sk + 63) / 64;
+  a.n_tiles = SPARSE ? a.Tk : (p.Sk + BN - 1) / BN;
+  a.cq_mult = A.sm_scale * kLog2e;
+  a.gran_block = p.granularity == IA_PER_BLOCK64 ? 1 : 0;
+  a.pad_query = (p.kv_valid != nullptr && p.Sq == p.Sk) ? 1 : 0;
+  a.qs_sb = p.qs_strides[0];
+  a.qs_sh = p.qs_strides[1];
+  a.ks_sb = p.ks_strides[0];
+  a.ks_sh = p.ks_strides[1];
+  a.o_sb = p.o_strides[0];
+  a.o_sh = p.o_strides[1];
+  a.o_ss = p.o_strides[2];
+  a.l_sb = p.lse_strides[0];
+  a.l_sh = p.lse_strides[1];
+  a.timeout_ns = 2000000000ull;
+  const size_t smem = L::SMEM_FIXED + (SPARSE ? static_cast<size_t>(a.Tk) * 2 : 0);
+  auto kern = attn_fwd_kernel<D, QS, BN, SPARSE, VBF16>;
+  if (smem > 232448) {
+    *msg = "key-tile list does not fit in shared memory (too many key tiles)";
+    return IA_ERR_UNSUPPORTED;
+  }
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) {
+    *msg = cudaGetErrorString(e);
+    return IA_ERR_CUDA;
+  }
+  dim3 grid((p.Sq + kM * QS - 1) / (kM * QS), p.H, p.B);
+  kern<<<grid, L::NWARPS * 32, smem, st>>>(tq, tk, tv, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *msg = cudaGetErrorString(e);
+    return IA_ERR_CUDA;
+  }
+  (void)num_sms;
+  return IA_OK;
+}
+
+}  // namespace
+
+ia_status launch_attention(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** msg) {
+  const ia_attn_params& p = A.p;
+  if (p.B == 0 || p.H == 0 || p.Sq == 0) return IA_OK;
+  const bool bf = p.v_dtype == IA_BF16;
+  if (A.mask != nullptr) {
+    if (p.D == 128)
+      return bf ? run<128, 1, 64, true, true>(A, num_sms, st, msg)
+                : run<128, 1, 64, true, false>(A, num_sms, st, msg);
+    return bf ? run<64, 1, 64, true, true>(A, num_sms, st, msg)
+              : run<64, 1, 64, true, false>(A, num_sms, st, msg);
+  }
+  if (p.D == 128)
+    return bf ? run<128, 2, 128, false, true>(A, num_sms, st, msg)
+              : run<128, 2, 128, false, false>(A, num_sms, st, msg);
+  return bf ? run<64, 2, 128, false, true>(A, num_sms, st, msg)
+            : run<64, 2, 128, false, false>(A, num_sms, st, msg);
+}
+
+cudaError_t attention_read_device_error(unsigned int* out, cudaStream_t st) {
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(out, g_attn_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(unsigned int));
+}
+
+}  // namespace ia

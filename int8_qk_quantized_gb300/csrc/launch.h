@@ -1,0 +1,61 @@
+// Internal launchers behind the C ABI. Arguments are already validated.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/ia.h"
+
+namespace ia {
+
+struct QuantArgs {
+  const void* x;           // 16-bit input
+  int64_t sb, sh, ss;      // input strides (elements)
+  int B, H, S, D;
+  int dtype;               // IA_BF16 / IA_FP16
+  int gran_block;          // 1: one scale per 64-row block
+  int center;              // subtract the mean (K only)
+  const int32_t* valid;    // optional per-64-row valid counts
+  const float* mean_in;    // optional [B,H,D] mean to use
+  float* mean_out;         // optional [B,H,D] mean that was used
+  int8_t* codes;           // [B,H,S,D] contiguous
+  float* scales;           // [B,H,S] or [B,H,ceil(S/64)] contiguous
+};
+
+cudaError_t launch_quantize(const QuantArgs& a, int num_sms, cudaStream_t st);
+
+struct MergeArgs {
+  const void* o1;
+  const float* l1;
+  const void* o2;
+  const float* l2;
+  void* o;
+  float* l;
+  int64_t rows;  // B*H*Sq
+  int D;
+  int dtype;
+};
+
+cudaError_t launch_merge(const MergeArgs& a, int num_sms, cudaStream_t st);
+
+struct AttnLaunch {
+  const int8_t* q;
+  const int8_t* k;
+  const float* q_scale;
+  const float* k_scale;
+  const void* v;
+  const float* bias;
+  const uint8_t* mask;
+  void* out;
+  float* lse;
+  ia_attn_params p;
+  float sm_scale;
+};
+
+// Returns IA_OK or an error status; message via the C ABI's error slot.
+ia_status launch_attention(const AttnLaunch& a, int num_sms, cudaStream_t st, const char** msg);
+
+// Reads (and clears) the attention kernel's device status word.
+cudaError_t attention_read_device_error(unsigned int* out, cudaStream_t st);
+
+}  // namespace ia

@@ -1,0 +1,117 @@
+// Exact merge of two partial attentions over disjoint key sets through their
+// log-sum-exps: "int8_attention: masked path costs ~1.8x unmasked, and a
+// request for optional return_lse", Question 2 (core + skirt calls merged
+// exactly), and "Add optional forward LSE output", Kernel implementation
+// (the split-K combine's LSE comes from the combined maximum and denominator).
+//
+//   M = max(L1, L2); w_k = exp(L_k - M); L = M + ln(w1 + w2)
+//   O = (w1*O1 + w2*O2) / (w1 + w2);   M = -inf gives O = 0, L = -inf.
+//
+// A streaming kernel: each row is D/8 threads holding 8 elements (16 bytes) of
+// O1, O2 and O, with FP32 arithmetic.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "launch.h"
+
+namespace ia {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <int DT>
+__device__ __forceinline__ void unpack8(const uint4 w, float (&v)[8]) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (DT == IA_BF16) {
+      v[2 * i] = __uint_as_float(u[i] << 16);
+      v[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+    } else {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
+  uint32_t u[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (DT == IA_BF16) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+      u[i] = *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+      const __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+      u[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+  }
+  return make_uint4(u[0], u[1], u[2], u[3]);
+}
+
+template <int D, int DT>
+__global__ void __launch_bounds__(kThreads) merge_kernel(const MergeArgs a) {
+  constexpr int TPR = D / 8;
+  constexpr int RPP = kThreads / TPR;
+  const int tc = threadIdx.x % TPR;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * RPP;
+  // Uniform trip count per CTA, so the warp barrier below is reached by all lanes.
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPP; base < a.rows; base += stride) {
+    const int64_t r = base + threadIdx.x / TPR;
+    const bool live = r < a.rows;
+    const int64_t rr = live ? r : 0;
+    const float l1 = a.l1[rr];
+    const float l2 = a.l2[rr];
+    const int64_t off = rr * D + tc * 8;
+    const uint4 w1 = *reinterpret_cast<const uint4*>(static_cast<const char*>(a.o1) + off * 2);
+    const uint4 w2 = *reinterpret_cast<const uint4*>(static_cast<const char*>(a.o2) + off * 2);
+    // Every lane of a row has read its inputs before any lane writes (outputs may alias).
+    __syncwarp();
+    if (!live) continue;
+    const float m = fmaxf(l1, l2);
+    float o[8];
+    float lse;
+    if (m == -INFINITY) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = 0.f;
+      lse = -INFINITY;
+    } else {
+      const float e1 = expf(l1 - m);  // exp(-inf) = 0 for an empty partial
+      const float e2 = expf(l2 - m);
+      const float den = e1 + e2;
+      const float c1 = e1 / den, c2 = e2 / den;
+      float x1[8], x2[8];
+      unpack8<DT>(w1, x1);
+      unpack8<DT>(w2, x2);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = c1 * x1[i] + c2 * x2[i];
+      lse = m + logf(den);
+    }
+    *reinterpret_cast<uint4*>(static_cast<char*>(a.o) + off * 2) = pack8<DT>(o);
+    if (a.l && tc == 0) a.l[r] = lse;
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const MergeArgs& a, int num_sms, cudaStream_t st) {
+  constexpr int RPP = kThreads / (D / 8);
+  int64_t blocks = (a.rows + RPP - 1) / RPP;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (a.dtype == IA_BF16)
+    merge_kernel<D, IA_BF16><<<static_cast<int>(blocks), kThreads, 0, st>>>(a);
+  else
+    merge_kernel<D, IA_FP16><<<static_cast<int>(blocks), kThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const MergeArgs& a, int num_sms, cudaStream_t st) {
+  if (a.rows == 0) return cudaSuccess;
+  return a.D == 128 ? launch_d<128>(a, num_sms, st) : launch_d<64>(a, num_sms, st);
+}
+
+}  // namespace ia

@@ -1,0 +1,294 @@
+// K mean and symmetric INT8 quantisation of Q and K.
+//
+// "minimax_h3_sparse_int8" (FastVideo API page): per-token scales, K centred by
+// its mean over the sequence (sum divided by the number of valid rows), codes
+// int8 [B,H,S,D], scales fp32 [B,H,S]. "Feature Request: Direct int8 Q/K
+// passthrough between Comfy Kitchen and SageAttention", 3.1: per-block
+// scales. "[attention-int8] Multiple build issues and numerical accuracy
+// problem", maintainer's point 1: symmetric range [-127, 127].
+//
+// One kernel handles a head's rows in chunks. For K with centring, the CTAs
+// of one head form a thread-block cluster: each CTA sums its chunk's columns
+// with error-free two-sum transformations in FP32 (a hi/lo pair per column,
+// exact whenever the float64 sum is), the partials are combined in FP64 in a
+// fixed order through distributed shared memory, and every CTA of the cluster
+// then quantises its own chunk with the same mean. No scratch memory is used.
+// The quantiser itself uses correctly rounded FP32 division, multiplication
+// and round-half-even, so codes and scales are reproducible bit for bit.
+#include <cooperative_groups.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "launch.h"
+
+namespace cg = cooperative_groups;
+
+namespace ia {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTile = 64;
+
+template <int DT>
+__device__ __forceinline__ void load8(const void* p, float (&v)[8]) {
+  const uint4 w = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (DT == IA_BF16) {
+      v[2 * i] = __uint_as_float(u[i] << 16);
+      v[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+    } else {
+      const __half2 h = *reinterpret_cast<const __half2*>(&u[i]);
+      const float2 f = __half22float2(h);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+}
+
+__device__ __forceinline__ bool row_valid(const int32_t* valid, int r) {
+  return valid == nullptr || (r % kTile) < __ldg(valid + r / kTile);
+}
+
+// Error-free accumulation: (hi, lo) += x with hi + lo exact when it fits.
+__device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float x) {
+  const float s = __fadd_rn(hi, x);
+  const float bp = __fsub_rn(s, hi);
+  const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(x, bp));
+  hi = s;
+  lo = __fadd_rn(lo, err);
+}
+
+__device__ __forceinline__ int8_t code_of(float x, float inv) {
+  int c = __float2int_rn(__fmul_rn(x, inv));
+  c = c > 127 ? 127 : (c < -127 ? -127 : c);
+  return static_cast<int8_t>(c);
+}
+
+__device__ __forceinline__ void store_codes(int8_t* dst, const float (&x)[8], float inv) {
+  uint32_t w[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t acc = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      acc |= (static_cast<uint32_t>(static_cast<uint8_t>(code_of(x[4 * h + i], inv))) << (8 * i));
+    w[h] = acc;
+  }
+  *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+}
+
+// grid: (chunks, H, B). Chunk c holds rows [c*chunk, min(S, (c+1)*chunk)).
+// With CLUSTER_MEAN the chunks of one head are one cluster and compute the mean.
+template <int D, int DT, bool CLUSTER_MEAN>
+__global__ void __launch_bounds__(kThreads) quantize_kernel(const QuantArgs a, int chunk) {
+  constexpr int TPR = D / 8;            // threads per row, 8 elements each
+  constexpr int RPP = kThreads / TPR;   // rows per pass
+  static_assert(RPP * TPR == kThreads, "layout");
+  __shared__ float s_mu[D];
+  __shared__ double s_red[CLUSTER_MEAN ? RPP : 1][CLUSTER_MEAN ? D : 1];
+  __shared__ double s_part[CLUSTER_MEAN ? D : 1];
+  __shared__ float s_wmax[kThreads / 32];
+  __shared__ int s_count;
+
+  const int tid = threadIdx.x;
+  const int tr = tid / TPR;
+  const int tc = tid % TPR;
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int r0 = blockIdx.x * chunk;
+  const int r1 = min(a.S, r0 + chunk);
+  const char* xb = static_cast<const char*>(a.x) + (static_cast<int64_t>(b) * a.sb +
+                                                    static_cast<int64_t>(h) * a.sh) * 2;
+  const int64_t bh = static_cast<int64_t>(b) * a.H + h;
+
+  // ---------------------------------------------------------------- mean
+  if (a.center) {
+    if (CLUSTER_MEAN) {
+      float hi[8], lo[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) hi[i] = lo[i] = 0.f;
+      for (int base = r0; base < r1; base += 4 * RPP) {
+        float v[4][8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int rr = base + u * RPP + tr;
+          if (rr < r1 && row_valid(a.valid, rr)) {
+            load8<DT>(xb + (static_cast<int64_t>(rr) * a.ss + tc * 8) * 2, v[u]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[u][i] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) two_sum_acc(hi[i], lo[i], v[u][i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        s_red[tr][tc * 8 + i] = static_cast<double>(hi[i]) + static_cast<double>(lo[i]);
+      if (tid == 0) {
+        int n = a.S;
+        if (a.valid) {
+          n = 0;
+          for (int t = 0; t < a.S / kTile; ++t) n += __ldg(a.valid + t);
+        }
+        s_count = n;
+      }
+      __syncthreads();
+      if (tid < D) {
+        double s = 0.0;
+        for (int j = 0; j < RPP; ++j) s += s_red[j][tid];
+        s_part[tid] = s;
+      }
+      cg::cluster_group cluster = cg::this_cluster();
+      cluster.sync();
+      if (tid < D) {
+        double tot = 0.0;
+        const int nr = static_cast<int>(cluster.num_blocks());
+        for (int rk = 0; rk < nr; ++rk) tot += *cluster.map_shared_rank(&s_part[tid], rk);
+        const int n = s_count > 0 ? s_count : 1;
+        s_mu[tid] = static_cast<float>(tot / static_cast<double>(n));
+        if (a.mean_out && cluster.block_rank() == 0) a.mean_out[bh * D + tid] = s_mu[tid];
+      }
+      cluster.sync();  // no CTA leaves while another still reads its partials
+    } else {
+      if (tid < D) {
+        s_mu[tid] = __ldg(a.mean_in + bh * D + tid);
+        if (a.mean_out && blockIdx.x == 0) a.mean_out[bh * D + tid] = s_mu[tid];
+      }
+      __syncthreads();
+    }
+  }
+  float mu[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mu[i] = a.center ? s_mu[tc * 8 + i] : 0.f;
+
+  int8_t* cb = a.codes + bh * static_cast<int64_t>(a.S) * D;
+  // ------------------------------------------------------ per-token codes
+  if (!a.gran_block) {
+    float* sc = a.scales + bh * a.S;
+    // The loop bound is uniform across the CTA: every lane reaches the shuffles.
+    for (int base = r0; base < r1; base += 2 * RPP) {
+      float v[2][8];
+      bool ok[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int rr = base + u * RPP + tr;
+        ok[u] = rr < r1 && row_valid(a.valid, rr);
+        if (ok[u]) {
+          load8<DT>(xb + (static_cast<int64_t>(rr) * a.ss + tc * 8) * 2, v[u]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[u][i] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int rr = base + u * RPP + tr;
+        float m = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (a.center && ok[u]) v[u][i] = __fsub_rn(v[u][i], mu[i]);
+          m = fmaxf(m, fabsf(v[u][i]));
+        }
+#pragma unroll
+        for (int off = TPR / 2; off > 0; off >>= 1)
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if (rr < r1) {
+          const float scale = m > 0.f ? __fdiv_rn(m, 127.f) : 0.f;
+          const float inv = m > 0.f ? __fdiv_rn(127.f, m) : 0.f;
+          store_codes(cb + static_cast<int64_t>(rr) * D + tc * 8, v[u], inv);
+          if (tc == 0) sc[rr] = ok[u] ? scale : 0.f;
+        }
+      }
+    }
+    return;
+  }
+  // ---------------------------------------------------- per-64-block codes
+  constexpr int PPB = kTile / RPP;  // passes per block
+  float* sc = a.scales + bh * ((a.S + kTile - 1) / kTile);
+  for (int blk0 = r0; blk0 < r1; blk0 += kTile) {
+    float v[PPB][8];
+    float m = 0.f;
+#pragma unroll
+    for (int p = 0; p < PPB; ++p) {
+      const int rr = blk0 + p * RPP + tr;
+      if (rr < r1 && row_valid(a.valid, rr)) {
+        load8<DT>(xb + (static_cast<int64_t>(rr) * a.ss + tc * 8) * 2, v[p]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[p][i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (a.center && rr < r1 && row_valid(a.valid, rr)) v[p][i] = __fsub_rn(v[p][i], mu[i]);
+        m = fmaxf(m, fabsf(v[p][i]));
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((tid & 31) == 0) s_wmax[tid / 32] = m;
+    __syncthreads();
+    m = 0.f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) m = fmaxf(m, s_wmax[w]);
+    __syncthreads();
+    const float scale = m > 0.f ? __fdiv_rn(m, 127.f) : 0.f;
+    const float inv = m > 0.f ? __fdiv_rn(127.f, m) : 0.f;
+#pragma unroll
+    for (int p = 0; p < PPB; ++p) {
+      const int rr = blk0 + p * RPP + tr;
+      if (rr < r1) store_codes(cb + static_cast<int64_t>(rr) * D + tc * 8, v[p], inv);
+    }
+    if (tid == 0) sc[blk0 / kTile] = scale;
+  }
+}
+
+template <int D, int DT>
+cudaError_t launch_typed(const QuantArgs& a, int num_sms, cudaStream_t st) {
+  const int BH = a.B * a.H;
+  if (a.center && a.mean_in == nullptr) {
+    // One cluster per head; enough CTAs to cover the SMs about twice.
+    int cl = (2 * num_sms + BH - 1) / BH;
+    cl = cl < 1 ? 1 : (cl > 8 ? 8 : cl);
+    const int max_chunks = (a.S + kTile - 1) / kTile;
+    if (cl > max_chunks) cl = max_chunks;
+    int chunk = (a.S + cl - 1) / cl;
+    chunk = (chunk + kTile - 1) / kTile * kTile;
+    cl = (a.S + chunk - 1) / chunk;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cl, a.H, a.B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quantize_kernel<D, DT, true>, a, chunk);
+  }
+  // Rows split into chunks of 256 (a multiple of 64); no cluster.
+  const int chunk = 256;
+  dim3 grid((a.S + chunk - 1) / chunk, a.H, a.B);
+  quantize_kernel<D, DT, false><<<grid, kThreads, 0, st>>>(a, chunk);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const QuantArgs& a, int num_sms, cudaStream_t st) {
+  if (a.S == 0 || a.B == 0 || a.H == 0) return cudaSuccess;
+  if (a.D == 128) {
+    return a.dtype == IA_BF16 ? launch_typed<128, IA_BF16>(a, num_sms, st)
+                              : launch_typed<128, IA_FP16>(a, num_sms, st);
+  }
+  return a.dtype == IA_BF16 ? launch_typed<64, IA_BF16>(a, num_sms, st)
+                            : launch_typed<64, IA_FP16>(a, num_sms, st);
+}
+
+}  // namespace ia
