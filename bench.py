@@ -1,0 +1,391 @@
+"""Benchmark of the INT8-QK attention path on GB300.
+
+One step = the whole path once on the banded cross-window workload
+(B1 H56 Q4096 K33600 D128, bf16, per-key raised-cosine skirt bias):
+  1. K mean + INT8 quantisation of Q and K          (2 launches)
+  2. core keys [6720, 26880) without bias, with LSE (1 launch)
+  3. left and right skirt keys with the bias, LSE   (2 launches, key sub-range views)
+  4. two exact LSE merges                           (2 launches)
+value = 4*B*H*Q*K*D / step time (TOPS). The single unmasked call and the
+single bias call over all keys are timed too (their ratio is the bias cost).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun each rank runs its own copy of the workload on its GPU (the
+heads are independent; no collective on the data path), rank 0 prints one
+JSON line. ``--impl reference`` times the CPU oracle on the host cores on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention TOPS and ms per call at 4096x33600x56x128 (unmasked/bias); % of roofline"
+UNIT = "TOPS"
+# comfy-kitchen issue #177, RTX 5090: core 20160 keys unmasked 5.19 ms + skirt
+# 13440 keys masked 5.86 ms = 11.05 ms for the same 4096x33600x56x128 problem.
+PAGE_SPLIT_MS = 11.05
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def start_clock_sampler():
+    try:
+        return subprocess.Popen(
+            ["nvidia-smi", "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap", "--format=csv,noheader,nounits", "-lms", "200"],
+            stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+    except Exception:
+        return None
+
+
+def stop_clock_sampler(proc, gpu_index):
+    if proc is None:
+        return None
+    proc.terminate()
+    try:
+        out, _ = proc.communicate(timeout=5)
+    except Exception:
+        proc.kill()
+        out = ""
+    sm, mx, reasons = [], None, set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in out.strip().splitlines():
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 9 or f[0] != str(gpu_index):
+            continue
+        try:
+            sm.append(float(f[1]))
+            mx = float(f[2])
+        except ValueError:
+            continue
+        for n, v in zip(names, f[5:9]):
+            if v.lower() == "active":
+                reasons.add(n)
+    if not sm:
+        return None
+    loaded = [s for s in sm if mx is None or s > 0.5 * mx] or sm
+    return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+def run_reference(args):
+    """The CPU oracle, timed on the host cores on a bounded sample per step."""
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    import oracle
+    from workloads import WORKLOADS, make_inputs
+
+    wl = WORKLOADS["banded"]
+    sample_heads, sample_rows = 1, 256
+    small = wl.with_(H=sample_heads)
+    inp = make_inputs(small, "cpu")
+    qn = inp.q.float().numpy()[:, :, :sample_rows]
+    kn = inp.k.float().numpy()
+    vn = inp.v.float().numpy()
+    bias = inp.bias.numpy()
+
+    def step():
+        oracle.quantize_and_attend(qn, kn, vn, bias=bias)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    ops = 4.0 * sample_heads * sample_rows * wl.Sk * wl.D
+    val = ops / dt / 1e12
+    cores = os.cpu_count()
+    sample = (f"{sample_heads} head x {sample_rows} query rows x {wl.Sk} keys per step: K mean "
+              f"+ quantise + same-quantisation fp64 attention with the skirt bias")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "banded cross-window attention B1 H56 Q4096 K33600 D128 bf16, "
+                              "per-key skirt bias", "sample": sample},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def cpu_baseline(seconds_target=12.0):
+    """The oracle as it stands on a bounded sample of the workload (host cores)."""
+    import numpy as np
+
+    import oracle
+    from workloads import WORKLOADS, make_inputs
+
+    wl = WORKLOADS["banded"].with_(H=1)
+    inp = make_inputs(wl, "cpu")
+    qn = inp.q.float().numpy()
+    kn = inp.k.float().numpy()
+    vn = inp.v.float().numpy()
+    bias = inp.bias.numpy()
+    rows = 512
+    t0 = time.perf_counter()
+    n = 0
+    total_rows = 0
+    while time.perf_counter() - t0 < seconds_target and n < 64:
+        oracle.quantize_and_attend(qn[:, :, :rows], kn, vn, bias=bias)
+        total_rows += rows
+        n += 1
+    dt = time.perf_counter() - t0
+    ops = 4.0 * total_rows * wl.Sk * wl.D
+    return {"value": ops / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} runs of 1 head x {rows} query rows x {wl.Sk} keys (K mean + "
+                      f"quantise + fp64 attention with bias) in {dt:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+
+    ws, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import int8_qk_quantized_gb300 as ia
+    from workloads import WORKLOADS, algorithmic_ops, make_inputs
+
+    wl = WORKLOADS["banded"]
+    B, H, Sq, Sk, D = wl.B, wl.H, wl.Sq, wl.Sk, wl.D
+    lo, hi = wl.skirt_width, Sk - wl.skirt_width
+    dev = torch.device("cuda", local)
+    inp = make_inputs(wl, dev)
+    q, k, v, bias = inp.q, inp.k, inp.v, inp.bias
+    stream = torch.cuda.current_stream()
+
+    # preallocated outputs: the step allocates nothing
+    q8 = torch.empty(B, H, Sq, D, dtype=torch.int8, device=dev)
+    k8 = torch.empty(B, H, Sk, D, dtype=torch.int8, device=dev)
+    qs = torch.empty(B, H, Sq, device=dev)
+    ks = torch.empty(B, H, Sk, device=dev)
+    o_core = torch.empty(B, H, Sq, D, dtype=q.dtype, device=dev)
+    o_l = torch.empty_like(o_core)
+    o_r = torch.empty_like(o_core)
+    l_core = torch.empty(B, H, Sq, device=dev)
+    l_l = torch.empty_like(l_core)
+    l_r = torch.empty_like(l_core)
+    o_full = torch.empty_like(o_core)
+    l_full = torch.empty_like(l_core)
+
+    L = ia.load_library()
+    import ctypes
+
+    def quantize():
+        st = (ctypes.c_int64 * 3)(*q.stride()[:3])
+        sk = (ctypes.c_int64 * 3)(*k.stride()[:3])
+        ia._check(L.ia_quantize_qk(ia._ptr(q), ia._ptr(k), ia.BF16, B, H, Sq, Sk, D, st, sk,
+                                   ia.PER_TOKEN, 1, None, None, ia._ptr(q8), ia._ptr(k8),
+                                   ia._ptr(qs), ia._ptr(ks), None, ia._stream(stream)))
+
+    def attn(a, b_, bias_t, out, lse):
+        ia.attention(q8, k8[:, :, a:b_], qs, ks[:, :, a:b_], v[:, :, a:b_], bias=bias_t,
+                     out=out, lse=lse, return_lse=True, stream=stream)
+
+    att_events = []
+
+    def step(record=False):
+        quantize()
+        for (a, b_, bt, o_, l_) in ((lo, hi, None, o_core, l_core),
+                                    (0, lo, bias[:lo], o_l, l_l),
+                                    (hi, Sk, bias[hi:], o_r, l_r)):
+            if record:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            attn(a, b_, bt, o_, l_)
+            if record:
+                e1.record(stream)
+                att_events.append((e0, e1, 4.0 * B * H * Sq * (b_ - a) * D))
+        ia.merge_lse(o_core, l_core, o_l, l_l, out=o_core, lse_out=l_core, stream=stream)
+        ia.merge_lse(o_core, l_core, o_r, l_r, out=o_core, lse_out=l_core, stream=stream)
+
+    launches_per_step = 2 + 3 + 2
+
+    for _ in range(args.warmup):
+        step()
+    ia.device_status()
+
+    sampler = start_clock_sampler() if rank == 0 else None
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    clocks = stop_clock_sampler(sampler, local)
+    ia.device_status()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    att_ms = sum(e0.elapsed_time(e1) for e0, e1, _ in att_events)
+    att_ops = sum(o for _, _, o in att_events)
+    if pg:
+        t = torch.tensor([elapsed_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        elapsed_ms = t.item()
+    ms_per_step = elapsed_ms / args.steps
+    ops = algorithmic_ops(wl)
+    value = ws * ops / (ms_per_step * 1e-3) / 1e12
+
+    # single calls over all keys: unmasked and with the bias
+    def time_call(fn, n=20):
+        for _ in range(3):
+            fn()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    unmasked_ms = time_call(lambda: ia.attention(q8, k8, qs, ks, v, out=o_full, lse=l_full,
+                                                 return_lse=True, stream=stream))
+    bias_ms = time_call(lambda: ia.attention(q8, k8, qs, ks, v, bias=bias, out=o_full,
+                                             lse=l_full, return_lse=True, stream=stream))
+    quant_ms = time_call(quantize)
+    merge_ms = time_call(lambda: ia.merge_lse(o_l, l_l, o_r, l_r, out=o_full, lse_out=l_full,
+                                              stream=stream))
+    ia.device_status()
+
+    # end to end: pinned host inputs -> device -> step -> host outputs
+    hq = q.cpu().pin_memory()
+    hk = k.cpu().pin_memory()
+    hv = v.cpu().pin_memory()
+    hb = bias.cpu().pin_memory()
+    ho = torch.empty(o_core.shape, dtype=o_core.dtype).pin_memory()
+    hl = torch.empty(l_core.shape, dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hb))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * 4
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        bias.copy_(hb, non_blocking=True)
+        step()
+        ho.copy_(o_core, non_blocking=True)
+        hl.copy_(l_core, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = t.item()
+    ia.device_status()
+
+    hbm, bf16, bf16_sus, peak_kind = peaks()
+    achieved = att_ops / (att_ms * 1e-3) / 1e12
+    quant_bytes = B * H * (Sq + Sk) * D * (2 + 1) + B * H * (Sq + Sk) * 4 + B * H * Sk * D * 2
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+    cpu = None if args.no_cpu_baseline else cpu_baseline()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": value / (ops / (PAGE_SPLIT_MS * 1e-3) / 1e12),
+        "vs_baseline_ref": "RTX 5090 core+skirt split of the same problem, 11.05 ms "
+                           "(comfy-kitchen issue #177); another machine: context only",
+        "dtype": "int8 QK (exact, fp16-coded MMA) / bf16 PV, fp32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": "banded cross-window attention B1 H56 Q4096 K33600 D128 bf16: "
+                               "quantise Q/K, core 20160 keys unmasked + two 6720-key skirts "
+                               "with the per-key raised-cosine bias, LSE merges",
+                   "B": B, "H": H, "Sq": Sq, "Sk": Sk, "D": D,
+                   "l2": "no flush: inputs (q+k+v = 1.02 GB) are larger than L2"},
+        "calls_ms": {"unmasked_all_keys": unmasked_ms, "bias_all_keys": bias_ms,
+                     "bias_over_unmasked": bias_ms / unmasked_ms, "quantize_qk": quant_ms,
+                     "merge_lse": merge_ms,
+                     "unmasked_tops": ops / (unmasked_ms * 1e-3) / 1e12,
+                     "bias_tops": ops / (bias_ms * 1e-3) / 1e12,
+                     "quantize_gbs": quant_bytes / (quant_ms * 1e-3) / 1e9},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
+                     "frac": achieved / bf16, "traffic": None,
+                     "kernel": "attn_fwd_kernel (QS=2, BN=128, D=128)",
+                     "peak_source": f"{peak_kind} bf16 dense burst (MEASURED_PEAKS.json)",
+                     "frac_of_sustained": achieved / bf16_sus if bf16_sus else None},
+        "e2e": {"value": ws * ops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
