@@ -169,6 +169,49 @@ def cpu_baseline(seconds_target=12.0):
                       f"quantise + fp64 attention with bias) in {dt:.1f} s"}
 
 
+def run_profile(args):
+    """One kernel alone on a (possibly smaller) copy of its workload, for ncu."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import int8_qk_quantized_gb300 as ia
+    from workloads import WORKLOADS, make_inputs
+
+    name = args.profile
+    wl = WORKLOADS["sparse" if name == "sparse" else "banded"]
+    if args.heads:
+        wl = wl.with_(H=args.heads)
+    inp = make_inputs(wl, "cuda")
+    q8, qs, k8, ks = ia.quantize_qk(inp.q, inp.k, kv_valid=inp.kv_valid)
+    out, lse = ia.attention(q8, k8, qs, ks, inp.v, block_mask=inp.block_mask,
+                            kv_valid=inp.kv_valid, return_lse=True)
+    o2, l2 = out.clone(), lse.clone()
+    fns = {
+        "attention": lambda: ia.attention(q8, k8, qs, ks, inp.v, out=out, lse=lse, return_lse=True),
+        "attention_bias": lambda: ia.attention(q8, k8, qs, ks, inp.v, bias=inp.bias, out=out,
+                                               lse=lse, return_lse=True),
+        "quantize": lambda: ia.quantize_qk(inp.q, inp.k),
+        "merge": lambda: ia.merge_lse(out, lse, o2, l2, out=o2, lse_out=l2),
+        "sparse": lambda: ia.attention(q8, k8, qs, ks, inp.v, block_mask=inp.block_mask,
+                                       kv_valid=inp.kv_valid, out=out, lse=lse, return_lse=True),
+    }
+    fn = fns[name]
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    ia.device_status()
+    print(json.dumps({"profile": name, "workload": wl.name, "H": wl.H,
+                      "ms_per_call": e0.elapsed_time(e1) / args.steps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -176,10 +219,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", default=None,
+                    choices=["attention", "attention_bias", "quantize", "merge", "sparse"],
+                    help="run one kernel alone, --steps times after --warmup (for ncu)")
+    ap.add_argument("--heads", type=int, default=None, help="heads of the --profile case")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.profile:
+        run_profile(args)
         return
 
     import torch

@@ -128,8 +128,8 @@ struct Ctl {
 // Bounded wait on an mbarrier phase. Returns false when the wait ran out here
 // (the status word and the CTA's abort flag are set) or another thread of
 // the CTA has already aborted.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c, unsigned code) {
-  if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, const Ctl& c,
+                                           unsigned code) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -144,6 +144,12 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& 
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c,
+                                         unsigned code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bar_slow(bar, parity, c, code);
 }
 
 // Bounded wait that ignores the abort flag: used to let copies and MMAs that
@@ -400,18 +406,40 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), 1)
     const float* ksb = a.k_scale + b * a.ks_sb + h * a.ks_sh;
     for (int it = 0; it < n_it && ok; ++it) {
       const int kt = SPARSE ? static_cast<int>(list[it]) : it;
-      // per-key softmax constants of this tile
+      // Per-key constants of this tile: the global loads are issued first and
+      // land while the K tile is widened.
+      constexpr int KPT = (BN + 63) / 64;  // keys per converter thread
+      float kv[KPT], bv[KPT];
+#pragma unroll
+      for (int e = 0; e < KPT; ++e) {
+        const int key = kt * BN + ct + 64 * e;
+        const bool valid = key < a.Sk && (a.kv_valid == nullptr || (key & 63) < __ldg(a.kv_valid + (key >> 6)));
+        kv[e] = valid ? __ldg(ksb + (a.gran_block ? (key >> 6) : key)) : 0.f;
+        bv[e] = valid ? (a.bias ? __ldg(a.bias + key) * kLog2e : 0.f) : -INFINITY;
+      }
+      // K tile: int8 -> fp16 codes in the swizzled layout the MMA reads
+      const int rs = it % L::NRS, kst = it % L::NKS;
+      ok = wait_bar(bar(L::B_KRF + rs), (it / L::NRS) & 1, ctl, kErrConverter);
+      if (!ok) break;
+      if (it >= L::NKS) ok = wait_bar(bar(L::B_KCE + kst), ((it / L::NKS) - 1) & 1, ctl, kErrConverter);
+      if (!ok) break;
+      widen_tile<D>(smem + L::OFF_KR + rs * L::KR, smem + L::OFF_KH + kst * L::KH, BN, ct);
+      fence_proxy_async_smem();
+      mbar_arrive(bar(L::B_KCF + kst));
+      mbar_arrive(bar(L::B_KRE + rs));
+      // k scales, bias * log2(e) (-inf past the valid keys) and tile flags
       const int ss = it % L::NSC;
       if (it >= L::NSC) ok = wait_bar(bar(L::B_SCE + ss), ((it / L::NSC) - 1) & 1, ctl, kErrConverter);
       if (!ok) break;
       float* ksm = reinterpret_cast<float*>(smem + L::OFF_SC + ss * L::SC);
       float* b2m = ksm + BN;
       uint32_t* flg = reinterpret_cast<uint32_t*>(b2m + BN);
-      for (int c = ct; c < BN; c += 64) {
-        const int key = kt * BN + c;
-        const bool valid = key < a.Sk && (a.kv_valid == nullptr || (key & 63) < __ldg(a.kv_valid + (key >> 6)));
-        ksm[c] = valid ? __ldg(ksb + (a.gran_block ? (key >> 6) : key)) : 0.f;
-        b2m[c] = valid ? (a.bias ? __ldg(a.bias + key) * kLog2e : 0.f) : -INFINITY;
+#pragma unroll
+      for (int e = 0; e < KPT; ++e) {
+        if (ct + 64 * e < BN) {
+          ksm[ct + 64 * e] = kv[e];
+          b2m[ct + 64 * e] = bv[e];
+        }
       }
       if (ct == 0) {
         bool partial = kt * BN + BN > a.Sk;
@@ -430,16 +458,6 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), 1)
         *flg = f;
       }
       mbar_arrive(bar(L::B_SCF + ss));
-      // K tile
-      const int rs = it % L::NRS, kst = it % L::NKS;
-      ok = wait_bar(bar(L::B_KRF + rs), (it / L::NRS) & 1, ctl, kErrConverter);
-      if (!ok) break;
-      if (it >= L::NKS) ok = wait_bar(bar(L::B_KCE + kst), ((it / L::NKS) - 1) & 1, ctl, kErrConverter);
-      if (!ok) break;
-      widen_tile<D>(smem + L::OFF_KR + rs * L::KR, smem + L::OFF_KH + kst * L::KH, BN, ct);
-      fence_proxy_async_smem();
-      mbar_arrive(bar(L::B_KCF + kst));
-      mbar_arrive(bar(L::B_KRE + rs));
     }
   } else {
     // ------------------------------------------------------------- softmax
@@ -467,42 +485,69 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), 1)
       const float* ksm = reinterpret_cast<const float*>(smem + L::OFF_SC + ss * L::SC);
       const float* b2m = ksm + BN;
       const uint32_t flags = *reinterpret_cast<const volatile uint32_t*>(b2m + BN);
-      float x[BN];
-#pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(tS + c0, rr);
-        tmem_wait_ld(rr);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[c0 + i] = __uint_as_float(rr[i]);
-      }
       const bool fast = (flags & 1u) == 0;
-      float tmax;
-      if (fast) {
-        float mx = -INFINITY;
+      const bool keep = SPARSE ? ((flags >> (1 + half)) & 1u) != 0 : true;
+      const uint64_t cq2 = pack2(cq, cq);
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // Pass 1 over 32-column chunks of S: u = acc * k_scale (fast tiles) or
+      // t = u * cq + bias*log2e / -inf (masked tiles), the row maximum, and u
+      // written back in place.
+      auto pass1 = [&](uint32_t (&r)[32], int c0) {
+        if (fast) {
 #pragma unroll
-        for (int c = 0; c < BN; c += 2) {
-          const float2 k2 = *reinterpret_cast<const float2*>(ksm + c);
-          const uint64_t u = fmul2(pack2(x[c], x[c + 1]), pack2(k2.x, k2.y));
-          unpack2(u, x[c], x[c + 1]);
-          mx = fmax3(mx, x[c], x[c + 1]);
-        }
-        tmax = cq * mx;
-      } else {
-        const bool keep = SPARSE ? ((flags >> (1 + half)) & 1u) != 0 : true;
-        float mx = -INFINITY;
+          for (int j = 0; j < 32; j += 8) {
+            const float4 ka = *reinterpret_cast<const float4*>(ksm + c0 + j);
+            const float4 kb = *reinterpret_cast<const float4*>(ksm + c0 + j + 4);
+            const uint64_t u0 = fmul2(pack2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), pack2(ka.x, ka.y));
+            const uint64_t u1 = fmul2(pack2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])), pack2(ka.z, ka.w));
+            const uint64_t u2 = fmul2(pack2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])), pack2(kb.x, kb.y));
+            const uint64_t u3 = fmul2(pack2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])), pack2(kb.z, kb.w));
+            float f[8];
+            unpack2(u0, f[0], f[1]);
+            unpack2(u1, f[2], f[3]);
+            unpack2(u2, f[4], f[5]);
+            unpack2(u3, f[6], f[7]);
 #pragma unroll
-        for (int c = 0; c < BN; c += 2) {
-          const float2 k2 = *reinterpret_cast<const float2*>(ksm + c);
-          const float2 bb = *reinterpret_cast<const float2*>(b2m + c);
-          const uint64_t u = fmul2(pack2(x[c], x[c + 1]), pack2(k2.x, k2.y));
-          const uint64_t t = ffma2(u, pack2(cq, cq), pack2(bb.x, bb.y));
-          unpack2(t, x[c], x[c + 1]);
-          if (!keep) x[c] = x[c + 1] = -INFINITY;
-          mx = fmax3(mx, x[c], x[c + 1]);
+            for (int q = 0; q < 4; ++q) mx[q] = fmax3(mx[q], f[2 * q], f[2 * q + 1]);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) r[j + q] = __float_as_uint(f[q]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            const float4 k4 = *reinterpret_cast<const float4*>(ksm + c0 + j);
+            const float4 b4 = *reinterpret_cast<const float4*>(b2m + c0 + j);
+            float f[4];
+            unpack2(ffma2(fmul2(pack2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), pack2(k4.x, k4.y)),
+                          cq2, pack2(b4.x, b4.y)), f[0], f[1]);
+            unpack2(ffma2(fmul2(pack2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])), pack2(k4.z, k4.w)),
+                          cq2, pack2(b4.z, b4.w)), f[2], f[3]);
+            if (!keep) f[0] = f[1] = f[2] = f[3] = -INFINITY;
+            const int q = (j >> 2) & 3;
+            mx[q] = fmax3(mx[q], fmaxf(f[0], f[1]), fmaxf(f[2], f[3]));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) r[j + e] = __float_as_uint(f[e]);
+          }
         }
-        tmax = mx;
+        tmem_st32(tS + c0, r);
+      };
+      {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tS, ra);
+        tmem_wait_ld(ra);
+#pragma unroll
+        for (int c0 = 0; c0 < BN; c0 += 64) {
+          tmem_ld32(tS + c0 + 32, rb);  // next chunk in flight
+          pass1(ra, c0);
+          tmem_wait_ld(rb);
+          if (c0 + 64 < BN) tmem_ld32(tS + c0 + 64, ra);
+          pass1(rb, c0 + 32);
+          if (c0 + 64 < BN) tmem_wait_ld(ra);
+        }
       }
+      tmem_wait_st();
+      const float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      const float tmax = fast ? cq * rmax : rmax;
       const float m_new = fmaxf(m, tmax);
       const bool need = m_new > m + kRescaleLog2;
       if (__any_sync(0xffffffffu, need)) {
@@ -525,24 +570,39 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), 1)
       const float k1 = fast ? cq : 1.f;
       const uint64_t k1v = pack2(k1, k1);
       const uint64_t nm = pack2(-mref, -mref);
-      uint64_t lsum = pack2(0.f, 0.f);
+      uint64_t lsum[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
+      // Pass 2: p = 2^(u*k1 - m), row sum in fp32, P packed to 16 bits into the
+      // first BN/2 columns of S (every S column it overwrites is already read).
+      auto pass2 = [&](uint32_t (&r)[32], int c0) {
+        uint32_t pk[16];
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 64) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c = c0 + 2 * i;
+        for (int i = 0; i < 16; ++i) {
           float t0, t1;
-          unpack2(ffma2(pack2(x[c], x[c + 1]), k1v, nm), t0, t1);
+          unpack2(ffma2(pack2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), k1v, nm), t0, t1);
           const float p0 = ex2(t0), p1 = ex2(t1);
-          lsum = fadd2(lsum, pack2(p0, p1));
+          lsum[i & 1] = fadd2(lsum[i & 1], pack2(p0, p1));
           pk[i] = VBF16 ? cvt_bf16x2(p0, p1) : cvt_f16x2(p0, p1);
         }
-        tmem_st32(tS + c0 / 2, pk);
+        tmem_st16(tS + c0 / 2, pk);
+      };
+      {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(tS, ra);
+        tmem_wait_ld(ra);
+#pragma unroll
+        for (int c0 = 0; c0 < BN; c0 += 64) {
+          tmem_ld32(tS + c0 + 32, rb);
+          pass2(ra, c0);
+          tmem_wait_ld(rb);
+          if (c0 + 64 < BN) tmem_ld32(tS + c0 + 64, ra);
+          pass2(rb, c0 + 32);
+          if (c0 + 64 < BN) tmem_wait_ld(ra);
+        }
       }
-      float la, lb;
-      unpack2(lsum, la, lb);
-      l += la + lb;
+      float la, lb, lc, ld;
+      unpack2(lsum[0], la, lb);
+      unpack2(lsum[1], lc, ld);
+      l += (la + lb) + (lc + ld);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(L::B_PF + s));
