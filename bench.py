@@ -35,12 +35,54 @@ UNIT = "TOPS"
 # 13440 keys masked 5.86 ms = 11.05 ms for the same 4096x33600x56x128 problem.
 PAGE_SPLIT_MS = 11.05
 
+# DRAM traffic of attn_fwd_kernel from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum) of the 16-head banded case (Sq 4096, Sk 33600,
+# unmasked), recorded in profiles/attn_fwd_banded_h16.md together with the
+# SHA-256 of the kernel sources it was taken on. A launch's traffic is scaled
+# from it per head, with the key-proportional part scaled by the keys of the
+# launch. When the kernel sources change, the figure no longer applies.
+ATTN_TRAFFIC = {"source_sha256": "28ea306767706a13a6ddc3ddddac603b8ca0864f635fc23b7baf1f8e874c33b7",
+                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 243852544.0}
+
+
+def attn_source_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("attention.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "int8_qk_quantized_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def attn_traffic_per_launch(H, Sq, sk_list, D):
+    """Average DRAM bytes per attention launch, or None if not measured on this source."""
+    t = ATTN_TRAFFIC
+    if t["bytes"] is None or t["source_sha256"] != attn_source_sha():
+        return None
+    fixed = t["sq"] * t["d"] * 3 + t["sq"] * 8          # q8 + out + lse + q_scale per head
+    per_key = (t["bytes"] / t["heads"] - fixed) / t["sk"]
+    per_launch = [H * (Sq * D * 3 + Sq * 8 + per_key * sk) for sk in sk_list]
+    return sum(per_launch) / len(per_launch)
+
 
 def dist_info():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def dist_max(value, dist, device):
+    """The largest `value` over all ranks (the slowest rank times the job)."""
+    import torch
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+def weak_value(world_size, ops_per_rank, ms_per_step):
+    """Whole-job throughput in TOPS when every rank runs its own copy of the workload."""
+    return world_size * ops_per_rank / (ms_per_step * 1e-3) / 1e12
 
 
 def peaks():
@@ -326,12 +368,10 @@ def main():
     att_ms = sum(e0.elapsed_time(e1) for e0, e1, _ in att_events)
     att_ops = sum(o for _, _, o in att_events)
     if pg:
-        t = torch.tensor([elapsed_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        elapsed_ms = t.item()
+        elapsed_ms = dist_max(elapsed_ms, pg, dev)
     ms_per_step = elapsed_ms / args.steps
     ops = algorithmic_ops(wl)
-    value = ws * ops / (ms_per_step * 1e-3) / 1e12
+    value = weak_value(ws, ops, ms_per_step)
 
     # single calls over all keys: unmasked and with the bias
     def time_call(fn, n=20):
@@ -388,9 +428,7 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = t.item()
+        e2e_ms = dist_max(e2e_ms, pg, dev)
     ia.device_status()
 
     hbm, bf16, bf16_sus, peak_kind = peaks()
@@ -422,11 +460,15 @@ def main():
                      "bias_tops": ops / (bias_ms * 1e-3) / 1e12,
                      "quantize_gbs": quant_bytes / (quant_ms * 1e-3) / 1e9},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
-                     "frac": achieved / bf16, "traffic": None,
-                     "kernel": "attn_fwd_kernel (QS=2, BN=128, D=128)",
+                     "frac": achieved / bf16,
+                     "traffic": attn_traffic_per_launch(H, Sq, [hi - lo, lo, Sk - hi], D),
+                     "algorithmic_bytes": sum(H * (Sq * D * 3 + Sq * 8 + n * (D * 3 + 4))
+                                              for n in (hi - lo, lo, Sk - hi)) / 3,
+                     "kernel": "attn_fwd_kernel (QS=2, BN=128, D=128); per launch = mean of "
+                               "the step's three attention launches",
                      "peak_source": f"{peak_kind} bf16 dense burst (MEASURED_PEAKS.json)",
                      "frac_of_sustained": achieved / bf16_sus if bf16_sus else None},
-        "e2e": {"value": ws * ops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": weak_value(ws, ops, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,

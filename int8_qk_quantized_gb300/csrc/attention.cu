@@ -48,6 +48,21 @@ namespace ia {
 
 __device__ unsigned int g_attn_status;
 
+// Phase timestamps of CTA (0,0,0), compiled in only with -DIA_TRACE (a
+// profiling build; the library never defines it).
+#ifdef IA_TRACE
+__device__ unsigned long long g_attn_trace[16][64];
+#define IA_TRACE_POINT(slot, it)                                                   \
+  do {                                                                               \
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (it) < 64)          \
+      g_attn_trace[slot][it] = clock64();                                            \
+  } while (0)
+#else
+#define IA_TRACE_POINT(slot, it) \
+  do {                           \
+  } while (0)
+#endif
+
 namespace {
 
 constexpr int kM = 128;              // query rows per stage (MMA M)
@@ -349,8 +364,10 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), 1)
       tc_fence_after();
       for (int it = 0; it < n_it && ok; ++it) {
         const int kst = it % L::NKS;
+        IA_TRACE_POINT(8, it);
         ok = wait_bar(bar(L::B_KCF + kst), (it / L::NKS) & 1, ctl, kErrMma);
         if (!ok) break;
+        IA_TRACE_POINT(9, it);
         tc_fence_after();
         const int pvs = (it + L::NVS - 1) % L::NVS;
         if (it > 0) {
@@ -367,6 +384,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), 1)
           }
           issue_qk(s, kst);
           mma_commit(bar(L::B_SF + s));
+          IA_TRACE_POINT(10 + s, it);
         }
         if (!ok) break;
         mma_commit(bar(L::B_KCE + kst));
@@ -423,7 +441,9 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), 1)
       if (!ok) break;
       if (it >= L::NKS) ok = wait_bar(bar(L::B_KCE + kst), ((it / L::NKS) - 1) & 1, ctl, kErrConverter);
       if (!ok) break;
+      if (ct == 0) IA_TRACE_POINT(12, it);
       widen_tile<D>(smem + L::OFF_KR + rs * L::KR, smem + L::OFF_KH + kst * L::KH, BN, ct);
+      if (ct == 0) IA_TRACE_POINT(13, it);
       fence_proxy_async_smem();
       mbar_arrive(bar(L::B_KCF + kst));
       mbar_arrive(bar(L::B_KRE + rs));
@@ -477,11 +497,13 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), 1)
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int ss = it % L::NSC;
+      if (r == 0) IA_TRACE_POINT(4 * s, it);
       bool w = wait_bar(bar(L::B_SF + s), it & 1, ctl, kErrSoftmax);
       w = w && wait_bar(bar(L::B_SCF + ss), (it / L::NSC) & 1, ctl, kErrSoftmax);
       ok = __all_sync(0xffffffffu, w);
       if (!ok) break;
       tc_fence_after();
+      if (r == 0) IA_TRACE_POINT(1 + 4 * s, it);
       const float* ksm = reinterpret_cast<const float*>(smem + L::OFF_SC + ss * L::SC);
       const float* b2m = ksm + BN;
       const uint32_t flags = *reinterpret_cast<const volatile uint32_t*>(b2m + BN);
@@ -546,6 +568,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), 1)
         }
       }
       tmem_wait_st();
+      if (r == 0) IA_TRACE_POINT(2 + 4 * s, it);
       const float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const float tmax = fast ? cq * rmax : rmax;
       const float m_new = fmaxf(m, tmax);
@@ -606,6 +629,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(L::B_PF + s));
+      if (r == 0) IA_TRACE_POINT(3 + 4 * s, it);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::B_SCE + ss));
     }
@@ -794,3 +818,10 @@ cudaError_t attention_read_device_error(unsigned int* out, cudaStream_t st) {
 }
 
 }  // namespace ia
+
+#ifdef IA_TRACE
+extern "C" __attribute__((visibility("default"))) int ia_trace_read(unsigned long long* out) {
+  cudaDeviceSynchronize();
+  return static_cast<int>(cudaMemcpyFromSymbol(out, ia::g_attn_trace, sizeof(ia::g_attn_trace)));
+}
+#endif
