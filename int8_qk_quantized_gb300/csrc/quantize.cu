@@ -26,12 +26,11 @@ namespace cg = cooperative_groups;
 namespace ia {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kTile = 64;
 
 template <int DT>
-__device__ __forceinline__ void load8(const void* p, float (&v)[8]) {
-  const uint4 w = __ldg(reinterpret_cast<const uint4*>(p));
+__device__ __forceinline__ void unpack8(const uint4 w, float (&v)[8]) {
   const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -45,6 +44,11 @@ __device__ __forceinline__ void load8(const void* p, float (&v)[8]) {
       v[2 * i + 1] = f.y;
     }
   }
+}
+
+template <int DT>
+__device__ __forceinline__ void load8(const void* p, float (&v)[8]) {
+  unpack8<DT>(__ldg(reinterpret_cast<const uint4*>(p)), v);
 }
 
 __device__ __forceinline__ bool row_valid(const int32_t* valid, int r) {
@@ -82,7 +86,7 @@ __device__ __forceinline__ void store_codes(int8_t* dst, const float (&x)[8], fl
 // grid: (chunks, H, B). Chunk c holds rows [c*chunk, min(S, (c+1)*chunk)).
 // With CLUSTER_MEAN the chunks of one head are one cluster and compute the mean.
 template <int D, int DT, bool CLUSTER_MEAN>
-__global__ void __launch_bounds__(kThreads) quantize_kernel(const QuantArgs a, int chunk) {
+__global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a, int chunk) {
   constexpr int TPR = D / 8;            // threads per row, 8 elements each
   constexpr int RPP = kThreads / TPR;   // rows per pass
   static_assert(RPP * TPR == kThreads, "layout");
@@ -108,22 +112,24 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const QuantArgs a, i
       float hi[8], lo[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) hi[i] = lo[i] = 0.f;
-      for (int base = r0; base < r1; base += 4 * RPP) {
-        float v[4][8];
+      // 8 rows of 16-byte loads in flight per thread, kept packed until used
+      constexpr int U1 = 8;
+      for (int base = r0; base < r1; base += U1 * RPP) {
+        uint4 w[U1];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < U1; ++u) {
           const int rr = base + u * RPP + tr;
-          if (rr < r1 && row_valid(a.valid, rr)) {
-            load8<DT>(xb + (static_cast<int64_t>(rr) * a.ss + tc * 8) * 2, v[u]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[u][i] = 0.f;
-          }
+          w[u] = (rr < r1 && row_valid(a.valid, rr))
+                     ? __ldg(reinterpret_cast<const uint4*>(xb + (static_cast<int64_t>(rr) * a.ss + tc * 8) * 2))
+                     : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < U1; ++u) {
+          float v[8];
+          unpack8<DT>(w[u], v);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) two_sum_acc(hi[i], lo[i], v[u][i]);
+          for (int i = 0; i < 8; ++i) two_sum_acc(hi[i], lo[i], v[i]);
+        }
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i)
@@ -170,28 +176,31 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const QuantArgs a, i
   if (!a.gran_block) {
     float* sc = a.scales + bh * a.S;
     // The loop bound is uniform across the CTA: every lane reaches the shuffles.
-    for (int base = r0; base < r1; base += 2 * RPP) {
-      float v[2][8];
-      bool ok[2];
+    // The chunk is walked from its end, so rows the mean pass read last are
+    // read again first, while they may still sit in L2.
+    constexpr int U2 = 8;  // rows of 16-byte loads in flight per thread
+    const int nbase = (r1 - r0 + U2 * RPP - 1) / (U2 * RPP);
+    for (int ib = nbase - 1; ib >= 0; --ib) {
+      const int base = r0 + ib * U2 * RPP;
+      uint4 w[U2];
+      bool ok[U2];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < U2; ++u) {
         const int rr = base + u * RPP + tr;
         ok[u] = rr < r1 && row_valid(a.valid, rr);
-        if (ok[u]) {
-          load8<DT>(xb + (static_cast<int64_t>(rr) * a.ss + tc * 8) * 2, v[u]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[u][i] = 0.f;
-        }
+        w[u] = ok[u] ? __ldg(reinterpret_cast<const uint4*>(xb + (static_cast<int64_t>(rr) * a.ss + tc * 8) * 2))
+                     : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < U2; ++u) {
         const int rr = base + u * RPP + tr;
+        float v[8];
+        unpack8<DT>(w[u], v);
         float m = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          if (a.center && ok[u]) v[u][i] = __fsub_rn(v[u][i], mu[i]);
-          m = fmaxf(m, fabsf(v[u][i]));
+          if (a.center && ok[u]) v[i] = __fsub_rn(v[i], mu[i]);
+          m = fmaxf(m, fabsf(v[i]));
         }
 #pragma unroll
         for (int off = TPR / 2; off > 0; off >>= 1)
@@ -199,7 +208,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const QuantArgs a, i
         if (rr < r1) {
           const float scale = m > 0.f ? __fdiv_rn(m, 127.f) : 0.f;
           const float inv = m > 0.f ? __fdiv_rn(127.f, m) : 0.f;
-          store_codes(cb + static_cast<int64_t>(rr) * D + tc * 8, v[u], inv);
+          store_codes(cb + static_cast<int64_t>(rr) * D + tc * 8, v, inv);
           if (tc == 0) sc[rr] = ok[u] ? scale : 0.f;
         }
       }
@@ -250,9 +259,25 @@ template <int D, int DT>
 cudaError_t launch_typed(const QuantArgs& a, int num_sms, cudaStream_t st) {
   const int BH = a.B * a.H;
   if (a.center && a.mean_in == nullptr) {
-    // One cluster per head; enough CTAs to cover the SMs about twice.
-    int cl = (2 * num_sms + BH - 1) / BH;
-    cl = cl < 1 ? 1 : (cl > 8 ? 8 : cl);
+    // One cluster per head, sized so that the grid fills two CTAs per SM in
+    // one wave where the heads allow (up to the largest cluster the device
+    // can place; 16 needs the non-portable cluster size attribute).
+    auto kern = quantize_kernel<D, DT, true>;
+    static int max_cl = 0;
+    if (max_cl == 0) {
+      max_cl = 8;
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+        cudaLaunchConfig_t q = {};
+        q.gridDim = dim3(16, 1, 1);
+        q.blockDim = dim3(kThreads);
+        int n = 0;
+        if (cudaOccupancyMaxPotentialClusterSize(&n, kern, &q) == cudaSuccess && n >= 8)
+          max_cl = n > 16 ? 16 : n;
+      }
+      cudaGetLastError();
+    }
+    int cl = (2 * num_sms) / BH;
+    cl = cl < 1 ? 1 : (cl > max_cl ? max_cl : cl);
     const int max_chunks = (a.S + kTile - 1) / kTile;
     if (cl > max_chunks) cl = max_chunks;
     int chunk = (a.S + cl - 1) / cl;
@@ -270,7 +295,7 @@ cudaError_t launch_typed(const QuantArgs& a, int num_sms, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, quantize_kernel<D, DT, true>, a, chunk);
+    return cudaLaunchKernelEx(&cfg, kern, a, chunk);
   }
   // Rows split into chunks of 256 (a multiple of 64); no cluster.
   const int chunk = 256;
