@@ -102,7 +102,12 @@ struct Params {
 
 template <int D, int QS, int BN, bool SPARSE>
 struct Layout {
-  static constexpr int NKS = 2, NVS = 2, NRS = 2, NSC = 2;
+  // Block-sparse, D == 128: the int8 K tile lands (by TMA) in the second
+  // 64-column block of its fp16 K buffer and is widened in place, which keeps
+  // the CTA small enough for two per SM. Otherwise it has staging buffers.
+  static constexpr bool INPLACE = SPARSE && D == 128;
+  static constexpr int NKS = 2, NVS = 2, NSC = 2;
+  static constexpr int NRS = INPLACE ? 0 : 2;
   static constexpr int QH = kM * D * 2;   // fp16 Q stage
   static constexpr int KH = BN * D * 2;   // fp16 K tile
   static constexpr int VB = BN * D * 2;   // 16-bit V tile
@@ -117,7 +122,7 @@ struct Layout {
   static constexpr int OFF_VS = OFF_SC + NSC * SC;
   static constexpr int OFF_BAR = (OFF_VS + D * 4 + 7) / 8 * 8;
   // barrier indices
-  static constexpr int B_QFULL = 0, B_QCONV = 1, B_KRF = 2, B_KRE = B_KRF + NRS,
+  static constexpr int B_QFULL = 0, B_QCONV = 1, B_KRF = 2, B_KRE = B_KRF + NKS,
                        B_KCF = B_KRE + NRS, B_KCE = B_KCF + NKS, B_VF = B_KCE + NKS,
                        B_VE = B_VF + NVS, B_SCF = B_VE + NVS, B_SCE = B_SCF + NSC,
                        B_SF = B_SCE + NSC, B_PF = B_SF + QS, B_OF = B_PF + QS,
@@ -133,6 +138,7 @@ struct Layout {
   static_assert(QS * QR <= VB, "raw Q is staged in the first V buffer");
   static_assert(TMEM_NEED <= 512, "TMEM budget");
   static_assert(OFF_QH % 1024 == 0 && OFF_KH % 1024 == 0 && OFF_V % 1024 == 0, "swizzle align");
+  static_assert(!INPLACE || KR == BN * 128, "the int8 tile fills one 64-column fp16 block");
 };
 
 struct Ctl {
@@ -182,13 +188,16 @@ __device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity, unsigned l
 
 // int8 tile [rows x D] row-major -> fp16 [rows x D] in 128-byte-swizzled
 // K-major blocks of 64 columns (block stride rows*128 bytes), as tcgen05 reads
-// with a SWIZZLE_128B descriptor. 64 threads.
-template <int D>
+// with a SWIZZLE_128B descriptor. 64 threads; each row belongs to one warp.
+// IN_PLACE: `raw` is the second block of `dst` (D == 128), so every lane reads
+// its chunk before any lane of the warp writes the row back.
+template <int D, bool IN_PLACE>
 __device__ __forceinline__ void widen_tile(const uint8_t* raw, uint8_t* dst, int rows, int ct) {
   constexpr int CPR = D / 16;  // 16-byte int8 chunks per row
   for (int idx = ct; idx < rows * CPR; idx += 64) {
     const int r = idx / CPR, c = idx % CPR;
     const uint4 w = *reinterpret_cast<const uint4*>(raw + r * D + c * 16);
+    if (IN_PLACE) __syncwarp();
     uint32_t h[8];
     i8x4_to_f16x4(w.x, h[0], h[1]);
     i8x4_to_f16x4(w.y, h[2], h[3]);
@@ -200,11 +209,12 @@ __device__ __forceinline__ void widen_tile(const uint8_t* raw, uint8_t* dst, int
     const int sw = r & 7;
     *reinterpret_cast<uint4*>(rowp + ((k0 ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint4*>(rowp + (((k0 + 1) ^ sw) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+    if (IN_PLACE) __syncwarp();
   }
 }
 
 template <int D, int QS, int BN, bool SPARSE, bool VBF16>
-__global__ void __launch_bounds__(32 * (4 * QS + 4), 1)
+__global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const Params a) {
@@ -229,14 +239,12 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), 1)
   if (tid == 0) {
     mbar_init(bar(L::B_QFULL), 1);
     mbar_init(bar(L::B_QCONV), 64);
-    for (int i = 0; i < L::NRS; ++i) {
-      mbar_init(bar(L::B_KRF + i), 1);
-      mbar_init(bar(L::B_KRE + i), 64);
-    }
     for (int i = 0; i < L::NKS; ++i) {
+      mbar_init(bar(L::B_KRF + i), 1);
       mbar_init(bar(L::B_KCF + i), 64);
       mbar_init(bar(L::B_KCE + i), 1);
     }
+    for (int i = 0; i < L::NRS; ++i) mbar_init(bar(L::B_KRE + i), 64);
     for (int i = 0; i < L::NVS; ++i) {
       mbar_init(bar(L::B_VF + i), 1);
       mbar_init(bar(L::B_VE + i), 1);
@@ -305,8 +313,8 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), 1)
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      int kr_last[L::NRS], v_last[L::NVS];
-      for (int i = 0; i < L::NRS; ++i) kr_last[i] = -1;
+      int kr_last[L::NKS], v_last[L::NVS];
+      for (int i = 0; i < L::NKS; ++i) kr_last[i] = -1;
       for (int i = 0; i < L::NVS; ++i) v_last[i] = -1;
       mbar_arrive_expect_tx(bar(L::B_QFULL), QS * kM * D);
       for (int s = 0; s < QS; ++s)
@@ -314,12 +322,21 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), 1)
       bool ok = true;
       for (int it = 0; it < n_it; ++it) {
         const int kt = SPARSE ? static_cast<int>(list[it]) : it;
-        const int rs = it % L::NRS;
-        if (it >= L::NRS) ok = wait_bar(bar(L::B_KRE + rs), ((it / L::NRS) - 1) & 1, ctl, kErrProducer);
+        // int8 K tile: into its fp16 buffer (in place) or a staging buffer
+        const int ks = it % L::NKS;
+        uint32_t kdst;
+        if constexpr (L::INPLACE) {
+          if (it >= L::NKS) ok = wait_bar(bar(L::B_KCE + ks), ((it / L::NKS) - 1) & 1, ctl, kErrProducer);
+          kdst = sm_kh + ks * L::KH + BN * 128;
+        } else {
+          const int rs = it % L::NRS;
+          if (it >= L::NRS) ok = wait_bar(bar(L::B_KRE + rs), ((it / L::NRS) - 1) & 1, ctl, kErrProducer);
+          kdst = sm_kr + rs * L::KR;
+        }
         if (!ok) break;
-        mbar_arrive_expect_tx(bar(L::B_KRF + rs), BN * D);
-        tma_load_4d(sm_kr + rs * L::KR, &tm_k, bar(L::B_KRF + rs), 0, kt * BN, h, b);
-        kr_last[rs] = it;
+        mbar_arrive_expect_tx(bar(L::B_KRF + ks), BN * D);
+        tma_load_4d(kdst, &tm_k, bar(L::B_KRF + ks), 0, kt * BN, h, b);
+        kr_last[ks] = it;
         const int vs = it % L::NVS;
         if (it == 0)
           ok = wait_bar(bar(L::B_QCONV), 0, ctl, kErrProducer);  // raw Q sits in V buffer 0
@@ -334,8 +351,8 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), 1)
       }
       if (!ok) {  // let issued copies land before the CTA's shared memory goes away
         drain_bar(bar(L::B_QFULL), 0, a.timeout_ns);
-        for (int i = 0; i < L::NRS; ++i)
-          if (kr_last[i] >= 0) drain_bar(bar(L::B_KRF + i), (kr_last[i] / L::NRS) & 1, a.timeout_ns);
+        for (int i = 0; i < L::NKS; ++i)
+          if (kr_last[i] >= 0) drain_bar(bar(L::B_KRF + i), (kr_last[i] / L::NKS) & 1, a.timeout_ns);
         for (int i = 0; i < L::NVS; ++i)
           if (v_last[i] >= 0) drain_bar(bar(L::B_VF + i), (v_last[i] / L::NVS) & 1, a.timeout_ns);
       }
@@ -411,7 +428,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), 1)
     bool ok = wait_bar(bar(L::B_QFULL), 0, ctl, kErrConverter);
     if (ok) {
       for (int s = 0; s < QS; ++s)
-        widen_tile<D>(smem + L::OFF_V + s * L::QR, smem + L::OFF_QH + s * L::QH, kM, ct);
+        widen_tile<D, false>(smem + L::OFF_V + s * L::QR, smem + L::OFF_QH + s * L::QH, kM, ct);
       fence_proxy_async_smem();
       mbar_arrive(bar(L::B_QCONV));
     }
@@ -436,17 +453,23 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), 1)
         bv[e] = valid ? (a.bias ? __ldg(a.bias + key) * kLog2e : 0.f) : -INFINITY;
       }
       // K tile: int8 -> fp16 codes in the swizzled layout the MMA reads
-      const int rs = it % L::NRS, kst = it % L::NKS;
-      ok = wait_bar(bar(L::B_KRF + rs), (it / L::NRS) & 1, ctl, kErrConverter);
-      if (!ok) break;
-      if (it >= L::NKS) ok = wait_bar(bar(L::B_KCE + kst), ((it / L::NKS) - 1) & 1, ctl, kErrConverter);
+      const int kst = it % L::NKS;
+      ok = wait_bar(bar(L::B_KRF + kst), (it / L::NKS) & 1, ctl, kErrConverter);
       if (!ok) break;
       if (ct == 0) IA_TRACE_POINT(12, it);
-      widen_tile<D>(smem + L::OFF_KR + rs * L::KR, smem + L::OFF_KH + kst * L::KH, BN, ct);
+      if constexpr (L::INPLACE) {
+        uint8_t* kh = smem + L::OFF_KH + kst * L::KH;
+        widen_tile<D, true>(kh + BN * 128, kh, BN, ct);
+      } else {
+        const int rs = it % L::NRS;
+        if (it >= L::NKS) ok = wait_bar(bar(L::B_KCE + kst), ((it / L::NKS) - 1) & 1, ctl, kErrConverter);
+        if (!ok) break;
+        widen_tile<D, false>(smem + L::OFF_KR + rs * L::KR, smem + L::OFF_KH + kst * L::KH, BN, ct);
+        mbar_arrive(bar(L::B_KRE + rs));
+      }
       if (ct == 0) IA_TRACE_POINT(13, it);
       fence_proxy_async_smem();
       mbar_arrive(bar(L::B_KCF + kst));
-      mbar_arrive(bar(L::B_KRE + rs));
       // k scales, bias * log2(e) (-inf past the valid keys) and tile flags
       const int ss = it % L::NSC;
       if (it >= L::NSC) ok = wait_bar(bar(L::B_SCE + ss), ((it / L::NSC) - 1) & 1, ctl, kErrConverter);
