@@ -211,6 +211,55 @@ def cpu_baseline(seconds_target=12.0):
                       f"quantise + fp64 attention with bias) in {dt:.1f} s"}
 
 
+def time_workloads(ia, torch, names=("tiny", "sdxl", "anima4k", "anima9k", "sparse"), n=10):
+    """Quantise and attention times of the other workloads (CUDA events,
+    after 3 warm-up calls). TOPS use algorithmic ops (kept tiles for sparse)."""
+    from workloads import WORKLOADS, algorithmic_ops, make_inputs
+    res = {}
+    for name in names:
+        wl = WORKLOADS[name]
+        inp = make_inputs(wl, "cuda")
+        kept = None
+        if wl.sparse:
+            kept = inp.block_mask.float().sum(-1).mean().item()
+        q8, qs, k8, ks = ia.quantize_qk(inp.q, inp.k, granularity=wl.granularity,
+                                        kv_valid=inp.kv_valid)
+        out, lse = ia.attention(q8, k8, qs, ks, inp.v, bias=inp.bias, block_mask=inp.block_mask,
+                                v_scale=inp.v_scale, kv_valid=inp.kv_valid,
+                                granularity=wl.granularity, return_lse=True)
+
+        def tq():
+            ia.quantize_qk(inp.q, inp.k, granularity=wl.granularity, kv_valid=inp.kv_valid)
+
+        def ta():
+            ia.attention(q8, k8, qs, ks, inp.v, bias=inp.bias, block_mask=inp.block_mask,
+                         v_scale=inp.v_scale, kv_valid=inp.kv_valid, granularity=wl.granularity,
+                         out=out, lse=lse, return_lse=True)
+
+        ms = {}
+        for key, fn in (("quantize_ms", tq), ("attention_ms", ta)):
+            for _ in range(3):
+                fn()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(n):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms[key] = e0.elapsed_time(e1) / n
+        ia.device_status()
+        ops = algorithmic_ops(wl, kept)
+        ms["attention_tops"] = ops / (ms["attention_ms"] * 1e-3) / 1e12
+        ms["shape"] = f"B{wl.B} H{wl.H} Sq{wl.Sq} Sk{wl.Sk} D{wl.D} {wl.dtype}"
+        if kept is not None:
+            ms["kept_tiles_per_row"] = kept
+        res[name] = ms
+        del inp, q8, k8, out
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_profile(args):
     """One kernel alone on a (possibly smaller) copy of its workload, for ncu."""
     import torch
@@ -261,6 +310,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip timing the other four workloads")
     ap.add_argument("--profile", default=None,
                     choices=["attention", "attention_bias", "quantize", "merge", "sparse"],
                     help="run one kernel alone, --steps times after --warmup (for ncu)")
@@ -438,6 +489,7 @@ def main():
         if pg:
             pg.destroy_process_group()
         return
+    others = None if args.no_extra else time_workloads(ia, torch)
     cpu = None if args.no_cpu_baseline else cpu_baseline()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -470,6 +522,7 @@ def main():
                      "frac_of_sustained": achieved / bf16_sus if bf16_sus else None},
         "e2e": {"value": weak_value(ws, ops, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "workloads": others,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,

@@ -113,6 +113,10 @@ typedef struct ia_attn_params {
   int64_t lse_strides[2];       /* lse (b,h); query index contiguous */
   const float* v_scale;         /* optional fp32 [H, D], applied once to the output */
   const int32_t* kv_valid;      /* optional int32 [Sk/64] valid keys per 64-key tile */
+  uint64_t wait_timeout_ns;     /* limit of each device-side wait; 0 selects 2 s */
+  int debug_stall;              /* test hook: nonzero makes one internal wait of every CTA
+                                   wait for a signal that never comes, so the call ends
+                                   through the timeout path (status IA_ERR_TIMEOUT) */
 } ia_attn_params;
 
 /* Fill p with contiguous BHSD strides for the given shape (no pointers set). */

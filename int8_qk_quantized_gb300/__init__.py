@@ -46,6 +46,7 @@ class AttnParams(ctypes.Structure):
         ("v_strides", ctypes.c_int64 * 3), ("o_strides", ctypes.c_int64 * 3),
         ("lse_strides", ctypes.c_int64 * 2),
         ("v_scale", ctypes.c_void_p), ("kv_valid", ctypes.c_void_p),
+        ("wait_timeout_ns", ctypes.c_uint64), ("debug_stall", ctypes.c_int),
     ]
 
 
@@ -165,7 +166,7 @@ def quantize_qk(q, k, granularity: str = "token", center_k: bool = True, kv_vali
 
 def attention(q8, k8, q_scale, k_scale, v, *, bias=None, block_mask=None, sm_scale=None,
               v_scale=None, kv_valid=None, granularity: str = "token", return_lse: bool = False,
-              out=None, lse=None, stream=None):
+              out=None, lse=None, stream=None, wait_timeout_ns: int = 0, debug_stall: bool = False):
     """Forward attention on INT8 Q/K codes with a 16-bit P.V (see ``ia_attention_fwd``).
 
     ``bias`` is fp32 ``[Sk]`` (any ``[1,1,1,Sk]`` view), ``block_mask`` bool
@@ -181,6 +182,8 @@ def attention(q8, k8, q_scale, k_scale, v, *, bias=None, block_mask=None, sm_sca
     p.sm_scale = float("nan") if sm_scale is None else float(sm_scale)
     p.granularity = _gran_code(granularity)
     p.v_dtype = vd
+    p.wait_timeout_ns = int(wait_timeout_ns)
+    p.debug_stall = 1 if debug_stall else 0
     if out is None:
         out = torch.empty((B, H, Sq, D), dtype=v.dtype, device=v.device)
     if return_lse and lse is None:

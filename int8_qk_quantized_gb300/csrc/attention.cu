@@ -98,6 +98,7 @@ struct Params {
   int64_t o_sb, o_sh, o_ss;
   int64_t l_sb, l_sh;
   unsigned long long timeout_ns;
+  int debug_stall;
 };
 
 template <int D, int QS, int BN, bool SPARSE>
@@ -126,7 +127,7 @@ struct Layout {
                        B_KCF = B_KRE + NRS, B_KCE = B_KCF + NKS, B_VF = B_KCE + NKS,
                        B_VE = B_VF + NVS, B_SCF = B_VE + NVS, B_SCE = B_SCF + NSC,
                        B_SF = B_SCE + NSC, B_PF = B_SF + QS, B_OF = B_PF + QS,
-                       B_DRAIN = B_OF + QS, NBAR = B_DRAIN + 1;
+                       B_DRAIN = B_OF + QS, B_STALL = B_DRAIN + 1, NBAR = B_STALL + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;       // tmem base, abort, count, pad
   static constexpr int OFF_LIST = OFF_MISC + 16 + 32;       // + warp counts for the list scan
   static constexpr int SMEM_FIXED = OFF_LIST;
@@ -259,6 +260,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       mbar_init(bar(L::B_OF + s), 1);
     }
     mbar_init(bar(L::B_DRAIN), 1);
+    mbar_init(bar(L::B_STALL), 1);  // never signalled: the timeout test hook waits on it
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -378,6 +380,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         }
       };
       bool ok = wait_bar(bar(L::B_QCONV), 0, ctl, kErrMma);
+      if (ok && a.debug_stall) ok = wait_bar(bar(L::B_STALL), 0, ctl, kErrMma);
       tc_fence_after();
       for (int it = 0; it < n_it && ok; ++it) {
         const int kst = it % L::NKS;
@@ -787,7 +790,8 @@ ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** ms
   a.o_ss = p.o_strides[2];
   a.l_sb = p.lse_strides[0];
   a.l_sh = p.lse_strides[1];
-  a.timeout_ns = 2000000000ull;
+  a.timeout_ns = p.wait_timeout_ns ? p.wait_timeout_ns : 2000000000ull;
+  a.debug_stall = p.debug_stall;
   const size_t smem = L::SMEM_FIXED + (SPARSE ? static_cast<size_t>(a.Tk) * 2 : 0);
   auto kern = attn_fwd_kernel<D, QS, BN, SPARSE, VBF16>;
   if (smem > 232448) {
