@@ -41,8 +41,8 @@ PAGE_SPLIT_MS = 11.05
 # SHA-256 of the kernel sources it was taken on. A launch's traffic is scaled
 # from it per head, with the key-proportional part scaled by the keys of the
 # launch. When the kernel sources change, the figure no longer applies.
-ATTN_TRAFFIC = {"source_sha256": "28ea306767706a13a6ddc3ddddac603b8ca0864f635fc23b7baf1f8e874c33b7",
-                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 243852544.0}
+ATTN_TRAFFIC = {"source_sha256": "edc32c366ccc4193ffdfbeb9f8ee2c61f376c0f7c95eaffa7fd0bced7ea8c4d9",
+                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 243976704.0}
 
 
 def attn_source_sha():
