@@ -364,20 +364,32 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     if (lane == 0) {
       constexpr uint32_t idq = idesc_f16(kM, BN, 0, 0, 0, 0);                  // f16 x f16, K-major
       constexpr uint32_t idv = idesc_f16(kM, D, VBF16 ? 1 : 0, VBF16 ? 1 : 0, 0, 1);  // V MN-major
+      // Descriptors are built once; a k-step or buffer offset is added to the
+      // 14-bit start-address field (16-byte units), which cannot overflow for
+      // addresses inside the CTA's shared memory. This keeps the issuing
+      // thread to a few instructions per MMA.
+      const uint64_t qdesc = sdesc_sw128(sm_qh, 16, 1024);
+      const uint64_t kdesc = sdesc_sw128(sm_kh, 16, 1024);
+      const uint64_t vdesc = sdesc_sw128(sm_v, BN * 128, 1024);
       auto issue_qk = [&](int s, int kst) {
+        const uint64_t qa = qdesc + static_cast<uint64_t>((s * L::QH) >> 4);
+        const uint64_t kb = kdesc + static_cast<uint64_t>((kst * L::KH) >> 4);
+        const uint32_t dt = tmem + s * BN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(sm_qh + s * L::QH + (kk >> 2) * (kM * 128) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sm_kh + kst * L::KH + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
-          mma_ss(tmem + s * BN, ad, bd, idq, kk > 0 ? 1u : 0u);
+          const uint64_t ad = qa + static_cast<uint64_t>(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
+          const uint64_t bd = kb + static_cast<uint64_t>(((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4);
+          mma_ss(dt, ad, bd, idq, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int s, int vs, bool first) {
+        const uint64_t vb = vdesc + static_cast<uint64_t>((vs * L::VB) >> 4);
+        const uint32_t dt = tmem + QS * BN + s * D;
+        const uint32_t pt = tmem + s * BN;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bd = sdesc_sw128(sm_v + vs * L::VB + kk * 16 * 128, BN * 128, 1024);
-          mma_ts(tmem + QS * BN + s * D, tmem + s * BN + kk * 8, bd, idv, (first && kk == 0) ? 0u : 1u);
-        }
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(dt, pt + kk * 8, vb + static_cast<uint64_t>((kk * 16 * 128) >> 4), idv,
+                 (first && kk == 0) ? 0u : 1u);
       };
       bool ok = wait_bar(bar(L::B_QCONV), 0, ctl, kErrMma);
       if (ok && a.debug_stall) ok = wait_bar(bar(L::B_STALL), 0, ctl, kErrMma);
@@ -536,65 +548,50 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       const bool fast = (flags & 1u) == 0;
       const bool keep = SPARSE ? ((flags >> (1 + half)) & 1u) != 0 : true;
       const uint64_t cq2 = pack2(cq, cq);
+      // The whole S row of this thread in one TMEM round trip.
+      uint32_t sv[BN];
+      if constexpr (BN == 128) {
+        tmem_ld128(tS, sv);
+      } else {
+        tmem_ld64(tS, sv);
+      }
+      tmem_wait_ld(sv);
+      if (r == 0) IA_TRACE_POINT(2 + 4 * s, it);
+      // u = acc * k_scale (fast tiles) or t = u * cq + bias*log2e / -inf
+      // (masked tiles), in place, and the row maximum.
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      // Pass 1 over 32-column chunks of S: u = acc * k_scale (fast tiles) or
-      // t = u * cq + bias*log2e / -inf (masked tiles), the row maximum, and u
-      // written back in place.
-      auto pass1 = [&](uint32_t (&r)[32], int c0) {
-        if (fast) {
+      if (fast) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            const float4 ka = *reinterpret_cast<const float4*>(ksm + c0 + j);
-            const float4 kb = *reinterpret_cast<const float4*>(ksm + c0 + j + 4);
-            const uint64_t u0 = fmul2(pack2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), pack2(ka.x, ka.y));
-            const uint64_t u1 = fmul2(pack2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])), pack2(ka.z, ka.w));
-            const uint64_t u2 = fmul2(pack2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])), pack2(kb.x, kb.y));
-            const uint64_t u3 = fmul2(pack2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])), pack2(kb.z, kb.w));
-            float f[8];
-            unpack2(u0, f[0], f[1]);
-            unpack2(u1, f[2], f[3]);
-            unpack2(u2, f[4], f[5]);
-            unpack2(u3, f[6], f[7]);
+        for (int c = 0; c < BN; c += 8) {
+          const float4 ka = *reinterpret_cast<const float4*>(ksm + c);
+          const float4 kb = *reinterpret_cast<const float4*>(ksm + c + 4);
+          float f[8];
+          unpack2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(ka.x, ka.y)), f[0], f[1]);
+          unpack2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(ka.z, ka.w)), f[2], f[3]);
+          unpack2(fmul2(pack2(__uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5])), pack2(kb.x, kb.y)), f[4], f[5]);
+          unpack2(fmul2(pack2(__uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7])), pack2(kb.z, kb.w)), f[6], f[7]);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) mx[q] = fmax3(mx[q], f[2 * q], f[2 * q + 1]);
+          for (int q = 0; q < 4; ++q) mx[q] = fmax3(mx[q], f[2 * q], f[2 * q + 1]);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) r[j + q] = __float_as_uint(f[q]);
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            const float4 k4 = *reinterpret_cast<const float4*>(ksm + c0 + j);
-            const float4 b4 = *reinterpret_cast<const float4*>(b2m + c0 + j);
-            float f[4];
-            unpack2(ffma2(fmul2(pack2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), pack2(k4.x, k4.y)),
-                          cq2, pack2(b4.x, b4.y)), f[0], f[1]);
-            unpack2(ffma2(fmul2(pack2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])), pack2(k4.z, k4.w)),
-                          cq2, pack2(b4.z, b4.w)), f[2], f[3]);
-            if (!keep) f[0] = f[1] = f[2] = f[3] = -INFINITY;
-            const int q = (j >> 2) & 3;
-            mx[q] = fmax3(mx[q], fmaxf(f[0], f[1]), fmaxf(f[2], f[3]));
-#pragma unroll
-            for (int e = 0; e < 4; ++e) r[j + e] = __float_as_uint(f[e]);
-          }
+          for (int q = 0; q < 8; ++q) sv[c + q] = __float_as_uint(f[q]);
         }
-        tmem_st32(tS + c0, r);
-      };
-      {
-        uint32_t ra[32], rb[32];
-        tmem_ld32(tS, ra);
-        tmem_wait_ld(ra);
+      } else {
 #pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 64) {
-          tmem_ld32(tS + c0 + 32, rb);  // next chunk in flight
-          pass1(ra, c0);
-          tmem_wait_ld(rb);
-          if (c0 + 64 < BN) tmem_ld32(tS + c0 + 64, ra);
-          pass1(rb, c0 + 32);
-          if (c0 + 64 < BN) tmem_wait_ld(ra);
+        for (int c = 0; c < BN; c += 4) {
+          const float4 k4 = *reinterpret_cast<const float4*>(ksm + c);
+          const float4 b4 = *reinterpret_cast<const float4*>(b2m + c);
+          float f[4];
+          unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(k4.x, k4.y)),
+                        cq2, pack2(b4.x, b4.y)), f[0], f[1]);
+          unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(k4.z, k4.w)),
+                        cq2, pack2(b4.z, b4.w)), f[2], f[3]);
+          if (!keep) f[0] = f[1] = f[2] = f[3] = -INFINITY;
+          const int q = (c >> 2) & 3;
+          mx[q] = fmax3(mx[q], fmaxf(f[0], f[1]), fmaxf(f[2], f[3]));
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sv[c + e] = __float_as_uint(f[e]);
         }
       }
-      tmem_wait_st();
-      if (r == 0) IA_TRACE_POINT(2 + 4 * s, it);
       const float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const float tmax = fast ? cq * rmax : rmax;
       const float m_new = fmaxf(m, tmax);
@@ -602,13 +599,13 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       if (__any_sync(0xffffffffu, need)) {
         const float alpha = need ? ex2(m - m_new) : 1.f;
         if (it > 0) {
-#pragma unroll
+#pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t rr[32];
             tmem_ld32(tO + c0, rr);
             tmem_wait_ld(rr);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+            for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
             tmem_st32(tO + c0, rr);
           }
         }
@@ -620,33 +617,21 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       const uint64_t k1v = pack2(k1, k1);
       const uint64_t nm = pack2(-mref, -mref);
       uint64_t lsum[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
-      // Pass 2: p = 2^(u*k1 - m), row sum in fp32, P packed to 16 bits into the
-      // first BN/2 columns of S (every S column it overwrites is already read).
-      auto pass2 = [&](uint32_t (&r)[32], int c0) {
-        uint32_t pk[16];
+      // p = 2^(t - m) with the row sum in fp32; P packed to 16 bits in place
+      // (pair i lands in word i, whose value is already consumed) and written
+      // to the first BN/2 columns of S in one store.
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float t0, t1;
-          unpack2(ffma2(pack2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), k1v, nm), t0, t1);
-          const float p0 = ex2(t0), p1 = ex2(t1);
-          lsum[i & 1] = fadd2(lsum[i & 1], pack2(p0, p1));
-          pk[i] = VBF16 ? cvt_bf16x2(p0, p1) : cvt_f16x2(p0, p1);
-        }
-        tmem_st16(tS + c0 / 2, pk);
-      };
-      {
-        uint32_t ra[32], rb[32];
-        tmem_ld32(tS, ra);
-        tmem_wait_ld(ra);
-#pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 64) {
-          tmem_ld32(tS + c0 + 32, rb);
-          pass2(ra, c0);
-          tmem_wait_ld(rb);
-          if (c0 + 64 < BN) tmem_ld32(tS + c0 + 64, ra);
-          pass2(rb, c0 + 32);
-          if (c0 + 64 < BN) tmem_wait_ld(ra);
-        }
+      for (int e = 0; e < BN / 2; ++e) {
+        float t0, t1;
+        unpack2(ffma2(pack2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), k1v, nm), t0, t1);
+        const float p0 = ex2(t0), p1 = ex2(t1);
+        lsum[e & 1] = fadd2(lsum[e & 1], pack2(p0, p1));
+        sv[e] = VBF16 ? cvt_bf16x2(p0, p1) : cvt_f16x2(p0, p1);
+      }
+      if constexpr (BN == 128) {
+        tmem_st64(tS, *reinterpret_cast<uint32_t(*)[64]>(sv));
+      } else {
+        tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(sv));
       }
       float la, lb, lc, ld;
       unpack2(lsum[0], la, lb);
