@@ -113,6 +113,15 @@ typedef struct ia_attn_params {
   int64_t lse_strides[2];       /* lse (b,h); query index contiguous */
   const float* v_scale;         /* optional fp32 [H, D], applied once to the output */
   const int32_t* kv_valid;      /* optional int32 [Sk/64] valid keys per 64-key tile */
+  int kv_splits;                /* 0 or 1: one pass over all keys. n >= 2 (at most 16): the
+                                   keys are cut into n ranges of whole key tiles (of the
+                                   kept-tile list with a block mask); each range is attended
+                                   separately into an fp32 partial (O, LSE) in `workspace`,
+                                   and the partials are merged exactly, as ia_merge_lse does,
+                                   into out and lse. Helps grids that cover the GPU poorly. */
+  void* workspace;              /* device scratch of ia_attention_workspace_size(p) bytes,
+                                   used only when kv_splits >= 2; owned by the caller */
+  size_t workspace_bytes;       /* its size, checked */
   uint64_t wait_timeout_ns;     /* limit of each device-side wait; 0 selects 2 s */
   int debug_stall;              /* test hook: nonzero makes one internal wait of every CTA
                                    wait for a signal that never comes, so the call ends
@@ -161,6 +170,38 @@ IA_API ia_status ia_attention_fwd(const int8_t* q_i8, const int8_t* k_i8, const 
                                   const float* k_scale, const void* v, const float* bias_or_null,
                                   const uint8_t* block_mask_or_null, void* out,
                                   float* lse_or_null, const ia_attn_params* p, void* stream);
+
+/*
+ * ia_attention_workspace_size -- bytes of scratch ia_attention_fwd needs for
+ * p->kv_splits (0 when kv_splits <= 1): kv_splits * B*H*Sq * (D + 1) * 4.
+ */
+IA_API size_t ia_attention_workspace_size(const ia_attn_params* p);
+
+/*
+ * ia_attention_default_splits -- the key split the library suggests for this
+ * shape on the current device: 1 unless the grid would occupy less than half
+ * of the SMs (short queries against long keys); then enough splits to fill
+ * them once, keeping at least 8 key tiles per split, at most 16.
+ * block_mask: nonzero if a block mask will be passed.
+ */
+IA_API int ia_attention_default_splits(const ia_attn_params* p, int block_mask);
+
+/*
+ * ia_merge_lse_n -- exact merge of n partial attentions over disjoint key sets
+ * (the many-way form of ia_merge_lse; "Add optional forward LSE output",
+ * Kernel implementation: the split-K combine reduces all splits, then stores
+ * the LSE from the combined maximum and denominator).
+ *
+ *   M = max_k L_k, w_k = e^{L_k - M}, L = M + ln sum_k w_k,
+ *   O = sum_k w_k O_k / sum_k w_k;  M = -inf gives O = 0, L = -inf.
+ * o_parts[k]: [B,H,Sq,D] contiguous of `dtype`; lse_parts[k]: fp32 [B,H,Sq]
+ * contiguous; the arrays of pointers live in host memory, 1 <= n <= 16.
+ * o_out, lse_out: contiguous; lse_out may be NULL; neither may alias an input.
+ * 16-byte aligned pointers.
+ */
+IA_API ia_status ia_merge_lse_n(const void* const* o_parts, const float* const* lse_parts, int n,
+                                void* o_out, float* lse_out, int B, int H, int Sq, int D,
+                                ia_dtype dtype, void* stream);
 
 /*
  * ia_merge_lse -- exact merge of two partial attentions over disjoint key sets.

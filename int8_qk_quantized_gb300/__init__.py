@@ -17,7 +17,7 @@ import os
 
 import torch
 
-__all__ = ["quantize_qk", "attention", "merge_lse", "device_status", "IAError", "lib_path",
+__all__ = ["quantize_qk", "attention", "merge_lse", "merge_lse_n", "device_status", "IAError", "lib_path",
            "load_library", "AttnParams", "BF16", "FP16", "PER_TOKEN", "PER_BLOCK64"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -46,6 +46,8 @@ class AttnParams(ctypes.Structure):
         ("v_strides", ctypes.c_int64 * 3), ("o_strides", ctypes.c_int64 * 3),
         ("lse_strides", ctypes.c_int64 * 2),
         ("v_scale", ctypes.c_void_p), ("kv_valid", ctypes.c_void_p),
+        ("kv_splits", ctypes.c_int), ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
         ("wait_timeout_ns", ctypes.c_uint64), ("debug_stall", ctypes.c_int),
     ]
 
@@ -72,6 +74,13 @@ def load_library():
     L.ia_attention_fwd.restype = i32
     L.ia_merge_lse.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
     L.ia_merge_lse.restype = i32
+    L.ia_merge_lse_n.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i32, vp, vp, i32, i32,
+                                 i32, i32, i32, vp]
+    L.ia_merge_lse_n.restype = i32
+    L.ia_attention_workspace_size.argtypes = [ctypes.POINTER(AttnParams)]
+    L.ia_attention_workspace_size.restype = ctypes.c_size_t
+    L.ia_attention_default_splits.argtypes = [ctypes.POINTER(AttnParams), i32]
+    L.ia_attention_default_splits.restype = i32
     L.ia_attn_params_init.argtypes = [ctypes.POINTER(AttnParams), i32, i32, i32, i32, i32, i32, i32]
     L.ia_attn_params_init.restype = None
     L.ia_device_status.argtypes = [vp]
@@ -166,12 +175,16 @@ def quantize_qk(q, k, granularity: str = "token", center_k: bool = True, kv_vali
 
 def attention(q8, k8, q_scale, k_scale, v, *, bias=None, block_mask=None, sm_scale=None,
               v_scale=None, kv_valid=None, granularity: str = "token", return_lse: bool = False,
-              out=None, lse=None, stream=None, wait_timeout_ns: int = 0, debug_stall: bool = False):
+              out=None, lse=None, stream=None, kv_splits=None, workspace=None,
+              wait_timeout_ns: int = 0, debug_stall: bool = False):
     """Forward attention on INT8 Q/K codes with a 16-bit P.V (see ``ia_attention_fwd``).
 
     ``bias`` is fp32 ``[Sk]`` (any ``[1,1,1,Sk]`` view), ``block_mask`` bool
     ``[B,H,ceil(Sq/64),ceil(Sk/64)]``, ``v_scale`` fp32 ``[H,D]``, ``kv_valid``
-    int32 ``[Sk/64]``. Returns ``out`` or ``(out, lse)``.
+    int32 ``[Sk/64]``. ``kv_splits``: None lets the library choose, 1 disables
+    the key split; with a split the scratch comes from ``workspace`` (a device
+    tensor of at least ``ia_attention_workspace_size`` bytes) or is allocated
+    here. Returns ``out`` or ``(out, lse)``.
     """
     L = load_library()
     B, H, Sq, D = q8.shape
@@ -183,6 +196,15 @@ def attention(q8, k8, q_scale, k_scale, v, *, bias=None, block_mask=None, sm_sca
     p.granularity = _gran_code(granularity)
     p.v_dtype = vd
     p.wait_timeout_ns = int(wait_timeout_ns)
+    if kv_splits is None:
+        kv_splits = L.ia_attention_default_splits(ctypes.byref(p), 1 if block_mask is not None else 0)
+    p.kv_splits = int(kv_splits)
+    if p.kv_splits > 1:
+        need = L.ia_attention_workspace_size(ctypes.byref(p))
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=v.device)
+        p.workspace = workspace.data_ptr()
+        p.workspace_bytes = workspace.numel() * workspace.element_size()
     p.debug_stall = 1 if debug_stall else 0
     if out is None:
         out = torch.empty((B, H, Sq, D), dtype=v.dtype, device=v.device)
@@ -235,6 +257,25 @@ def merge_lse(o1, lse1, o2, lse2, out=None, lse_out=None, stream=None):
         lse_out = torch.empty_like(lse1)
     _check(L.ia_merge_lse(_ptr(o1), _ptr(lse1), _ptr(o2), _ptr(lse2), _ptr(out), _ptr(lse_out),
                           B, H, Sq, D, _dtype_code(o1.dtype), _stream(stream)))
+    return out, lse_out
+
+
+def merge_lse_n(outs, lses, out=None, lse_out=None, stream=None):
+    """Exact merge of n partial attentions (contiguous, same shapes) through their LSEs."""
+    L = load_library()
+    n = len(outs)
+    B, H, Sq, D = outs[0].shape
+    for t in list(outs) + list(lses):
+        if not t.is_contiguous():
+            raise ValueError("merge_lse_n expects contiguous inputs")
+    if out is None:
+        out = torch.empty_like(outs[0])
+    if lse_out is None:
+        lse_out = torch.empty_like(lses[0])
+    op = (ctypes.c_void_p * n)(*[t.data_ptr() for t in outs])
+    lp = (ctypes.c_void_p * n)(*[t.data_ptr() for t in lses])
+    _check(L.ia_merge_lse_n(op, lp, n, _ptr(out), _ptr(lse_out), B, H, Sq, D,
+                            _dtype_code(outs[0].dtype), _stream(stream)))
     return out, lse_out
 
 

@@ -211,6 +211,15 @@ IA_API ia_status ia_attention_fwd(const int8_t* q_i8, const int8_t* k_i8, const 
     return fail(IA_ERR_INVALID_ARG, "kv_valid requires Sk to be a multiple of 64 (Sk=%d)", p->Sk);
   if (p->Sk > 65535 * 64)
     return fail(IA_ERR_UNSUPPORTED, "Sk too large (%d)", p->Sk);
+  if (p->kv_splits < 0 || p->kv_splits > ia::kMaxParts)
+    return fail(IA_ERR_INVALID_ARG, "kv_splits must be in [0, %d] (got %d)", ia::kMaxParts, p->kv_splits);
+  if (p->kv_splits > 1) {
+    const size_t need = ia_attention_workspace_size(p);
+    if (p->workspace == nullptr || p->workspace_bytes < need)
+      return fail(IA_ERR_INVALID_ARG, "kv_splits=%d needs a workspace of %zu bytes (got %zu)",
+                  p->kv_splits, need, p->workspace == nullptr ? static_cast<size_t>(0) : p->workspace_bytes);
+    if (!aligned16(p->workspace)) return fail(IA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  }
   float sm = p->sm_scale;
   if (std::isnan(sm)) sm = 1.0f / std::sqrt(static_cast<float>(p->D));
   if (!std::isfinite(sm) || sm <= 0.f) return fail(IA_ERR_INVALID_ARG, "sm_scale must be positive");
@@ -229,9 +238,79 @@ IA_API ia_status ia_attention_fwd(const int8_t* q_i8, const int8_t* k_i8, const 
   a.lse = lse_or_null;
   a.p = *p;
   a.sm_scale = sm;
+  a.workspace = p->kv_splits > 1 ? p->workspace : nullptr;
   const char* msg = "";
   s = ia::launch_attention(a, sms, static_cast<cudaStream_t>(stream), &msg);
   if (s != IA_OK) return fail(s, "attention: %s", msg);
+  return ok();
+}
+
+IA_API size_t ia_attention_workspace_size(const ia_attn_params* p) {
+  if (p == nullptr || p->kv_splits <= 1 || p->B <= 0 || p->H <= 0 || p->Sq <= 0) return 0;
+  return static_cast<size_t>(p->kv_splits) * static_cast<size_t>(p->B) * p->H * p->Sq *
+         (static_cast<size_t>(p->D) + 1) * sizeof(float);
+}
+
+IA_API int ia_attention_default_splits(const ia_attn_params* p, int block_mask) {
+  if (p == nullptr || p->B <= 0 || p->H <= 0 || p->Sq <= 0 || p->Sk <= 0) return 1;
+  int sms = 0;
+  if (check_device(&sms) != IA_OK) return 1;
+  // one dense CTA (256 query rows) per SM; two block-sparse CTAs (128 rows)
+  const int64_t rows_per_cta = block_mask ? 128 : 256;
+  const int64_t slots = static_cast<int64_t>(sms) * (block_mask ? 2 : 1);
+  const int64_t ctas = (static_cast<int64_t>(p->Sq) + rows_per_cta - 1) / rows_per_cta * p->H * p->B;
+  // A split CTA pays a fixed prologue/epilogue and the merge; splitting pays
+  // only when the grid leaves most SMs idle (short queries, long keys).
+  if (2 * ctas > slots) return 1;
+  int64_t n = slots / ctas;
+  const int64_t tile = block_mask ? 64 : 128;
+  const int64_t tiles = (p->Sk + tile - 1) / tile;
+  const int64_t cap = tiles / 8;  // at least 8 key tiles per split
+  if (n > cap) n = cap;
+  if (n > ia::kMaxParts) n = ia::kMaxParts;
+  return n < 2 ? 1 : static_cast<int>(n);
+}
+
+IA_API ia_status ia_merge_lse_n(const void* const* o_parts, const float* const* lse_parts, int n,
+                                void* o_out, float* lse_out, int B, int H, int Sq, int D,
+                                ia_dtype dtype, void* stream) {
+  if (B < 0 || H < 0 || Sq < 0) return fail(IA_ERR_INVALID_ARG, "negative shape");
+  if (D != 64 && D != 128) return fail(IA_ERR_INVALID_ARG, "D must be 64 or 128 (got %d)", D);
+  if (dtype != IA_BF16 && dtype != IA_FP16) return fail(IA_ERR_INVALID_ARG, "dtype");
+  if (n < 1 || n > ia::kMaxParts) return fail(IA_ERR_INVALID_ARG, "n must be in [1, %d]", ia::kMaxParts);
+  if (static_cast<int64_t>(B) * H * Sq == 0) return ok();
+  if (o_parts == nullptr || lse_parts == nullptr || o_out == nullptr)
+    return fail(IA_ERR_INVALID_ARG, "a required pointer is NULL");
+  for (int k = 0; k < n; ++k) {
+    if (o_parts[k] == nullptr || lse_parts[k] == nullptr)
+      return fail(IA_ERR_INVALID_ARG, "partial %d is NULL", k);
+    if (!aligned16(o_parts[k])) return fail(IA_ERR_INVALID_ARG, "partial %d is not 16-byte aligned", k);
+  }
+  if (!aligned16(o_out)) return fail(IA_ERR_INVALID_ARG, "o_out must be 16-byte aligned");
+  int sms = 0;
+  ia_status s = check_device(&sms);
+  if (s != IA_OK) return s;
+  ia::MergeNArgs a{};
+  for (int k = 0; k < n; ++k) {
+    a.o[k] = o_parts[k];
+    a.l[k] = lse_parts[k];
+  }
+  a.n = n;
+  a.in_f32 = 0;
+  a.out = o_out;
+  a.lse = lse_out;
+  a.B = B;
+  a.H = H;
+  a.Sq = Sq;
+  a.D = D;
+  a.dtype = dtype;
+  a.o_sb = static_cast<int64_t>(H) * Sq * D;
+  a.o_sh = static_cast<int64_t>(Sq) * D;
+  a.o_ss = D;
+  a.l_sb = static_cast<int64_t>(H) * Sq;
+  a.l_sh = Sq;
+  cudaError_t e = ia::launch_merge_n(a, sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(IA_ERR_CUDA, "merge_n: %s", cudaGetErrorString(e));
   return ok();
 }
 

@@ -99,6 +99,11 @@ struct Params {
   int64_t l_sb, l_sh;
   unsigned long long timeout_ns;
   int debug_stall;
+  int nsplit;        // key ranges per (query tiles, head); 1 = no split
+  int tps;           // dense: key tiles per range
+  float* ws_o;       // nsplit >= 2: fp32 partial O [nsplit][B][H][Sq][D]
+  float* ws_l;       //              fp32 partial LSE [nsplit][B][H][Sq]
+  int B;
 };
 
 template <int D, int QS, int BN, bool SPARSE>
@@ -224,7 +229,9 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.y, b = blockIdx.z;
+  const int h = blockIdx.y;
+  const int b = blockIdx.z / a.nsplit;
+  const int split = blockIdx.z % a.nsplit;
   const int q0 = blockIdx.x * (kM * QS);
 
   if ((smem_u32(smem) & 1023u) != 0) {  // swizzled operands need 1024-byte alignment
@@ -274,7 +281,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
   // Key tiles this CTA visits: all of them (dense) or the union of the kept
   // tiles of its two 64-row query tiles, in ascending order (block-sparse).
   uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::OFF_LIST);
-  int n_it;
+  int n_it, it0;
   const int qt0 = q0 / 64;
   const int qt1 = qt0 + 1;
   if constexpr (SPARSE) {
@@ -295,9 +302,13 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       for (int w = 0; w < nw; ++w) total += wcnt[w];
       __syncthreads();
     }
-    n_it = total;
+    // this CTA's share of the kept-tile list
+    const int per = (total + a.nsplit - 1) / a.nsplit;
+    it0 = split * per;
+    n_it = max(0, min(total - it0, per));
   } else {
-    n_it = a.n_tiles;
+    it0 = split * a.tps;
+    n_it = max(0, min(a.n_tiles - it0, a.tps));
   }
   tc_fence_before();
   __syncthreads();
@@ -323,7 +334,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         tma_load_4d(sm_v + s * L::QR, &tm_q, bar(L::B_QFULL), 0, q0 + s * kM, h, b);
       bool ok = true;
       for (int it = 0; it < n_it; ++it) {
-        const int kt = SPARSE ? static_cast<int>(list[it]) : it;
+        const int kt = SPARSE ? static_cast<int>(list[it0 + it]) : it0 + it;
         // int8 K tile: into its fp16 buffer (in place) or a staging buffer
         const int ks = it % L::NKS;
         uint32_t kdst;
@@ -455,7 +466,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     }
     const float* ksb = a.k_scale + b * a.ks_sb + h * a.ks_sh;
     for (int it = 0; it < n_it && ok; ++it) {
-      const int kt = SPARSE ? static_cast<int>(list[it]) : it;
+      const int kt = SPARSE ? static_cast<int>(list[it0 + it]) : it0 + it;
       // Per-key constants of this tile: the global loads are issued first and
       // land while the K tile is widened.
       constexpr int KPT = (BN + 63) / 64;  // keys per converter thread
@@ -671,16 +682,30 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
           if (pad) o0 = o1 = 0.f;
           pk[i] = VBF16 ? cvt_bf16x2(o0, o1) : cvt_f16x2(o0, o1);
         }
-        if (row_ok) {
+        if (row_ok && a.ws_o != nullptr) {  // fp32 partial of this key range
+          float4* dst = reinterpret_cast<float4*>(
+              a.ws_o + ((static_cast<int64_t>(split * a.B + b) * a.H + h) * a.Sq + row) * D + c0);
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4) {
+            float f[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              f[e] = pad ? 0.f : __uint_as_float(rr[4 * v4 + e]) * inv_l * vsc[c0 + 4 * v4 + e];
+            dst[v4] = make_float4(f[0], f[1], f[2], f[3]);
+          }
+        } else if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c0 * 2);
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4)
             dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
         }
       }
-      if (row_ok && a.lse != nullptr) {
+      if (row_ok && (a.lse != nullptr || a.ws_l != nullptr)) {
         const float lse = (pad || !(l > 0.f)) ? -INFINITY : (m + log2f(l)) * kLn2;
-        a.lse[b * a.l_sb + h * a.l_sh + row] = lse;
+        if (a.ws_l != nullptr)
+          a.ws_l[(static_cast<int64_t>(split * a.B + b) * a.H + h) * a.Sq + row] = lse;
+        else
+          a.lse[b * a.l_sb + h * a.l_sh + row] = lse;
       }
     }
   }
@@ -777,6 +802,17 @@ ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** ms
   a.l_sh = p.lse_strides[1];
   a.timeout_ns = p.wait_timeout_ns ? p.wait_timeout_ns : 2000000000ull;
   a.debug_stall = p.debug_stall;
+  a.B = p.B;
+  const int nsplit = p.kv_splits > 1 ? p.kv_splits : 1;
+  a.nsplit = nsplit;
+  a.tps = (a.n_tiles + nsplit - 1) / nsplit;
+  a.ws_o = nullptr;
+  a.ws_l = nullptr;
+  const int64_t rows = static_cast<int64_t>(p.B) * p.H * p.Sq;
+  if (nsplit > 1) {
+    a.ws_o = static_cast<float*>(A.workspace);
+    a.ws_l = a.ws_o + static_cast<int64_t>(nsplit) * rows * D;
+  }
   const size_t smem = L::SMEM_FIXED + (SPARSE ? static_cast<size_t>(a.Tk) * 2 : 0);
   auto kern = attn_fwd_kernel<D, QS, BN, SPARSE, VBF16>;
   if (smem > 232448) {
@@ -789,14 +825,39 @@ ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** ms
     *msg = cudaGetErrorString(e);
     return IA_ERR_CUDA;
   }
-  dim3 grid((p.Sq + kM * QS - 1) / (kM * QS), p.H, p.B);
+  dim3 grid((p.Sq + kM * QS - 1) / (kM * QS), p.H, p.B * nsplit);
   kern<<<grid, L::NWARPS * 32, smem, st>>>(tq, tk, tv, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     *msg = cudaGetErrorString(e);
     return IA_ERR_CUDA;
   }
-  (void)num_sms;
+  if (nsplit > 1) {  // exact merge of the key ranges
+    MergeNArgs m{};
+    for (int k = 0; k < nsplit; ++k) {
+      m.o[k] = a.ws_o + static_cast<int64_t>(k) * rows * D;
+      m.l[k] = a.ws_l + static_cast<int64_t>(k) * rows;
+    }
+    m.n = nsplit;
+    m.in_f32 = 1;
+    m.out = A.out;
+    m.lse = A.lse;
+    m.B = p.B;
+    m.H = p.H;
+    m.Sq = p.Sq;
+    m.D = D;
+    m.dtype = VBF16 ? IA_BF16 : IA_FP16;
+    m.o_sb = p.o_strides[0];
+    m.o_sh = p.o_strides[1];
+    m.o_ss = p.o_strides[2];
+    m.l_sb = p.lse_strides[0];
+    m.l_sh = p.lse_strides[1];
+    e = launch_merge_n(m, num_sms, st);
+    if (e != cudaSuccess) {
+      *msg = cudaGetErrorString(e);
+      return IA_ERR_CUDA;
+    }
+  }
   return IA_OK;
 }
 

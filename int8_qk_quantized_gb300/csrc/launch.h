@@ -38,7 +38,27 @@ struct MergeArgs {
 
 cudaError_t launch_merge(const MergeArgs& a, int num_sms, cudaStream_t st);
 
+constexpr int kMaxParts = 16;
+
+// n-way merge of partial attentions: part k is o[k] ([B,H,Sq,D] contiguous,
+// fp32 when in_f32 else `dtype`) and l[k] (fp32 [B,H,Sq] contiguous).
+struct MergeNArgs {
+  const void* o[kMaxParts];
+  const float* l[kMaxParts];
+  int n;
+  int in_f32;
+  void* out;                 // `dtype`, strides (b,h,s) in elements
+  float* lse;                // optional, strides (b,h)
+  int B, H, Sq, D;
+  int dtype;
+  int64_t o_sb, o_sh, o_ss;
+  int64_t l_sb, l_sh;
+};
+
+cudaError_t launch_merge_n(const MergeNArgs& a, int num_sms, cudaStream_t st);
+
 struct AttnLaunch {
+  void* workspace;  // fp32 partials when p.kv_splits >= 2
   const int8_t* q;
   const int8_t* k;
   const float* q_scale;

@@ -107,7 +107,79 @@ cudaError_t launch_d(const MergeArgs& a, int num_sms, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// n-way merge: a row is D/8 threads holding 8 output elements each.
+template <int D, int DT, bool IN_F32>
+__global__ void __launch_bounds__(kThreads) merge_n_kernel(const MergeNArgs a) {
+  constexpr int TPR = D / 8;
+  constexpr int RPP = kThreads / TPR;
+  const int tc = threadIdx.x % TPR;
+  const int64_t rows = static_cast<int64_t>(a.B) * a.H * a.Sq;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * RPP;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPP; base < rows; base += stride) {
+    const int64_t r = base + threadIdx.x / TPR;
+    if (r >= rows) continue;
+    float m = -INFINITY;
+    for (int k = 0; k < a.n; ++k) m = fmaxf(m, a.l[k][r]);
+    float o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = 0.f;
+    float lse = -INFINITY;
+    if (m != -INFINITY) {
+      float den = 0.f;
+      for (int k = 0; k < a.n; ++k) {
+        const float w = expf(a.l[k][r] - m);  // 0 for an empty partial
+        den += w;
+        float x[8];
+        if (IN_F32) {
+          const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(a.o[k]) + r * D + tc * 8);
+          const float4 x0 = src[0], x1 = src[1];
+          x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+          x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
+        } else {
+          const uint4 w16 = *reinterpret_cast<const uint4*>(static_cast<const char*>(a.o[k]) + (r * D + tc * 8) * 2);
+          unpack8<DT>(w16, x);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] += w * x[i];
+      }
+      const float inv = 1.f / den;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] *= inv;
+      lse = m + logf(den);
+    }
+    const int64_t sidx = r % a.Sq;
+    const int64_t bh = r / a.Sq;
+    const int64_t hh = bh % a.H, bb = bh / a.H;
+    char* dst = static_cast<char*>(a.out) + (bb * a.o_sb + hh * a.o_sh + sidx * a.o_ss + tc * 8) * 2;
+    *reinterpret_cast<uint4*>(dst) = pack8<DT>(o);
+    if (a.lse && tc == 0) a.lse[bb * a.l_sb + hh * a.l_sh + sidx] = lse;
+  }
+}
+
+template <int D>
+cudaError_t launch_n_d(const MergeNArgs& a, int num_sms, cudaStream_t st) {
+  constexpr int RPP = kThreads / (D / 8);
+  const int64_t rows = static_cast<int64_t>(a.B) * a.H * a.Sq;
+  int64_t blocks = (rows + RPP - 1) / RPP;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  const int g = static_cast<int>(blocks);
+  if (a.in_f32) {
+    if (a.dtype == IA_BF16) merge_n_kernel<D, IA_BF16, true><<<g, kThreads, 0, st>>>(a);
+    else merge_n_kernel<D, IA_FP16, true><<<g, kThreads, 0, st>>>(a);
+  } else {
+    if (a.dtype == IA_BF16) merge_n_kernel<D, IA_BF16, false><<<g, kThreads, 0, st>>>(a);
+    else merge_n_kernel<D, IA_FP16, false><<<g, kThreads, 0, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_merge_n(const MergeNArgs& a, int num_sms, cudaStream_t st) {
+  if (static_cast<int64_t>(a.B) * a.H * a.Sq == 0) return cudaSuccess;
+  return a.D == 128 ? launch_n_d<128>(a, num_sms, st) : launch_n_d<64>(a, num_sms, st);
+}
 
 cudaError_t launch_merge(const MergeArgs& a, int num_sms, cudaStream_t st) {
   if (a.rows == 0) return cudaSuccess;

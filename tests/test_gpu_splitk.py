@@ -1,0 +1,94 @@
+"""Key-split attention and the n-way LSE merge against the oracle.
+
+A split call attends each range of key tiles separately into fp32 partials and
+merges them exactly ("Add optional forward LSE output", Kernel implementation:
+split-K combine); the result must meet the same bar as one pass over all keys.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from util import assert_lse_close, assert_out_close, ensure_built, to_np
+from workloads import WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+
+
+def oracle_full(inp, wl):
+    vbs = None if inp.kv_valid is None else inp.kv_valid.cpu().numpy()
+    o, lse, _ = oracle.quantize_and_attend(
+        to_np(inp.q), to_np(inp.k), to_np(inp.v), granularity=wl.granularity, kv_valid=vbs,
+        bias=None if inp.bias is None else to_np(inp.bias),
+        block_mask=None if inp.block_mask is None else to_np(inp.block_mask),
+        v_scale=None if inp.v_scale is None else to_np(inp.v_scale))
+    return o, lse
+
+
+CASES = [
+    ("anima4k", dict(H=2, Sq=700, Sk=2000)),
+    ("banded", dict(H=2, Sq=300, Sk=2500, skirt_width=500)),
+    ("sdxl", dict(H=2, Sq=1000, Sk=1000)),
+    ("sparse", dict(H=2, Sq=2048, Sk=2048, band_tiles=8, random_tiles=4)),
+]
+
+
+@pytest.mark.parametrize("name,kw", CASES)
+@pytest.mark.parametrize("splits", [2, 3, 5])
+def test_split_matches_oracle_and_unsplit(name, kw, splits):
+    import int8_qk_quantized_gb300 as ia
+    wl = WORKLOADS[name].with_(**kw)
+    inp = make_inputs(wl, "cuda")
+    q8, qs, k8, ks = ia.quantize_qk(inp.q, inp.k, granularity=wl.granularity, kv_valid=inp.kv_valid)
+    args = dict(bias=inp.bias, block_mask=inp.block_mask, v_scale=inp.v_scale,
+                kv_valid=inp.kv_valid, granularity=wl.granularity, return_lse=True)
+    o1, l1 = ia.attention(q8, k8, qs, ks, inp.v, kv_splits=1, **args)
+    os_, ls = ia.attention(q8, k8, qs, ks, inp.v, kv_splits=splits, **args)
+    ia.device_status()
+    d = (os_.float() - o1.float()).abs()
+    assert d.max().item() < 2e-2 and d.mean().item() < 1e-3
+    ro, rl = oracle_full(inp, wl)
+    valid = None
+    if inp.kv_valid is not None:
+        valid = oracle.row_validity(wl.Sq, inp.kv_valid.cpu().numpy())
+    assert_out_close(to_np(os_), ro, valid=valid)
+    assert_lse_close(to_np(ls), rl)
+
+
+def test_more_splits_than_tiles_and_workspace_checks():
+    import int8_qk_quantized_gb300 as ia
+    wl = WORKLOADS["anima4k"].with_(H=1, Sq=200, Sk=300, v_scale=False)  # 3 key tiles
+    inp = make_inputs(wl, "cuda")
+    q8, qs, k8, ks = ia.quantize_qk(inp.q, inp.k)
+    o, l = ia.attention(q8, k8, qs, ks, inp.v, kv_splits=7, return_lse=True)
+    ia.device_status()
+    ro, rl = oracle_full(inp, wl)
+    assert_out_close(to_np(o), ro)
+    assert_lse_close(to_np(l), rl)
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ia.IAError, match="workspace"):
+        ia.attention(q8, k8, qs, ks, inp.v, kv_splits=2, workspace=small)
+
+
+def test_merge_n_of_key_ranges_equals_oracle():
+    import int8_qk_quantized_gb300 as ia
+    wl = WORKLOADS["banded"].with_(H=3, Sq=500, Sk=3000, skirt_width=600)
+    inp = make_inputs(wl, "cuda")
+    q8, qs, k8, ks = ia.quantize_qk(inp.q, inp.k)
+    cuts = [0, 640, 1920, 3000]
+    outs, lses = [], []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        o, l = ia.attention(q8, k8[:, :, a:b], qs, ks[:, :, a:b], inp.v[:, :, a:b],
+                            bias=inp.bias[a:b], return_lse=True, kv_splits=1)
+        outs.append(o)
+        lses.append(l)
+    mo, ml = ia.merge_lse_n(outs, lses)
+    ia.device_status()
+    ro, rl = oracle_full(inp, wl)
+    assert_out_close(to_np(mo), ro)
+    assert_lse_close(to_np(ml), rl)
