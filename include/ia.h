@@ -179,9 +179,13 @@ IA_API size_t ia_attention_workspace_size(const ia_attn_params* p);
 
 /*
  * ia_attention_default_splits -- the key split the library suggests for this
- * shape on the current device: 1 unless the grid would occupy less than half
- * of the SMs (short queries against long keys); then enough splits to fill
- * them once, keeping at least 8 key tiles per split, at most 16.
+ * shape on the current device, from a cost model: the grid runs in rounds of
+ * one CTA per SM (two with a block mask), each CTA costs a fixed prologue and
+ * epilogue plus its share of the key tiles, and each split adds an fp32
+ * partial written and read back by the merge. A split is suggested only when
+ * the model expects it to save at least 5%, which happens when the grid
+ * covers the SMs poorly (short queries against long keys); with a block mask
+ * only when the grid is under one wave. Returns 1..16.
  * block_mask: nonzero if a block mask will be passed.
  */
 IA_API int ia_attention_default_splits(const ia_attn_params* p, int block_mask);

@@ -259,15 +259,32 @@ IA_API int ia_attention_default_splits(const ia_attn_params* p, int block_mask) 
   const int64_t rows_per_cta = block_mask ? 128 : 256;
   const int64_t slots = static_cast<int64_t>(sms) * (block_mask ? 2 : 1);
   const int64_t ctas = (static_cast<int64_t>(p->Sq) + rows_per_cta - 1) / rows_per_cta * p->H * p->B;
-  // A split CTA pays a fixed prologue/epilogue and the merge; splitting pays
-  // only when the grid leaves most SMs idle (short queries, long keys).
-  if (2 * ctas > slots) return 1;
-  int64_t n = slots / ctas;
+  // With a block mask the kept tiles per CTA are unknown here and uneven; a
+  // grid of a wave or more balances itself.
+  if (block_mask && ctas >= slots) return 1;
+  // Cost model in units of one CTA's key-tile iteration: a CTA costs a fixed
+  // prologue/epilogue (kFixed tiles) plus its share of the key tiles; the
+  // grid runs in ceil(ctas*n / slots) rounds; each split adds the write and
+  // the merge read of an fp32 partial (B*H*Sq*(D+1)*8 bytes), converted at
+  // kBytesPerTile bytes of HBM traffic per tile time.
+  constexpr int64_t kFixed = 4;
+  constexpr double kBytesPerTile = 14.0e6;
   const int64_t tile = block_mask ? 64 : 128;
   const int64_t tiles = (p->Sk + tile - 1) / tile;
-  const int64_t cap = tiles / 8;  // at least 8 key tiles per split
-  if (n > cap) n = cap;
-  if (n > ia::kMaxParts) n = ia::kMaxParts;
+  const double merge_per_split =
+      static_cast<double>(p->B) * p->H * p->Sq * (p->D + 1) * 8.0 / kBytesPerTile;
+  int64_t best = 1;
+  double best_cost = 0.0;
+  for (int64_t n = 1; n <= ia::kMaxParts && n <= tiles; ++n) {
+    const int64_t rounds = (ctas * n + slots - 1) / slots;
+    double cost = static_cast<double>(rounds) * (kFixed + (tiles + n - 1) / n);
+    if (n > 1) cost += merge_per_split * static_cast<double>(n);
+    if (n == 1 || cost < best_cost * (best == 1 ? 0.95 : 1.0)) {
+      best = n;
+      best_cost = cost;
+    }
+  }
+  const int64_t n = best;
   return n < 2 ? 1 : static_cast<int>(n);
 }
 
