@@ -178,6 +178,43 @@ IA_API ia_status ia_attention_fwd(const int8_t* q_i8, const int8_t* k_i8, const 
 IA_API size_t ia_attention_workspace_size(const ia_attn_params* p);
 
 /*
+ * ia_attention_fwd_static_workspace -- ia_attention_fwd for callers that must
+ * not allocate device memory per call. The paper has no counterpart: it is an
+ * integration entry point of this library.
+ *
+ * Who needs it: a caller embedded in a runtime that owns all device memory
+ * and hands out no allocator (a plugin inside an inference server, a C
+ * program with its own pool), a latency-critical loop that cannot afford
+ * cudaMalloc/cudaFree (both may synchronise the device), or a process whose
+ * memory budget is fixed at start-up. Such a caller cannot provide the
+ * kv_splits >= 2 workspace that ia_attention_fwd asks for.
+ *
+ * Same arguments, results and errors as ia_attention_fwd, except that
+ * p->workspace and p->workspace_bytes are ignored: with kv_splits >= 2 the
+ * fp32 partials go to a fixed scratch array inside the library, of
+ * IA_STATIC_WORKSPACE_BYTES per device. A call whose
+ * ia_attention_workspace_size(p) exceeds that returns IA_ERR_INVALID_ARG
+ * before any work. The call allocates nothing (no cudaMalloc, no cudaFree, no
+ * allocating library routine).
+ *
+ * Set-up: the first call on each device, with that device current, looks up
+ * the array's device address (cudaGetSymbolAddress) and caches it; make that
+ * first call before any stream capture.
+ *
+ * Sharing: every call on a device uses the same array, and the array keeps
+ * the last call's contents. Nothing in it needs to start at zero: every entry
+ * the merge reads is written earlier in the same call. Calls that overlap on
+ * the GPU (different streams, or host threads launching concurrently) race on
+ * the array and give wrong results; calls on one stream are ordered and safe.
+ */
+#define IA_STATIC_WORKSPACE_BYTES ((size_t)64 << 20) /* 64 MiB per device */
+
+IA_API ia_status ia_attention_fwd_static_workspace(
+    const int8_t* q_i8, const int8_t* k_i8, const float* q_scale, const float* k_scale,
+    const void* v, const float* bias_or_null, const uint8_t* block_mask_or_null, void* out,
+    float* lse_or_null, const ia_attn_params* p, void* stream);
+
+/*
  * ia_attention_default_splits -- the key split the library suggests for this
  * shape on the current device, from a cost model: the grid runs in rounds of
  * one CTA per SM (two with a block mask), each CTA costs a fixed prologue and

@@ -72,6 +72,8 @@ def load_library():
     L.ia_attention_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                    ctypes.POINTER(AttnParams), vp]
     L.ia_attention_fwd.restype = i32
+    L.ia_attention_fwd_static_workspace.argtypes = L.ia_attention_fwd.argtypes
+    L.ia_attention_fwd_static_workspace.restype = i32
     L.ia_merge_lse.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
     L.ia_merge_lse.restype = i32
     L.ia_merge_lse_n.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(vp), i32, vp, vp, i32, i32,
@@ -242,6 +244,70 @@ def attention(q8, k8, q_scale, k_scale, v, *, bias=None, block_mask=None, sm_sca
                               _ptr(bias), _ptr(block_mask), _ptr(out), _ptr(lse),
                               ctypes.byref(p), _stream(stream)))
     return (out, lse) if return_lse else out
+
+
+STATIC_WORKSPACE_BYTES = 64 << 20  # IA_STATIC_WORKSPACE_BYTES: fixed scratch per device
+
+
+def attention_static_workspace(q8, k8, q_scale, k_scale, v, out, *, lse=None, bias=None,
+                               block_mask=None, sm_scale=None, v_scale=None, kv_valid=None,
+                               granularity: str = "token", kv_splits: int = 1, stream=None):
+    """``ia_attention_fwd_static_workspace``: attention that allocates nothing.
+
+    For callers that cannot allocate device memory per call (a plugin inside
+    a runtime that owns the memory, a latency-critical loop that cannot pay
+    for cudaMalloc/cudaFree, a fixed memory budget). With ``kv_splits >= 2``
+    the partials go to the library's fixed per-device scratch
+    (``IA_STATIC_WORKSPACE_BYTES``) instead of a caller workspace. Nothing is
+    allocated here either: ``out`` (and ``lse`` if wanted) are given, and
+    ``v_scale`` / ``kv_valid`` must already be contiguous fp32 / int32 device
+    tensors. Calls that overlap on the GPU share the scratch and race; calls
+    on one stream are safe. The first call on a device looks up the scratch
+    address, so make it before any stream capture. Returns ``out`` or
+    ``(out, lse)`` when ``lse`` is given.
+    """
+    L = load_library()
+    B, H, Sq, D = q8.shape
+    Sk = k8.shape[2]
+    p = AttnParams()
+    p.B, p.H, p.Sq, p.Sk, p.D = B, H, Sq, Sk, D
+    p.sm_scale = float("nan") if sm_scale is None else float(sm_scale)
+    p.granularity = _gran_code(granularity)
+    p.v_dtype = _dtype_code(v.dtype)
+    p.kv_splits = int(kv_splits)
+    if out.shape != (B, H, Sq, D) or out.dtype != v.dtype:
+        raise ValueError("out must be [B,H,Sq,D] of V's dtype")
+    for name, t in (("q_strides", q8), ("k_strides", k8), ("v_strides", v), ("o_strides", out)):
+        getattr(p, name)[:] = list(_strides3(t))
+    for name, t in (("qs_strides", q_scale), ("ks_strides", k_scale)):
+        if t.dim() != 3 or t.stride(2) != 1:
+            raise ValueError("scales must be [B,H,n] with a contiguous last dimension")
+        getattr(p, name)[:] = [t.stride(0), t.stride(1)]
+    if lse is not None:
+        if lse.shape != (B, H, Sq) or lse.dtype != torch.float32 or lse.stride(2) != 1:
+            raise ValueError("lse must be fp32 [B,H,Sq] with a contiguous last dimension")
+        p.lse_strides[:] = [lse.stride(0), lse.stride(1)]
+    if bias is not None:
+        bias = bias.reshape(-1)
+        if bias.dtype != torch.float32 or bias.numel() != Sk or not bias.is_contiguous():
+            raise ValueError("bias must be a contiguous fp32 tensor with Sk elements")
+    if block_mask is not None:
+        if block_mask.dtype not in (torch.bool, torch.uint8) or not block_mask.is_contiguous():
+            raise ValueError("block_mask must be a contiguous bool/uint8 tensor")
+        if tuple(block_mask.shape) != (B, H, (Sq + 63) // 64, (Sk + 63) // 64):
+            raise ValueError("block_mask must be [B, H, ceil(Sq/64), ceil(Sk/64)]")
+    if v_scale is not None:
+        if v_scale.shape != (H, D) or v_scale.dtype != torch.float32 or not v_scale.is_contiguous():
+            raise ValueError("v_scale must be a contiguous fp32 [H, D] tensor")
+        p.v_scale = v_scale.data_ptr()
+    if kv_valid is not None:
+        if kv_valid.dtype != torch.int32 or not kv_valid.is_contiguous():
+            raise ValueError("kv_valid must be a contiguous int32 tensor")
+        p.kv_valid = kv_valid.data_ptr()
+    _check(L.ia_attention_fwd_static_workspace(
+        _ptr(q8), _ptr(k8), _ptr(q_scale), _ptr(k_scale), _ptr(v), _ptr(bias), _ptr(block_mask),
+        _ptr(out), _ptr(lse), ctypes.byref(p), _stream(stream)))
+    return out if lse is None else (out, lse)
 
 
 def merge_lse(o1, lse1, o2, lse2, out=None, lse_out=None, stream=None):

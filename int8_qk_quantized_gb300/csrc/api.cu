@@ -1,6 +1,7 @@
 // C ABI of libia.so: argument checking, status codes and dispatch to the
 // kernel launchers. Nothing here allocates device memory or synchronises
 // (except ia_device_status, which exists to synchronise).
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -60,6 +61,32 @@ bool strides_ok(const int64_t* st, int n, int64_t esize) {
   for (int i = 0; i < n; ++i)
     if (st[i] < 0 || ((st[i] * esize) & 15) != 0) return false;
   return true;
+}
+
+// Fixed scratch of ia_attention_fwd_static_workspace: one array per device,
+// shared by every call of that entry point on the device.
+static __device__ __align__(256) unsigned char g_static_workspace[IA_STATIC_WORKSPACE_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::atomic<void*> g_static_workspace_ptr[kMaxDevices];
+
+// Device address of g_static_workspace on the current device, looked up once
+// per device with that device current.
+ia_status static_workspace(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(IA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(IA_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev, kMaxDevices);
+  void* ptr = g_static_workspace_ptr[dev].load(std::memory_order_acquire);
+  if (ptr == nullptr) {
+    e = cudaGetSymbolAddress(&ptr, g_static_workspace);
+    if (e != cudaSuccess || ptr == nullptr)
+      return fail(IA_ERR_CUDA, "cudaGetSymbolAddress(static workspace): %s", cudaGetErrorString(e));
+    g_static_workspace_ptr[dev].store(ptr, std::memory_order_release);
+  }
+  *out = ptr;
+  return IA_OK;
 }
 
 }  // namespace
@@ -243,6 +270,33 @@ IA_API ia_status ia_attention_fwd(const int8_t* q_i8, const int8_t* k_i8, const 
   s = ia::launch_attention(a, sms, static_cast<cudaStream_t>(stream), &msg);
   if (s != IA_OK) return fail(s, "attention: %s", msg);
   return ok();
+}
+
+IA_API ia_status ia_attention_fwd_static_workspace(
+    const int8_t* q_i8, const int8_t* k_i8, const float* q_scale, const float* k_scale,
+    const void* v, const float* bias_or_null, const uint8_t* block_mask_or_null, void* out,
+    float* lse_or_null, const ia_attn_params* p, void* stream) {
+  if (p == nullptr) return fail(IA_ERR_INVALID_ARG, "params is NULL");
+  ia_attn_params q = *p;
+  q.workspace = nullptr;
+  q.workspace_bytes = 0;
+  if (q.kv_splits > 1) {
+    const size_t need = ia_attention_workspace_size(&q);
+    if (need > IA_STATIC_WORKSPACE_BYTES)
+      return fail(IA_ERR_INVALID_ARG,
+                  "kv_splits=%d needs %zu bytes of scratch; the fixed workspace holds %zu "
+                  "(use fewer splits, or ia_attention_fwd with a caller workspace)",
+                  q.kv_splits, need, static_cast<size_t>(IA_STATIC_WORKSPACE_BYTES));
+  }
+  void* ws = nullptr;
+  ia_status s = static_workspace(&ws);
+  if (s != IA_OK) return s;
+  if (q.kv_splits > 1) {
+    q.workspace = ws;
+    q.workspace_bytes = IA_STATIC_WORKSPACE_BYTES;
+  }
+  return ia_attention_fwd(q_i8, k_i8, q_scale, k_scale, v, bias_or_null, block_mask_or_null, out,
+                          lse_or_null, &q, stream);
 }
 
 IA_API size_t ia_attention_workspace_size(const ia_attn_params* p) {

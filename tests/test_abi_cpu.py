@@ -133,3 +133,20 @@ def test_binding_raises_when_library_missing(tmp_path, monkeypatch):
     monkeypatch.setattr(ia, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         ia.load_library()
+
+
+def test_static_workspace_limit_checked_before_any_work(lib):
+    import re
+    import int8_qk_quantized_gb300 as ia
+    m = re.search(r"#define IA_STATIC_WORKSPACE_BYTES \(\(size_t\)(\d+) << (\d+)\)", open(HEADER).read())
+    assert m and int(m.group(1)) << int(m.group(2)) == ia.STATIC_WORKSPACE_BYTES
+    fake = ctypes.c_void_p(0x1000)
+    p = _params(lib, Sq=4096, Sk=4096)
+    p.H = 16
+    p.kv_splits = 8  # 8 * 16 * 4096 * 129 * 4 bytes of partials > the fixed scratch
+    assert lib.ia_attention_workspace_size(ctypes.byref(p)) > ia.STATIC_WORKSPACE_BYTES
+    assert lib.ia_attention_fwd_static_workspace(fake, fake, fake, fake, fake, None, None, fake,
+                                                 None, ctypes.byref(p), None) == 1
+    assert b"fixed workspace" in lib.ia_last_error_message()
+    assert lib.ia_attention_fwd_static_workspace(fake, fake, fake, fake, fake, None, None, fake,
+                                                 None, None, None) == 1
