@@ -172,6 +172,34 @@ IA_API ia_status ia_attention_fwd(const int8_t* q_i8, const int8_t* k_i8, const 
                                   float* lse_or_null, const ia_attn_params* p, void* stream);
 
 /*
+ * ia_attention_fwd_quant_q -- ia_attention_fwd with the Q quantization fused
+ * into the attention kernel: Q arrives as 16-bit rows and never makes the
+ * round trip through HBM as int8 codes.
+ *
+ * Defined by: "minimax_h3_sparse_int8" (FastVideo API page), module
+ * description and the quant_qk_int8 step (symmetric INT8 codes with one fp32
+ * scale per token or per 64-row block, Q not centred); comfy-kitchen issue
+ * #101 (int8 Q/K passthrough), the measurements of the quantization stage's
+ * share of attention time and the maintainer's point that the 16-bit
+ * activations are the interface. Per row i (or 64-row block) of Q:
+ *   amax = max |q_i|, scale_i = fl(amax / 127), code = rne(fl(q * fl(127 / amax))),
+ *   amax == 0 gives codes 0 and scale 0;
+ * bit-identical to ia_quantize_qk on Q followed by ia_attention_fwd, for the
+ * same k_i8 / k_scale (quantize K, with its mean, by ia_quantize_qk with q NULL).
+ *
+ *   q        [B,H,Sq,D] of p->v_dtype (Q and V share the 16-bit type), strides
+ *            p->q_strides in elements; 16-byte aligned base and strides.
+ *   others   as ia_attention_fwd; p->granularity sets the layout of both the
+ *            in-kernel Q scales and k_scale. Query rows past kv_valid (when
+ *            Sq == Sk) are padding: they are excluded from their block's amax.
+ */
+IA_API ia_status ia_attention_fwd_quant_q(const void* q, const int8_t* k_i8, const float* k_scale,
+                                          const void* v, const float* bias_or_null,
+                                          const uint8_t* block_mask_or_null, void* out,
+                                          float* lse_or_null, const ia_attn_params* p,
+                                          void* stream);
+
+/*
  * ia_attention_workspace_size -- bytes of scratch ia_attention_fwd needs for
  * p->kv_splits (0 when kv_splits <= 1): kv_splits * B*H*Sq * (D + 1) * 4.
  */

@@ -72,6 +72,8 @@ def load_library():
     L.ia_attention_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                    ctypes.POINTER(AttnParams), vp]
     L.ia_attention_fwd.restype = i32
+    L.ia_attention_fwd_quant_q.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(AttnParams), vp]
+    L.ia_attention_fwd_quant_q.restype = i32
     L.ia_attention_fwd_static_workspace.argtypes = L.ia_attention_fwd.argtypes
     L.ia_attention_fwd_static_workspace.restype = i32
     L.ia_merge_lse.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
@@ -175,28 +177,17 @@ def quantize_qk(q, k, granularity: str = "token", center_k: bool = True, kv_vali
     return res + (mu,) if return_mean else res
 
 
-def attention(q8, k8, q_scale, k_scale, v, *, bias=None, block_mask=None, sm_scale=None,
-              v_scale=None, kv_valid=None, granularity: str = "token", return_lse: bool = False,
-              out=None, lse=None, stream=None, kv_splits=None, workspace=None,
-              wait_timeout_ns: int = 0, debug_stall: bool = False):
-    """Forward attention on INT8 Q/K codes with a 16-bit P.V (see ``ia_attention_fwd``).
-
-    ``bias`` is fp32 ``[Sk]`` (any ``[1,1,1,Sk]`` view), ``block_mask`` bool
-    ``[B,H,ceil(Sq/64),ceil(Sk/64)]``, ``v_scale`` fp32 ``[H,D]``, ``kv_valid``
-    int32 ``[Sk/64]``. ``kv_splits``: None lets the library choose, 1 disables
-    the key split; with a split the scratch comes from ``workspace`` (a device
-    tensor of at least ``ia_attention_workspace_size`` bytes) or is allocated
-    here. Returns ``out`` or ``(out, lse)``.
-    """
-    L = load_library()
-    B, H, Sq, D = q8.shape
+def _attn_setup(L, q, k8, q_scale, k_scale, v, bias, block_mask, sm_scale, v_scale, kv_valid,
+                granularity, return_lse, out, lse, kv_splits, workspace, wait_timeout_ns,
+                debug_stall):
+    """ia_attn_params and the checked tensors of one attention call."""
+    B, H, Sq, D = q.shape
     Sk = k8.shape[2]
-    vd = _dtype_code(v.dtype)
     p = AttnParams()
     p.B, p.H, p.Sq, p.Sk, p.D = B, H, Sq, Sk, D
     p.sm_scale = float("nan") if sm_scale is None else float(sm_scale)
     p.granularity = _gran_code(granularity)
-    p.v_dtype = vd
+    p.v_dtype = _dtype_code(v.dtype)
     p.wait_timeout_ns = int(wait_timeout_ns)
     if kv_splits is None:
         kv_splits = L.ia_attention_default_splits(ctypes.byref(p), 1 if block_mask is not None else 0)
@@ -212,10 +203,12 @@ def attention(q8, k8, q_scale, k_scale, v, *, bias=None, block_mask=None, sm_sca
         out = torch.empty((B, H, Sq, D), dtype=v.dtype, device=v.device)
     if return_lse and lse is None:
         lse = torch.empty((B, H, Sq), dtype=torch.float32, device=v.device)
-    for name, t in (("q_strides", q8), ("k_strides", k8), ("v_strides", v), ("o_strides", out)):
+    for name, t in (("q_strides", q), ("k_strides", k8), ("v_strides", v), ("o_strides", out)):
         s = _strides3(t)
         getattr(p, name)[:] = list(s)
     for name, t in (("qs_strides", q_scale), ("ks_strides", k_scale)):
+        if t is None:
+            continue
         if t.dim() != 3 or t.stride(2) != 1:
             raise ValueError("scales must be [B,H,n] with a contiguous last dimension")
         getattr(p, name)[:] = [t.stride(0), t.stride(1)]
@@ -240,9 +233,52 @@ def attention(q8, k8, q_scale, k_scale, v, *, bias=None, block_mask=None, sm_sca
     if kv_valid is not None:
         kv_valid = kv_valid.to(device=v.device, dtype=torch.int32).contiguous()
         p.kv_valid = kv_valid.data_ptr()
+    # the tensors are returned so that they stay alive until the launch
+    return p, out, lse, bias, block_mask, (workspace, v_scale, kv_valid)
+
+
+def attention(q8, k8, q_scale, k_scale, v, *, bias=None, block_mask=None, sm_scale=None,
+              v_scale=None, kv_valid=None, granularity: str = "token", return_lse: bool = False,
+              out=None, lse=None, stream=None, kv_splits=None, workspace=None,
+              wait_timeout_ns: int = 0, debug_stall: bool = False):
+    """Forward attention on INT8 Q/K codes with a 16-bit P.V (see ``ia_attention_fwd``).
+
+    ``bias`` is fp32 ``[Sk]`` (any ``[1,1,1,Sk]`` view), ``block_mask`` bool
+    ``[B,H,ceil(Sq/64),ceil(Sk/64)]``, ``v_scale`` fp32 ``[H,D]``, ``kv_valid``
+    int32 ``[Sk/64]``. ``kv_splits``: None lets the library choose, 1 disables
+    the key split; with a split the scratch comes from ``workspace`` (a device
+    tensor of at least ``ia_attention_workspace_size`` bytes) or is allocated
+    here. Returns ``out`` or ``(out, lse)``.
+    """
+    L = load_library()
+    p, out, lse, bias, block_mask, _keep = _attn_setup(
+        L, q8, k8, q_scale, k_scale, v, bias, block_mask, sm_scale, v_scale, kv_valid,
+        granularity, return_lse, out, lse, kv_splits, workspace, wait_timeout_ns, debug_stall)
     _check(L.ia_attention_fwd(_ptr(q8), _ptr(k8), _ptr(q_scale), _ptr(k_scale), _ptr(v),
                               _ptr(bias), _ptr(block_mask), _ptr(out), _ptr(lse),
                               ctypes.byref(p), _stream(stream)))
+    return (out, lse) if return_lse else out
+
+
+def attention_quant_q(q, k8, k_scale, v, *, bias=None, block_mask=None, sm_scale=None,
+                      v_scale=None, kv_valid=None, granularity: str = "token",
+                      return_lse: bool = False, out=None, lse=None, stream=None, kv_splits=None,
+                      workspace=None, wait_timeout_ns: int = 0):
+    """Attention with Q quantized inside the kernel (see ``ia_attention_fwd_quant_q``).
+
+    ``q`` is the 16-bit ``[B,H,Sq,D]`` query of V's dtype; ``k8``/``k_scale``
+    come from ``quantize_qk(None, k, ...)`` or ``quantize_qk(q, k, ...)``.
+    The other arguments and the result are those of ``attention``.
+    """
+    L = load_library()
+    if q.dtype != v.dtype:
+        raise ValueError("q and v must share the 16-bit dtype")
+    p, out, lse, bias, block_mask, _keep = _attn_setup(
+        L, q, k8, None, k_scale, v, bias, block_mask, sm_scale, v_scale, kv_valid, granularity,
+        return_lse, out, lse, kv_splits, workspace, wait_timeout_ns, False)
+    _check(L.ia_attention_fwd_quant_q(_ptr(q), _ptr(k8), _ptr(k_scale), _ptr(v), _ptr(bias),
+                                      _ptr(block_mask), _ptr(out), _ptr(lse), ctypes.byref(p),
+                                      _stream(stream)))
     return (out, lse) if return_lse else out
 
 

@@ -89,6 +89,70 @@ ia_status static_workspace(void** out) {
   return IA_OK;
 }
 
+// Checks and launch shared by ia_attention_fwd (int8 Q codes and their scales)
+// and ia_attention_fwd_quant_q (16-bit Q rows of p->v_dtype, quantized inside
+// the kernel; q_scale unused).
+ia_status attention(const void* q, bool q_raw, const int8_t* k_i8, const float* q_scale,
+                    const float* k_scale, const void* v, const float* bias_or_null,
+                    const uint8_t* block_mask_or_null, void* out, float* lse_or_null,
+                    const ia_attn_params* p, void* stream) {
+  if (p == nullptr) return fail(IA_ERR_INVALID_ARG, "params is NULL");
+  if (p->B < 0 || p->H < 0 || p->Sq < 0 || p->Sk < 0) return fail(IA_ERR_INVALID_ARG, "negative shape");
+  if (p->D != 64 && p->D != 128) return fail(IA_ERR_INVALID_ARG, "D must be 64 or 128 (got %d)", p->D);
+  if (p->v_dtype != IA_BF16 && p->v_dtype != IA_FP16) return fail(IA_ERR_INVALID_ARG, "v_dtype");
+  if (p->granularity != IA_PER_TOKEN && p->granularity != IA_PER_BLOCK64)
+    return fail(IA_ERR_INVALID_ARG, "granularity");
+  if (p->B == 0 || p->H == 0 || p->Sq == 0) return ok();
+  if (q == nullptr || k_i8 == nullptr || (!q_raw && q_scale == nullptr) || k_scale == nullptr ||
+      v == nullptr || out == nullptr)
+    return fail(IA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned16(q) || !aligned16(k_i8) || !aligned16(v) || !aligned16(out))
+    return fail(IA_ERR_INVALID_ARG, "q, k_i8, v and out must be 16-byte aligned");
+  if (!strides_ok(p->q_strides, 3, q_raw ? 2 : 1) || !strides_ok(p->k_strides, 3, 1) ||
+      !strides_ok(p->v_strides, 3, 2) || !strides_ok(p->o_strides, 3, 2))
+    return fail(IA_ERR_INVALID_ARG, "row/head/batch strides must be non-negative multiples of 16 bytes");
+  if ((p->q_strides[2] < p->D) || (p->k_strides[2] < p->D) || (p->v_strides[2] < p->D) ||
+      (p->o_strides[2] < p->D))
+    return fail(IA_ERR_INVALID_ARG, "row stride smaller than D");
+  if (p->kv_valid != nullptr && (p->Sk % 64) != 0)
+    return fail(IA_ERR_INVALID_ARG, "kv_valid requires Sk to be a multiple of 64 (Sk=%d)", p->Sk);
+  if (p->Sk > 65535 * 64)
+    return fail(IA_ERR_UNSUPPORTED, "Sk too large (%d)", p->Sk);
+  if (p->kv_splits < 0 || p->kv_splits > ia::kMaxParts)
+    return fail(IA_ERR_INVALID_ARG, "kv_splits must be in [0, %d] (got %d)", ia::kMaxParts, p->kv_splits);
+  if (p->kv_splits > 1) {
+    const size_t need = ia_attention_workspace_size(p);
+    if (p->workspace == nullptr || p->workspace_bytes < need)
+      return fail(IA_ERR_INVALID_ARG, "kv_splits=%d needs a workspace of %zu bytes (got %zu)",
+                  p->kv_splits, need, p->workspace == nullptr ? static_cast<size_t>(0) : p->workspace_bytes);
+    if (!aligned16(p->workspace)) return fail(IA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  }
+  float sm = p->sm_scale;
+  if (std::isnan(sm)) sm = 1.0f / std::sqrt(static_cast<float>(p->D));
+  if (!std::isfinite(sm) || sm <= 0.f) return fail(IA_ERR_INVALID_ARG, "sm_scale must be positive");
+  int sms = 0;
+  ia_status s = check_device(&sms);
+  if (s != IA_OK) return s;
+  ia::AttnLaunch a{};
+  a.q = q;
+  a.q_raw = q_raw ? 1 : 0;
+  a.k = k_i8;
+  a.q_scale = q_scale;
+  a.k_scale = k_scale;
+  a.v = v;
+  a.bias = bias_or_null;
+  a.mask = block_mask_or_null;
+  a.out = out;
+  a.lse = lse_or_null;
+  a.p = *p;
+  a.sm_scale = sm;
+  a.workspace = p->kv_splits > 1 ? p->workspace : nullptr;
+  const char* msg = "";
+  s = ia::launch_attention(a, sms, static_cast<cudaStream_t>(stream), &msg);
+  if (s != IA_OK) return fail(s, "attention: %s", msg);
+  return ok();
+}
+
 }  // namespace
 
 extern "C" {
@@ -216,60 +280,17 @@ IA_API ia_status ia_attention_fwd(const int8_t* q_i8, const int8_t* k_i8, const 
                                   const float* k_scale, const void* v, const float* bias_or_null,
                                   const uint8_t* block_mask_or_null, void* out,
                                   float* lse_or_null, const ia_attn_params* p, void* stream) {
-  if (p == nullptr) return fail(IA_ERR_INVALID_ARG, "params is NULL");
-  if (p->B < 0 || p->H < 0 || p->Sq < 0 || p->Sk < 0) return fail(IA_ERR_INVALID_ARG, "negative shape");
-  if (p->D != 64 && p->D != 128) return fail(IA_ERR_INVALID_ARG, "D must be 64 or 128 (got %d)", p->D);
-  if (p->v_dtype != IA_BF16 && p->v_dtype != IA_FP16) return fail(IA_ERR_INVALID_ARG, "v_dtype");
-  if (p->granularity != IA_PER_TOKEN && p->granularity != IA_PER_BLOCK64)
-    return fail(IA_ERR_INVALID_ARG, "granularity");
-  if (p->B == 0 || p->H == 0 || p->Sq == 0) return ok();
-  if (q_i8 == nullptr || k_i8 == nullptr || q_scale == nullptr || k_scale == nullptr ||
-      v == nullptr || out == nullptr)
-    return fail(IA_ERR_INVALID_ARG, "a required pointer is NULL");
-  if (!aligned16(q_i8) || !aligned16(k_i8) || !aligned16(v) || !aligned16(out))
-    return fail(IA_ERR_INVALID_ARG, "q_i8, k_i8, v and out must be 16-byte aligned");
-  if (!strides_ok(p->q_strides, 3, 1) || !strides_ok(p->k_strides, 3, 1) ||
-      !strides_ok(p->v_strides, 3, 2) || !strides_ok(p->o_strides, 3, 2))
-    return fail(IA_ERR_INVALID_ARG, "row/head/batch strides must be non-negative multiples of 16 bytes");
-  if ((p->q_strides[2] < p->D) || (p->k_strides[2] < p->D) || (p->v_strides[2] < p->D) ||
-      (p->o_strides[2] < p->D))
-    return fail(IA_ERR_INVALID_ARG, "row stride smaller than D");
-  if (p->kv_valid != nullptr && (p->Sk % 64) != 0)
-    return fail(IA_ERR_INVALID_ARG, "kv_valid requires Sk to be a multiple of 64 (Sk=%d)", p->Sk);
-  if (p->Sk > 65535 * 64)
-    return fail(IA_ERR_UNSUPPORTED, "Sk too large (%d)", p->Sk);
-  if (p->kv_splits < 0 || p->kv_splits > ia::kMaxParts)
-    return fail(IA_ERR_INVALID_ARG, "kv_splits must be in [0, %d] (got %d)", ia::kMaxParts, p->kv_splits);
-  if (p->kv_splits > 1) {
-    const size_t need = ia_attention_workspace_size(p);
-    if (p->workspace == nullptr || p->workspace_bytes < need)
-      return fail(IA_ERR_INVALID_ARG, "kv_splits=%d needs a workspace of %zu bytes (got %zu)",
-                  p->kv_splits, need, p->workspace == nullptr ? static_cast<size_t>(0) : p->workspace_bytes);
-    if (!aligned16(p->workspace)) return fail(IA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
-  }
-  float sm = p->sm_scale;
-  if (std::isnan(sm)) sm = 1.0f / std::sqrt(static_cast<float>(p->D));
-  if (!std::isfinite(sm) || sm <= 0.f) return fail(IA_ERR_INVALID_ARG, "sm_scale must be positive");
-  int sms = 0;
-  ia_status s = check_device(&sms);
-  if (s != IA_OK) return s;
-  ia::AttnLaunch a{};
-  a.q = q_i8;
-  a.k = k_i8;
-  a.q_scale = q_scale;
-  a.k_scale = k_scale;
-  a.v = v;
-  a.bias = bias_or_null;
-  a.mask = block_mask_or_null;
-  a.out = out;
-  a.lse = lse_or_null;
-  a.p = *p;
-  a.sm_scale = sm;
-  a.workspace = p->kv_splits > 1 ? p->workspace : nullptr;
-  const char* msg = "";
-  s = ia::launch_attention(a, sms, static_cast<cudaStream_t>(stream), &msg);
-  if (s != IA_OK) return fail(s, "attention: %s", msg);
-  return ok();
+  return attention(q_i8, false, k_i8, q_scale, k_scale, v, bias_or_null, block_mask_or_null, out,
+                   lse_or_null, p, stream);
+}
+
+IA_API ia_status ia_attention_fwd_quant_q(const void* q, const int8_t* k_i8, const float* k_scale,
+                                          const void* v, const float* bias_or_null,
+                                          const uint8_t* block_mask_or_null, void* out,
+                                          float* lse_or_null, const ia_attn_params* p,
+                                          void* stream) {
+  return attention(q, true, k_i8, nullptr, k_scale, v, bias_or_null, block_mask_or_null, out,
+                   lse_or_null, p, stream);
 }
 
 IA_API ia_status ia_attention_fwd_static_workspace(

@@ -141,7 +141,8 @@ struct Layout {
                                    : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
   static constexpr int NWARPS = 4 * QS + 4;
   static constexpr int W_PROD = 4 * QS, W_MMA = 4 * QS + 1, W_CONV = 4 * QS + 2;
-  static_assert(QS * QR <= VB, "raw Q is staged in the first V buffer");
+  static_assert(QS * QR <= VB, "int8 Q is staged in the first V buffer");
+  static_assert(QS * QR * 2 <= NVS * VB, "16-bit Q is staged in the V buffers");
   static_assert(TMEM_NEED <= 512, "TMEM budget");
   static_assert(OFF_QH % 1024 == 0 && OFF_KH % 1024 == 0 && OFF_V % 1024 == 0, "swizzle align");
   static_assert(!INPLACE || KR == BN * 128, "the int8 tile fills one 64-column fp16 block");
@@ -219,7 +220,73 @@ __device__ __forceinline__ void widen_tile(const uint8_t* raw, uint8_t* dst, int
   }
 }
 
-template <int D, int QS, int BN, bool SPARSE, bool VBF16>
+// max |x| over one row of D 16-bit values in shared memory, as the 16-bit
+// pattern of |x| (for non-negative IEEE values the pattern order is the value
+// order). Thread r starts at chunk r so that a warp's 32 rows spread over the
+// shared-memory banks.
+template <int D>
+__device__ __forceinline__ uint32_t row_amax_bits(const uint8_t* row, int r) {
+  constexpr int CPR = D / 8;  // 16-byte chunks per row
+  uint32_t am = 0;
+#pragma unroll
+  for (int c = 0; c < CPR; ++c) {
+    const uint4 w = *reinterpret_cast<const uint4*>(row + ((c + r) & (CPR - 1)) * 16);
+    am = max_u16x2(am, w.x & 0x7fff7fffu);
+    am = max_u16x2(am, w.y & 0x7fff7fffu);
+    am = max_u16x2(am, w.z & 0x7fff7fffu);
+    am = max_u16x2(am, w.w & 0x7fff7fffu);
+  }
+  return max(am & 0xffffu, am >> 16);
+}
+
+template <bool BF16>
+__device__ __forceinline__ float half_bits_to_float(uint32_t b) {
+  if constexpr (BF16) return __uint_as_float(b << 16);
+  else return __half2float(__ushort_as_half(static_cast<unsigned short>(b)));
+}
+
+template <bool BF16>
+__device__ __forceinline__ float2 unpack_16x2(uint32_t w) {
+  if constexpr (BF16) return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  else return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
+// Round-half-to-even to an integer, for |v| < 2^22: adding 1.5 * 2^23 leaves
+// no fraction bits, so the IEEE addition rounds v to the nearest integer
+// (ties to even, as 1.5 * 2^23 is even) and the subtraction is exact.
+__device__ __forceinline__ float rne_integer(float v) {
+  return __fsub_rn(__fadd_rn(v, 12582912.0f), 12582912.0f);
+}
+
+// Symmetric INT8 quantization of one Q row inside the kernel ("minimax_h3_
+// sparse_int8", FastVideo API page, quant_qk_int8 and the per-token or
+// per-64-row-block scale layouts): scale = amax / 127, code =
+// rne(x * (127 / amax)), both divisions IEEE-rounded, amax = 0 gives codes 0.
+// |code| <= 127 without a clamp: x * fl(127/amax) <= 127 (1 + 2^-24), which
+// rounds to at most 127 + 2^-17 and then to the integer 127. The codes go to
+// the fp16 Q stage in the 128-byte-swizzled K-major layout the MMA reads;
+// returns the scale. `inv` is 0 for rows that are not quantized (padding).
+template <int D, bool BF16>
+__device__ __forceinline__ void write_q_codes(const uint8_t* row, uint8_t* qh, int r, float inv) {
+  constexpr int CPR = D / 8;
+#pragma unroll
+  for (int c = 0; c < CPR; ++c) {
+    const int cc = (c + r) & (CPR - 1);
+    const uint4 w = *reinterpret_cast<const uint4*>(row + cc * 16);
+    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+    uint32_t hv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = unpack_16x2<BF16>(in[e]);
+      hv[e] = cvt_f16x2(rne_integer(__fmul_rn(f.x, inv)), rne_integer(__fmul_rn(f.y, inv)));
+    }
+    const int blk = cc >> 3, k0 = cc & 7;  // 64-column block, 16-byte chunk in the row
+    *reinterpret_cast<uint4*>(qh + blk * (kM * 128) + r * 128 + ((k0 ^ (r & 7)) << 4)) =
+        make_uint4(hv[0], hv[1], hv[2], hv[3]);
+  }
+}
+
+template <int D, int QS, int BN, bool SPARSE, bool VBF16, bool QRAW>
 __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -246,7 +313,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
 
   if (tid == 0) {
     mbar_init(bar(L::B_QFULL), 1);
-    mbar_init(bar(L::B_QCONV), 64);
+    mbar_init(bar(L::B_QCONV), QRAW ? QS * kM : 64);
     for (int i = 0; i < L::NKS; ++i) {
       mbar_init(bar(L::B_KRF + i), 1);
       mbar_init(bar(L::B_KCF + i), 64);
@@ -329,9 +396,12 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       int kr_last[L::NKS], v_last[L::NVS];
       for (int i = 0; i < L::NKS; ++i) kr_last[i] = -1;
       for (int i = 0; i < L::NVS; ++i) v_last[i] = -1;
-      mbar_arrive_expect_tx(bar(L::B_QFULL), QS * kM * D);
+      // int8 Q codes, or 16-bit Q rows that the softmax warps quantize; either
+      // way they are staged in the V buffers until converted
+      constexpr int QB = QRAW ? 2 : 1;
+      mbar_arrive_expect_tx(bar(L::B_QFULL), QS * kM * D * QB);
       for (int s = 0; s < QS; ++s)
-        tma_load_4d(sm_v + s * L::QR, &tm_q, bar(L::B_QFULL), 0, q0 + s * kM, h, b);
+        tma_load_4d(sm_v + s * L::QR * QB, &tm_q, bar(L::B_QFULL), 0, q0 + s * kM, h, b);
       bool ok = true;
       for (int it = 0; it < n_it; ++it) {
         const int kt = SPARSE ? static_cast<int>(list[it0 + it]) : it0 + it;
@@ -351,8 +421,8 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         tma_load_4d(kdst, &tm_k, bar(L::B_KRF + ks), 0, kt * BN, h, b);
         kr_last[ks] = it;
         const int vs = it % L::NVS;
-        if (it == 0)
-          ok = wait_bar(bar(L::B_QCONV), 0, ctl, kErrProducer);  // raw Q sits in V buffer 0
+        if (it == 0 || (QRAW && it < L::NVS))  // raw Q sits in V buffer 0 (all of them)
+          ok = wait_bar(bar(L::B_QCONV), 0, ctl, kErrProducer);
         else if (it >= L::NVS)
           ok = wait_bar(bar(L::B_VE + vs), ((it / L::NVS) - 1) & 1, ctl, kErrProducer);
         if (!ok) break;
@@ -451,8 +521,8 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
   } else if (warp >= L::W_CONV) {
     // ---------------------------------------------- int8 -> fp16 converters
     const int ct = tid - L::W_CONV * 32;
-    bool ok = wait_bar(bar(L::B_QFULL), 0, ctl, kErrConverter);
-    if (ok) {
+    bool ok = QRAW ? true : wait_bar(bar(L::B_QFULL), 0, ctl, kErrConverter);
+    if (ok && !QRAW) {
       for (int s = 0; s < QS; ++s)
         widen_tile<D, false>(smem + L::OFF_V + s * L::QR, smem + L::OFF_QH + s * L::QH, kM, ct);
       fence_proxy_async_smem();
@@ -538,13 +608,40 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     const int row = q0 + s * kM + r;
     const bool row_ok = row < a.Sq;
     float cq = 0.f;
-    if (row_ok)
+    bool ok = true;
+    if constexpr (QRAW) {
+      // This thread quantizes its own row (per 64-row block: each of the
+      // block's two warps also scans the other warp's rows, so no barrier
+      // between warps is needed).
+      ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_QFULL), 0, ctl, kErrSoftmax));
+      if (ok) {
+        const uint8_t* raw = smem + L::OFF_V + static_cast<size_t>(s * kM) * D * 2;
+        auto quantized = [&](int rr) {  // row rr of this stage: real and not padding
+          const int gr = q0 + s * kM + rr;
+          return gr < a.Sq && !(a.pad_query && (gr & 63) >= __ldg(a.kv_valid + (gr >> 6)));
+        };
+        const bool keep = quantized(r);
+        uint32_t am = keep ? row_amax_bits<D>(raw + r * D * 2, r) : 0u;
+        if (a.gran_block) {
+          const int rp = r ^ 32;
+          if (quantized(rp)) am = max(am, row_amax_bits<D>(raw + rp * D * 2, r));
+          am = __reduce_max_sync(0xffffffffu, am);
+        }
+        const float amax = half_bits_to_float<VBF16>(am);
+        const float scale = __fdiv_rn(amax, 127.0f);
+        const float inv = (keep && amax > 0.f) ? __fdiv_rn(127.0f, amax) : 0.f;
+        write_q_codes<D, VBF16>(raw + r * D * 2, smem + L::OFF_QH + s * L::QH, r, inv);
+        cq = scale * a.cq_mult;
+        fence_proxy_async_smem();
+        mbar_arrive(bar(L::B_QCONV));
+      }
+    } else if (row_ok) {
       cq = __ldg(a.q_scale + b * a.qs_sb + h * a.qs_sh + (a.gran_block ? (row >> 6) : row)) * a.cq_mult;
+    }
     const int half = (r >= 64) ? 1 : 0;
     float m = -INFINITY;  // reference maximum (log2 units) that P is relative to
     float l = 0.f;
-    bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
+    for (int it = 0; it < n_it && ok; ++it) {
       const int ss = it % L::NSC;
       if (r == 0) IA_TRACE_POINT(4 * s, it);
       bool w = wait_bar(bar(L::B_SF + s), it & 1, ctl, kErrSoftmax);
@@ -755,14 +852,16 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int esiz
   return r == CUDA_SUCCESS;
 }
 
-template <int D, int QS, int BN, bool SPARSE, bool VBF16>
+template <int D, int QS, int BN, bool SPARSE, bool VBF16, bool QRAW>
 ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** msg) {
   using L = Layout<D, QS, BN, SPARSE>;
   const ia_attn_params& p = A.p;
   CUtensorMap tq, tk, tv;
-  const bool okq = make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, A.q, 1, D, p.Sq, p.H, p.B,
-                            p.q_strides[2], p.q_strides[1], p.q_strides[0], D, kM,
-                            CU_TENSOR_MAP_SWIZZLE_NONE);
+  const CUtensorMapDataType qdt = !QRAW ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                  : VBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const bool okq = make_map(&tq, qdt, A.q, QRAW ? 2 : 1, D, p.Sq, p.H, p.B, p.q_strides[2],
+                            p.q_strides[1], p.q_strides[0], D, kM, CU_TENSOR_MAP_SWIZZLE_NONE);
   const bool okk = make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, A.k, 1, D, p.Sk, p.H, p.B,
                             p.k_strides[2], p.k_strides[1], p.k_strides[0], D, BN,
                             CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -814,7 +913,7 @@ ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** ms
     a.ws_l = a.ws_o + static_cast<int64_t>(nsplit) * rows * D;
   }
   const size_t smem = L::SMEM_FIXED + (SPARSE ? static_cast<size_t>(a.Tk) * 2 : 0);
-  auto kern = attn_fwd_kernel<D, QS, BN, SPARSE, VBF16>;
+  auto kern = attn_fwd_kernel<D, QS, BN, SPARSE, VBF16, QRAW>;
   if (smem > 232448) {
     *msg = "key-tile list does not fit in shared memory (too many key tiles)";
     return IA_ERR_UNSUPPORTED;
@@ -861,24 +960,30 @@ ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** ms
   return IA_OK;
 }
 
+template <bool QRAW>
+ia_status dispatch(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** msg) {
+  const ia_attn_params& p = A.p;
+  const bool bf = p.v_dtype == IA_BF16;
+  if (A.mask != nullptr) {
+    if (p.D == 128)
+      return bf ? run<128, 1, 64, true, true, QRAW>(A, num_sms, st, msg)
+                : run<128, 1, 64, true, false, QRAW>(A, num_sms, st, msg);
+    return bf ? run<64, 1, 64, true, true, QRAW>(A, num_sms, st, msg)
+              : run<64, 1, 64, true, false, QRAW>(A, num_sms, st, msg);
+  }
+  if (p.D == 128)
+    return bf ? run<128, 2, 128, false, true, QRAW>(A, num_sms, st, msg)
+              : run<128, 2, 128, false, false, QRAW>(A, num_sms, st, msg);
+  return bf ? run<64, 2, 128, false, true, QRAW>(A, num_sms, st, msg)
+            : run<64, 2, 128, false, false, QRAW>(A, num_sms, st, msg);
+}
+
 }  // namespace
 
 ia_status launch_attention(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** msg) {
   const ia_attn_params& p = A.p;
   if (p.B == 0 || p.H == 0 || p.Sq == 0) return IA_OK;
-  const bool bf = p.v_dtype == IA_BF16;
-  if (A.mask != nullptr) {
-    if (p.D == 128)
-      return bf ? run<128, 1, 64, true, true>(A, num_sms, st, msg)
-                : run<128, 1, 64, true, false>(A, num_sms, st, msg);
-    return bf ? run<64, 1, 64, true, true>(A, num_sms, st, msg)
-              : run<64, 1, 64, true, false>(A, num_sms, st, msg);
-  }
-  if (p.D == 128)
-    return bf ? run<128, 2, 128, false, true>(A, num_sms, st, msg)
-              : run<128, 2, 128, false, false>(A, num_sms, st, msg);
-  return bf ? run<64, 2, 128, false, true>(A, num_sms, st, msg)
-            : run<64, 2, 128, false, false>(A, num_sms, st, msg);
+  return A.q_raw ? dispatch<true>(A, num_sms, st, msg) : dispatch<false>(A, num_sms, st, msg);
 }
 
 cudaError_t attention_read_device_error(unsigned int* out, cudaStream_t st) {

@@ -59,7 +59,8 @@ cudaError_t launch_merge_n(const MergeNArgs& a, int num_sms, cudaStream_t st);
 
 struct AttnLaunch {
   void* workspace;  // fp32 partials when p.kv_splits >= 2
-  const int8_t* q;
+  const void* q;    // int8 codes, or 16-bit rows of p.v_dtype when q_raw
+  int q_raw;        // quantize Q inside the kernel (q_scale unused)
   const int8_t* k;
   const float* q_scale;
   const float* k_scale;

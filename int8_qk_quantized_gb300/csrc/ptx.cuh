@@ -285,6 +285,13 @@ __device__ __forceinline__ uint32_t cvt_f16x2(float lo, float hi) {
   return r;
 }
 
+// Lane-wise unsigned maximum of two pairs of 16-bit integers.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 // Four int8 codes (one 32-bit word) -> four exact fp16 values in two words.
 // Each byte is biased to x+128, placed under the fp16 pattern 0x64xx (the value
 // 1024 + (x+128)) and 1152 is subtracted; every step is exact.
