@@ -25,6 +25,10 @@ Sources (page title, then the part of the page):
   request for optional return_lse": the opening paragraph (one additive bias
   per key, shape [1,1,1,K]) and "Question 2" (merging two partial softmaxes
   exactly through their log-sum-exp).
+* [comfy-kitchen] "The measurement" (the attn_mask forms callers pass: fp32,
+  bf16 and fp16 additive masks and bool masks, shaped [1,1,1,K] or expanded
+  to [1,1,Q,K]) and the repro (the bool mask is True where the key's weight
+  is kept).
 * [FlyDSL] "Add optional forward LSE output": "Summary" (LSE = sm_scale*m +
   ln l, natural log), "Kernel implementation" (-inf for fully masked rows;
   split-K combine from the combined maximum and denominator) and "Public API"
@@ -49,6 +53,7 @@ PARITY_STATUS = {
     "k_mean": "pinned (exact rational sum on small inputs, translation property)",
     "quantize": "pinned (hand-derived codes, ties, zero rows, error bound)",
     "attention": "pinned (brute-force softmax, torch fp64 SDPA, special cases)",
+    "attention(mask=)": "pinned (brute-force masked softmax, bool = 0/-inf, row shifts)",
     "exact_attention": "pinned (torch fp64 SDPA, centring invariance)",
     "merge": "pinned (split of one softmax equals the whole)",
 }
@@ -194,9 +199,34 @@ def _key_mask(b, h, rows, Sk, block_mask, kv_valid):
     return vis
 
 
+def _mask_rows(mask, B, H, Sq, Sk, b, h, rows):
+    """Rows ``rows`` of head (b, h) of a general attention mask.
+
+    ``mask`` is broadcastable to [B,H,Sq,Sk] (numpy broadcasting, as the
+    [1,1,1,K] and [1,1,Q,K] views of [comfy-kitchen] "The measurement"). A
+    float mask holds additive logit offsets (the exact bf16/fp16/fp32 values,
+    widened to float64); a bool mask keeps a key where it is True and
+    excludes it (logit -inf) where it is False.
+    Returns ("add", float64 [n, Sk]) or ("keep", bool [n, Sk])."""
+    m = np.asarray(mask)
+    while m.ndim < 4:
+        m = m[None]
+    full = np.broadcast_to(m, (B, H, Sq, Sk))[b, h][np.asarray(rows)]
+    if full.dtype == np.bool_:
+        return "keep", full
+    return "add", full.astype(np.float64)
+
+
+def _apply_mask(s, kind_rows):
+    kind, mr = kind_rows
+    if kind == "keep":
+        return np.where(mr, s, -np.inf)
+    return s + mr
+
+
 def attention(q_codes, q_scale, k_codes, k_scale, v, *, sm_scale=None, bias=None,
               block_mask=None, kv_valid=None, v_scale=None, granularity="token",
-              rows=None, row_chunk=256):
+              rows=None, row_chunk=256, mask=None):
     """Same-quantisation FP64 attention reference.
 
     q_hat = code * scale and k_hat likewise (float64);
@@ -216,6 +246,10 @@ def attention(q_codes, q_scale, k_codes, k_scale, v, *, sm_scale=None, bias=None
 
     Reading: with a validity vector and Sq == Sk, query rows past it are
     padding; they give O = 0 and LSE = -inf (the pages leave them undefined).
+
+    ``mask`` is the general form of the bias (see :func:`_mask_rows`): a float
+    mask broadcastable to [B,H,Sq,Sk] is added where ``bias`` would be; a bool
+    mask excludes the keys where it is False.
 
     ``rows`` optionally restricts the query rows (a 1-D index array); rows are
     independent, so they are processed in chunks of ``row_chunk``.
@@ -239,6 +273,8 @@ def attention(q_codes, q_scale, k_codes, k_scale, v, *, sm_scale=None, bias=None
                 s = sm_scale * (qh[b, h, r] @ kh[b, h].T)
                 if bias64 is not None:
                     s = s + bias64[None, :]
+                if mask is not None:
+                    s = _apply_mask(s, _mask_rows(mask, B, H, Sq, Sk, b, h, r))
                 vis = _key_mask(b, h, r, Sk, block_mask, kv_valid)
                 s = np.where(vis, s, -np.inf)
                 o, l = _softmax_rows(s, vv[b, h])
@@ -254,7 +290,7 @@ def attention(q_codes, q_scale, k_codes, k_scale, v, *, sm_scale=None, bias=None
 
 
 def exact_attention(q, k, v, *, sm_scale=None, bias=None, block_mask=None, kv_valid=None,
-                    v_scale=None, rows=None, row_chunk=256):
+                    v_scale=None, rows=None, row_chunk=256, mask=None):
     """Textbook softmax attention in float64 on the unquantised inputs (no
     centring, no quantisation): the yardstick the INT8 path is measured
     against ([model-kernels] "5. Numerical accuracy" compares against SDPA).
@@ -277,6 +313,8 @@ def exact_attention(q, k, v, *, sm_scale=None, bias=None, block_mask=None, kv_va
                 s = sm_scale * (qq[b, h, r] @ kk[b, h].T)
                 if bias64 is not None:
                     s = s + bias64[None, :]
+                if mask is not None:
+                    s = _apply_mask(s, _mask_rows(mask, B, H, Sq, Sk, b, h, r))
                 vis = _key_mask(b, h, r, Sk, block_mask, kv_valid)
                 s = np.where(vis, s, -np.inf)
                 o, l = _softmax_rows(s, vv[b, h])
