@@ -53,6 +53,14 @@ typedef enum ia_dtype { IA_BF16 = 0, IA_FP16 = 1 } ia_dtype;
 /* One fp32 scale per row ("per token") or per 64-row block of a head. */
 typedef enum ia_granularity { IA_PER_TOKEN = 0, IA_PER_BLOCK64 = 1 } ia_granularity;
 
+/* Element type of a general attention mask (ia_attn_params.mask). */
+typedef enum ia_mask_dtype {
+  IA_MASK_F32 = 0,  /* additive logit offset */
+  IA_MASK_BF16 = 1, /* additive logit offset */
+  IA_MASK_F16 = 2,  /* additive logit offset */
+  IA_MASK_BOOL = 3  /* one byte: nonzero keeps the key, zero excludes it */
+} ia_mask_dtype;
+
 /*
  * ia_quantize_qk -- K mean-centring and symmetric INT8 quantisation of Q and K.
  *
@@ -126,6 +134,20 @@ typedef struct ia_attn_params {
   int debug_stall;              /* test hook: nonzero makes one internal wait of every CTA
                                    wait for a signal that never comes, so the call ends
                                    through the timeout path (status IA_ERR_TIMEOUT) */
+  const void* mask;             /* optional general mask, in place of bias_or_null: logically
+                                   [B,H,Sq,Sk], element (b,h,i,j) at mask + b*mask_strides[0]
+                                   + h*mask_strides[1] + i*mask_strides[2] + j (elements).
+                                   Float masks are added to the scaled logits like the bias;
+                                   bool masks exclude the keys where they are zero. A zero
+                                   stride broadcasts that dimension ("int8_attention: masked
+                                   path costs ~1.8x unmasked, ...", The measurement: fp32/bf16/
+                                   fp16/bool, [1,1,1,K] and [1,1,Q,K] expanded). */
+  ia_mask_dtype mask_dtype;
+  int64_t mask_strides[4];      /* (b, h, q, k); k must be 1. q == 0 (one row of keys per b,h,
+                                   shared by all queries) takes the per-key path at the cost
+                                   of a bias. q != 0 (a row per query) is read by TMA into
+                                   shared memory per key tile: base and the b, h, q strides
+                                   16-byte aligned; not combinable with a block mask. */
 } ia_attn_params;
 
 /* Fill p with contiguous BHSD strides for the given shape (no pointers set). */

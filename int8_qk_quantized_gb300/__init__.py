@@ -49,6 +49,8 @@ class AttnParams(ctypes.Structure):
         ("kv_splits", ctypes.c_int), ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
         ("wait_timeout_ns", ctypes.c_uint64), ("debug_stall", ctypes.c_int),
+        ("mask", ctypes.c_void_p), ("mask_dtype", ctypes.c_int),
+        ("mask_strides", ctypes.c_int64 * 4),
     ]
 
 
@@ -177,9 +179,34 @@ def quantize_qk(q, k, granularity: str = "token", center_k: bool = True, kv_vali
     return res + (mu,) if return_mean else res
 
 
+MASK_DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2, torch.bool: 3}
+
+
+def _set_mask(p, mask, B, H, Sq, Sk, device):
+    """Fill the general-mask fields of ``p`` from a tensor broadcastable to
+    [B,H,Sq,Sk]; broadcast dimensions keep stride 0. Returns the tensor the
+    pointer refers to."""
+    if mask.dtype not in MASK_DTYPES:
+        raise ValueError("mask must be float32, bfloat16, float16 or bool")
+    if mask.device != device:
+        raise ValueError("mask must be on the device of q/k/v")
+    m = mask
+    while m.dim() < 4:
+        m = m.unsqueeze(0)
+    if m.dim() != 4:
+        raise ValueError("mask must have at most 4 dimensions")
+    if m.shape[3] != 1 and m.stride(3) != 1:
+        m = m.contiguous()
+    m = m.expand(B, H, Sq, Sk)
+    p.mask = m.data_ptr()
+    p.mask_dtype = MASK_DTYPES[m.dtype]
+    p.mask_strides[:] = [m.stride(i) if m.shape[i] > 1 else 0 for i in range(3)] + [1]
+    return m
+
+
 def _attn_setup(L, q, k8, q_scale, k_scale, v, bias, block_mask, sm_scale, v_scale, kv_valid,
                 granularity, return_lse, out, lse, kv_splits, workspace, wait_timeout_ns,
-                debug_stall):
+                debug_stall, mask=None):
     """ia_attn_params and the checked tensors of one attention call."""
     B, H, Sq, D = q.shape
     Sk = k8.shape[2]
@@ -233,19 +260,25 @@ def _attn_setup(L, q, k8, q_scale, k_scale, v, bias, block_mask, sm_scale, v_sca
     if kv_valid is not None:
         kv_valid = kv_valid.to(device=v.device, dtype=torch.int32).contiguous()
         p.kv_valid = kv_valid.data_ptr()
+    if mask is not None:
+        mask = _set_mask(p, mask, B, H, Sq, Sk, v.device)
     # the tensors are returned so that they stay alive until the launch
-    return p, out, lse, bias, block_mask, (workspace, v_scale, kv_valid)
+    return p, out, lse, bias, block_mask, (workspace, v_scale, kv_valid, mask)
 
 
 def attention(q8, k8, q_scale, k_scale, v, *, bias=None, block_mask=None, sm_scale=None,
               v_scale=None, kv_valid=None, granularity: str = "token", return_lse: bool = False,
               out=None, lse=None, stream=None, kv_splits=None, workspace=None,
-              wait_timeout_ns: int = 0, debug_stall: bool = False):
+              wait_timeout_ns: int = 0, debug_stall: bool = False, mask=None):
     """Forward attention on INT8 Q/K codes with a 16-bit P.V (see ``ia_attention_fwd``).
 
     ``bias`` is fp32 ``[Sk]`` (any ``[1,1,1,Sk]`` view), ``block_mask`` bool
     ``[B,H,ceil(Sq/64),ceil(Sk/64)]``, ``v_scale`` fp32 ``[H,D]``, ``kv_valid``
-    int32 ``[Sk/64]``. ``kv_splits``: None lets the library choose, 1 disables
+    int32 ``[Sk/64]``. ``mask`` (instead of ``bias``) is a float32/bfloat16/
+    float16 additive or bool keep mask broadcastable to ``[B,H,Sq,Sk]``; a
+    mask that is the same for every query (stride 0 along queries, e.g.
+    ``[1,1,1,Sk]`` or an ``expand``-ed view) runs at the cost of a bias.
+    ``kv_splits``: None lets the library choose, 1 disables
     the key split; with a split the scratch comes from ``workspace`` (a device
     tensor of at least ``ia_attention_workspace_size`` bytes) or is allocated
     here. Returns ``out`` or ``(out, lse)``.
@@ -253,7 +286,8 @@ def attention(q8, k8, q_scale, k_scale, v, *, bias=None, block_mask=None, sm_sca
     L = load_library()
     p, out, lse, bias, block_mask, _keep = _attn_setup(
         L, q8, k8, q_scale, k_scale, v, bias, block_mask, sm_scale, v_scale, kv_valid,
-        granularity, return_lse, out, lse, kv_splits, workspace, wait_timeout_ns, debug_stall)
+        granularity, return_lse, out, lse, kv_splits, workspace, wait_timeout_ns, debug_stall,
+        mask)
     _check(L.ia_attention_fwd(_ptr(q8), _ptr(k8), _ptr(q_scale), _ptr(k_scale), _ptr(v),
                               _ptr(bias), _ptr(block_mask), _ptr(out), _ptr(lse),
                               ctypes.byref(p), _stream(stream)))
@@ -263,7 +297,7 @@ def attention(q8, k8, q_scale, k_scale, v, *, bias=None, block_mask=None, sm_sca
 def attention_quant_q(q, k8, k_scale, v, *, bias=None, block_mask=None, sm_scale=None,
                       v_scale=None, kv_valid=None, granularity: str = "token",
                       return_lse: bool = False, out=None, lse=None, stream=None, kv_splits=None,
-                      workspace=None, wait_timeout_ns: int = 0):
+                      workspace=None, wait_timeout_ns: int = 0, mask=None):
     """Attention with Q quantized inside the kernel (see ``ia_attention_fwd_quant_q``).
 
     ``q`` is the 16-bit ``[B,H,Sq,D]`` query of V's dtype; ``k8``/``k_scale``
@@ -275,7 +309,7 @@ def attention_quant_q(q, k8, k_scale, v, *, bias=None, block_mask=None, sm_scale
         raise ValueError("q and v must share the 16-bit dtype")
     p, out, lse, bias, block_mask, _keep = _attn_setup(
         L, q, k8, None, k_scale, v, bias, block_mask, sm_scale, v_scale, kv_valid, granularity,
-        return_lse, out, lse, kv_splits, workspace, wait_timeout_ns, False)
+        return_lse, out, lse, kv_splits, workspace, wait_timeout_ns, False, mask)
     _check(L.ia_attention_fwd_quant_q(_ptr(q), _ptr(k8), _ptr(k_scale), _ptr(v), _ptr(bias),
                                       _ptr(block_mask), _ptr(out), _ptr(lse), ctypes.byref(p),
                                       _stream(stream)))

@@ -127,6 +127,28 @@ ia_status attention(const void* q, bool q_raw, const int8_t* k_i8, const float* 
                   p->kv_splits, need, p->workspace == nullptr ? static_cast<size_t>(0) : p->workspace_bytes);
     if (!aligned16(p->workspace)) return fail(IA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
   }
+  // General mask: its query stride decides between the per-key path (one row
+  // of keys per (b, h)) and the per-row path (mask tiles by TMA).
+  bool row_mask = false;
+  if (p->mask != nullptr) {
+    if (bias_or_null != nullptr)
+      return fail(IA_ERR_INVALID_ARG, "pass either bias_or_null or params.mask, not both");
+    if (p->mask_dtype < IA_MASK_F32 || p->mask_dtype > IA_MASK_BOOL)
+      return fail(IA_ERR_INVALID_ARG, "mask_dtype");
+    for (int i = 0; i < 4; ++i)
+      if (p->mask_strides[i] < 0) return fail(IA_ERR_INVALID_ARG, "negative mask stride");
+    if (p->mask_strides[3] != 1 && p->Sk > 1)
+      return fail(IA_ERR_INVALID_ARG, "the mask's key stride must be 1");
+    row_mask = p->mask_strides[2] != 0 && p->Sq > 1;
+    if (row_mask) {
+      const int64_t es = p->mask_dtype == IA_MASK_F32 ? 4 : p->mask_dtype == IA_MASK_BOOL ? 1 : 2;
+      if (!aligned16(p->mask) || !strides_ok(p->mask_strides, 3, es))
+        return fail(IA_ERR_INVALID_ARG,
+                    "a per-query-row mask needs a 16-byte aligned base and b, h, q strides");
+      if (block_mask_or_null != nullptr)
+        return fail(IA_ERR_UNSUPPORTED, "a per-query-row mask cannot be combined with a block mask");
+    }
+  }
   float sm = p->sm_scale;
   if (std::isnan(sm)) sm = 1.0f / std::sqrt(static_cast<float>(p->D));
   if (!std::isfinite(sm) || sm <= 0.f) return fail(IA_ERR_INVALID_ARG, "sm_scale must be positive");
@@ -140,7 +162,16 @@ ia_status attention(const void* q, bool q_raw, const int8_t* k_i8, const float* 
   a.q_scale = q_scale;
   a.k_scale = k_scale;
   a.v = v;
-  a.bias = bias_or_null;
+  if (bias_or_null != nullptr) {
+    a.bias = bias_or_null;
+    a.bias_dtype = IA_MASK_F32;
+  } else if (p->mask != nullptr && !row_mask) {
+    a.bias = p->mask;
+    a.bias_dtype = p->mask_dtype;
+    a.bias_sb = p->mask_strides[0];
+    a.bias_sh = p->mask_strides[1];
+  }
+  a.row_mask = row_mask ? 1 : 0;
   a.mask = block_mask_or_null;
   a.out = out;
   a.lse = lse_or_null;

@@ -40,6 +40,7 @@
 
 #include <cmath>
 #include <cstdio>
+#include <cstring>
 
 #include "launch.h"
 #include "ptx.cuh"
@@ -82,7 +83,11 @@ enum : unsigned {
 struct Params {
   const float* q_scale;
   const float* k_scale;
-  const float* bias;
+  const void* bias;  // per-key offsets: the fp32 bias, or a mask whose query stride is 0
+  int bias_dtype;    // ia_mask_dtype
+  int64_t bias_sb, bias_sh;  // element strides of the per-(b,h) key rows (0 broadcasts)
+  int rm_dtype;      // ROWMASK kernels: ia_mask_dtype of the per-row mask tiles
+  int rm_h, rm_b;    //   1 if the mask has that dimension (0: broadcast, coordinate 0)
   const uint8_t* mask;
   const int32_t* kv_valid;
   const float* v_scale;
@@ -106,7 +111,7 @@ struct Params {
   int B;
 };
 
-template <int D, int QS, int BN, bool SPARSE>
+template <int D, int QS, int BN, bool SPARSE, bool ROWMASK = false>
 struct Layout {
   // Block-sparse, D == 128: the int8 K tile lands (by TMA) in the second
   // 64-column block of its fp16 K buffer and is widened in place, which keeps
@@ -120,11 +125,15 @@ struct Layout {
   static constexpr int KR = BN * D;       // int8 K tile
   static constexpr int QR = kM * D;       // int8 Q stage
   static constexpr int SC = BN * 8 + 16;  // k scales, bias*log2e, flags
+  // Per-row mask tile (ROWMASK): kM rows x BN keys as TMA boxes of 128-byte
+  // rows with the 128-byte swizzle; 32 fp32, 64 16-bit or 128 bool keys per box.
+  static constexpr int MB = ROWMASK ? BN * 4 * kM : 0;
   static constexpr int OFF_QH = 0;
   static constexpr int OFF_KH = OFF_QH + QS * QH;
   static constexpr int OFF_V = OFF_KH + NKS * KH;
   static constexpr int OFF_KR = OFF_V + NVS * VB;
-  static constexpr int OFF_SC = OFF_KR + NRS * KR;
+  static constexpr int OFF_MK = OFF_KR + NRS * KR;
+  static constexpr int OFF_SC = OFF_MK + NSC * MB;
   static constexpr int OFF_VS = OFF_SC + NSC * SC;
   static constexpr int OFF_BAR = (OFF_VS + D * 4 + 7) / 8 * 8;
   // barrier indices
@@ -132,7 +141,8 @@ struct Layout {
                        B_KCF = B_KRE + NRS, B_KCE = B_KCF + NKS, B_VF = B_KCE + NKS,
                        B_VE = B_VF + NVS, B_SCF = B_VE + NVS, B_SCE = B_SCF + NSC,
                        B_SF = B_SCE + NSC, B_PF = B_SF + QS, B_OF = B_PF + QS,
-                       B_DRAIN = B_OF + QS, B_STALL = B_DRAIN + 1, NBAR = B_STALL + 1;
+                       B_DRAIN = B_OF + QS, B_STALL = B_DRAIN + 1, B_MF = B_STALL + 1,
+                       NBAR = B_MF + NSC;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;       // tmem base, abort, count, pad
   static constexpr int OFF_LIST = OFF_MISC + 16 + 32;       // + warp counts for the list scan
   static constexpr int SMEM_FIXED = OFF_LIST;
@@ -144,7 +154,9 @@ struct Layout {
   static_assert(QS * QR <= VB, "int8 Q is staged in the first V buffer");
   static_assert(QS * QR * 2 <= NVS * VB, "16-bit Q is staged in the V buffers");
   static_assert(TMEM_NEED <= 512, "TMEM budget");
-  static_assert(OFF_QH % 1024 == 0 && OFF_KH % 1024 == 0 && OFF_V % 1024 == 0, "swizzle align");
+  static_assert(OFF_QH % 1024 == 0 && OFF_KH % 1024 == 0 && OFF_V % 1024 == 0 &&
+                    OFF_MK % 1024 == 0, "swizzle align");
+  static_assert(!ROWMASK || (QS == 1 && BN == 64 && !SPARSE), "row-mask shape");
   static_assert(!INPLACE || KR == BN * 128, "the int8 tile fills one 64-column fp16 block");
 };
 
@@ -286,12 +298,58 @@ __device__ __forceinline__ void write_q_codes(const uint8_t* row, uint8_t* qh, i
   }
 }
 
-template <int D, int QS, int BN, bool SPARSE, bool VBF16, bool QRAW>
+// One per-key offset of a key row of a general mask, in two steps so that the
+// load can be issued early and converted later: the raw bits of element
+// `key`, then their value in logit units (float dtypes as they are, bool as
+// 0 or -inf).
+__device__ __forceinline__ uint32_t key_bias_bits(const void* row, int key, int dt) {
+  if (dt == IA_MASK_F32) return __ldg(reinterpret_cast<const unsigned int*>(row) + key);
+  if (dt == IA_MASK_BOOL) return __ldg(reinterpret_cast<const unsigned char*>(row) + key);
+  return __ldg(reinterpret_cast<const unsigned short*>(row) + key);
+}
+
+__device__ __forceinline__ float key_bias_value(uint32_t bits, int dt) {
+  if (dt == IA_MASK_F32) return __uint_as_float(bits);
+  if (dt == IA_MASK_BF16) return __uint_as_float(bits << 16);
+  if (dt == IA_MASK_F16) return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
+  return bits ? 0.f : -INFINITY;
+}
+
+// Four consecutive keys c..c+3 of row r of a per-row mask tile in shared
+// memory (TMA boxes of 128-byte rows, 128-byte swizzle: 16-byte chunk j of
+// row r sits at chunk j ^ (r & 7)), as logit offsets.
+__device__ __forceinline__ void row_mask4(const uint8_t* buf, int r, int c, int dt, float out[4]) {
+  const uint8_t* row = buf + r * 128;
+  const int sw = r & 7;
+  if (dt == IA_MASK_F32) {
+    const int j = (c & 31) >> 2;
+    const float4 v = *reinterpret_cast<const float4*>(buf + (c >> 5) * (kM * 128) + r * 128 +
+                                                      ((j ^ sw) << 4));
+    out[0] = v.x, out[1] = v.y, out[2] = v.z, out[3] = v.w;
+  } else if (dt == IA_MASK_BOOL) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(row + (((c >> 4) ^ sw) << 4) + (c & 15));
+#pragma unroll
+    for (int e = 0; e < 4; ++e) out[e] = ((w >> (8 * e)) & 0xffu) ? 0.f : -INFINITY;
+  } else {
+    const uint2 w = *reinterpret_cast<const uint2*>(row + (((c >> 3) ^ sw) << 4) + (c & 7) * 2);
+    if (dt == IA_MASK_BF16) {
+      out[0] = __uint_as_float(w.x << 16), out[1] = __uint_as_float(w.x & 0xffff0000u);
+      out[2] = __uint_as_float(w.y << 16), out[3] = __uint_as_float(w.y & 0xffff0000u);
+    } else {
+      const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+      const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+      out[0] = lo.x, out[1] = lo.y, out[2] = hi.x, out[3] = hi.y;
+    }
+  }
+}
+
+template <int D, int QS, int BN, bool SPARSE, bool VBF16, bool QRAW, bool ROWMASK>
 __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const Params a) {
-  using L = Layout<D, QS, BN, SPARSE>;
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_m, const Params a) {
+  using L = Layout<D, QS, BN, SPARSE, ROWMASK>;
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x;
@@ -333,6 +391,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       mbar_init(bar(L::B_PF + s), kM);
       mbar_init(bar(L::B_OF + s), 1);
     }
+    for (int i = 0; i < L::NSC; ++i) mbar_init(bar(L::B_MF + i), 1);
     mbar_init(bar(L::B_DRAIN), 1);
     mbar_init(bar(L::B_STALL), 1);  // never signalled: the timeout test hook waits on it
     misc[1] = 0;
@@ -393,9 +452,15 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      int kr_last[L::NKS], v_last[L::NVS];
+      if (ROWMASK) prefetch_tmap(&tm_m);
+      int kr_last[L::NKS], v_last[L::NVS], m_last[L::NSC];
       for (int i = 0; i < L::NKS; ++i) kr_last[i] = -1;
       for (int i = 0; i < L::NVS; ++i) v_last[i] = -1;
+      for (int i = 0; i < L::NSC; ++i) m_last[i] = -1;
+      // per-row mask boxes: 128-byte rows of 32 fp32, 64 16-bit or 128 bool keys
+      const int m_kpb = a.rm_dtype == IA_MASK_F32 ? 32 : a.rm_dtype == IA_MASK_BOOL ? 128 : 64;
+      const int m_nbox = a.rm_dtype == IA_MASK_F32 ? 2 : 1;
+      const int m_h = a.rm_h ? h : 0, m_b = a.rm_b ? b : 0;
       // int8 Q codes, or 16-bit Q rows that the softmax warps quantize; either
       // way they are staged in the V buffers until converted
       constexpr int QB = QRAW ? 2 : 1;
@@ -431,6 +496,16 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         for (int c = 0; c < D / 64; ++c)
           tma_load_4d(sm_v + vs * L::VB + c * BN * 128, &tm_v, bar(L::B_VF + vs), c * 64, kt * BN, h, b);
         v_last[vs] = it;
+        if constexpr (ROWMASK) {  // the tile's mask rows, released with the tile's k scales
+          const int ms = it % L::NSC;
+          if (it >= L::NSC) ok = wait_bar(bar(L::B_SCE + ms), ((it / L::NSC) - 1) & 1, ctl, kErrProducer);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar(L::B_MF + ms), m_nbox * kM * 128);
+          for (int x = 0; x < m_nbox; ++x)
+            tma_load_4d(smem_u32(smem + L::OFF_MK + ms * L::MB + x * kM * 128), &tm_m,
+                        bar(L::B_MF + ms), kt * BN + x * m_kpb, q0, m_h, m_b);
+          m_last[ms] = it;
+        }
       }
       if (!ok) {  // let issued copies land before the CTA's shared memory goes away
         drain_bar(bar(L::B_QFULL), 0, a.timeout_ns);
@@ -438,6 +513,8 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
           if (kr_last[i] >= 0) drain_bar(bar(L::B_KRF + i), (kr_last[i] / L::NKS) & 1, a.timeout_ns);
         for (int i = 0; i < L::NVS; ++i)
           if (v_last[i] >= 0) drain_bar(bar(L::B_VF + i), (v_last[i] / L::NVS) & 1, a.timeout_ns);
+        for (int i = 0; i < L::NSC; ++i)
+          if (m_last[i] >= 0) drain_bar(bar(L::B_MF + i), (m_last[i] / L::NSC) & 1, a.timeout_ns);
       }
     }
   } else if (warp == L::W_MMA) {
@@ -535,18 +612,25 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       mrow1 = qt1 < a.Tq ? mrow0 + a.Tk : nullptr;
     }
     const float* ksb = a.k_scale + b * a.ks_sb + h * a.ks_sh;
+    const void* brow = nullptr;  // this (b, h)'s row of per-key offsets
+    if (a.bias != nullptr) {
+      const int es = a.bias_dtype == IA_MASK_F32 ? 4 : a.bias_dtype == IA_MASK_BOOL ? 1 : 2;
+      brow = static_cast<const char*>(a.bias) + (b * a.bias_sb + h * a.bias_sh) * es;
+    }
     for (int it = 0; it < n_it && ok; ++it) {
       const int kt = SPARSE ? static_cast<int>(list[it0 + it]) : it0 + it;
       // Per-key constants of this tile: the global loads are issued first and
       // land while the K tile is widened.
       constexpr int KPT = (BN + 63) / 64;  // keys per converter thread
-      float kv[KPT], bv[KPT];
+      float kv[KPT];
+      uint32_t braw[KPT];
+      bool kval[KPT];
 #pragma unroll
       for (int e = 0; e < KPT; ++e) {
         const int key = kt * BN + ct + 64 * e;
-        const bool valid = key < a.Sk && (a.kv_valid == nullptr || (key & 63) < __ldg(a.kv_valid + (key >> 6)));
-        kv[e] = valid ? __ldg(ksb + (a.gran_block ? (key >> 6) : key)) : 0.f;
-        bv[e] = valid ? (a.bias ? __ldg(a.bias + key) * kLog2e : 0.f) : -INFINITY;
+        kval[e] = key < a.Sk && (a.kv_valid == nullptr || (key & 63) < __ldg(a.kv_valid + (key >> 6)));
+        kv[e] = kval[e] ? __ldg(ksb + (a.gran_block ? (key >> 6) : key)) : 0.f;
+        braw[e] = (kval[e] && brow != nullptr) ? key_bias_bits(brow, key, a.bias_dtype) : 0u;
       }
       // K tile: int8 -> fp16 codes in the swizzled layout the MMA reads
       const int kst = it % L::NKS;
@@ -577,7 +661,8 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       for (int e = 0; e < KPT; ++e) {
         if (ct + 64 * e < BN) {
           ksm[ct + 64 * e] = kv[e];
-          b2m[ct + 64 * e] = bv[e];
+          b2m[ct + 64 * e] =
+              kval[e] ? (brow ? key_bias_value(braw[e], a.bias_dtype) * kLog2e : 0.f) : -INFINITY;
         }
       }
       if (ct == 0) {
@@ -585,7 +670,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         if (a.kv_valid)
           for (int t = (kt * BN) >> 6; t < ((kt + 1) * BN) >> 6 && t * 64 < a.Sk; ++t)
             partial |= __ldg(a.kv_valid + t) < 64;
-        uint32_t f = (a.bias != nullptr || partial) ? 1u : 0u;
+        uint32_t f = (a.bias != nullptr || ROWMASK || partial) ? 1u : 0u;
         if (SPARSE) {
           const uint32_t k0 = mrow0[kt] ? 1u : 0u;
           const uint32_t k1 = (mrow1 != nullptr && mrow1[kt]) ? 1u : 0u;
@@ -646,6 +731,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       if (r == 0) IA_TRACE_POINT(4 * s, it);
       bool w = wait_bar(bar(L::B_SF + s), it & 1, ctl, kErrSoftmax);
       w = w && wait_bar(bar(L::B_SCF + ss), (it / L::NSC) & 1, ctl, kErrSoftmax);
+      if (ROWMASK) w = w && wait_bar(bar(L::B_MF + ss), (it / L::NSC) & 1, ctl, kErrSoftmax);
       ok = __all_sync(0xffffffffu, w);
       if (!ok) break;
       tc_fence_after();
@@ -693,6 +779,12 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
                         cq2, pack2(b4.x, b4.y)), f[0], f[1]);
           unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(k4.z, k4.w)),
                         cq2, pack2(b4.z, b4.w)), f[2], f[3]);
+          if constexpr (ROWMASK) {
+            float mk[4];
+            row_mask4(smem + L::OFF_MK + ss * L::MB, r, c, a.rm_dtype, mk);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f[e] = fmaf(mk[e], kLog2e, f[e]);
+          }
           if (!keep) f[0] = f[1] = f[2] = f[3] = -INFINITY;
           const int q = (c >> 2) & 3;
           mx[q] = fmax3(mx[q], fmaxf(f[0], f[1]), fmaxf(f[2], f[3]));
@@ -852,11 +944,26 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int esiz
   return r == CUDA_SUCCESS;
 }
 
-template <int D, int QS, int BN, bool SPARSE, bool VBF16, bool QRAW>
+template <int D, int QS, int BN, bool SPARSE, bool VBF16, bool QRAW, bool ROWMASK>
 ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** msg) {
-  using L = Layout<D, QS, BN, SPARSE>;
+  using L = Layout<D, QS, BN, SPARSE, ROWMASK>;
   const ia_attn_params& p = A.p;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, tm;
+  std::memset(&tm, 0, sizeof(tm));
+  if constexpr (ROWMASK) {  // per-row mask tiles: [B][H][Sq][Sk], broadcast dims of size 1
+    const int dt = p.mask_dtype;
+    const int es = dt == IA_MASK_F32 ? 4 : dt == IA_MASK_BOOL ? 1 : 2;
+    const CUtensorMapDataType mdt = dt == IA_MASK_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                    : dt == IA_MASK_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                    : dt == IA_MASK_F16  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const int Hm = p.mask_strides[1] != 0 ? p.H : 1, Bm = p.mask_strides[0] != 0 ? p.B : 1;
+    if (!make_map(&tm, mdt, p.mask, es, p.Sk, p.Sq, Hm, Bm, p.mask_strides[2], p.mask_strides[1],
+                  p.mask_strides[0], 128 / es, kM, CU_TENSOR_MAP_SWIZZLE_128B)) {
+      *msg = "cuTensorMapEncodeTiled rejected the mask layout (alignment or stride)";
+      return IA_ERR_INVALID_ARG;
+    }
+  }
   const CUtensorMapDataType qdt = !QRAW ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                   : VBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -876,6 +983,12 @@ ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** ms
   a.q_scale = A.q_scale;
   a.k_scale = A.k_scale;
   a.bias = A.bias;
+  a.bias_dtype = A.bias_dtype;
+  a.bias_sb = A.bias_sb;
+  a.bias_sh = A.bias_sh;
+  a.rm_dtype = p.mask_dtype;
+  a.rm_h = p.mask_strides[1] != 0 ? 1 : 0;
+  a.rm_b = p.mask_strides[0] != 0 ? 1 : 0;
   a.mask = A.mask;
   a.kv_valid = p.kv_valid;
   a.v_scale = p.v_scale;
@@ -913,7 +1026,7 @@ ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** ms
     a.ws_l = a.ws_o + static_cast<int64_t>(nsplit) * rows * D;
   }
   const size_t smem = L::SMEM_FIXED + (SPARSE ? static_cast<size_t>(a.Tk) * 2 : 0);
-  auto kern = attn_fwd_kernel<D, QS, BN, SPARSE, VBF16, QRAW>;
+  auto kern = attn_fwd_kernel<D, QS, BN, SPARSE, VBF16, QRAW, ROWMASK>;
   if (smem > 232448) {
     *msg = "key-tile list does not fit in shared memory (too many key tiles)";
     return IA_ERR_UNSUPPORTED;
@@ -925,7 +1038,7 @@ ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** ms
     return IA_ERR_CUDA;
   }
   dim3 grid((p.Sq + kM * QS - 1) / (kM * QS), p.H, p.B * nsplit);
-  kern<<<grid, L::NWARPS * 32, smem, st>>>(tq, tk, tv, a);
+  kern<<<grid, L::NWARPS * 32, smem, st>>>(tq, tk, tv, tm, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     *msg = cudaGetErrorString(e);
@@ -964,18 +1077,25 @@ template <bool QRAW>
 ia_status dispatch(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** msg) {
   const ia_attn_params& p = A.p;
   const bool bf = p.v_dtype == IA_BF16;
+  if (A.row_mask) {  // one 128-row stage, 64-key tiles, mask tiles by TMA
+    if (p.D == 128)
+      return bf ? run<128, 1, 64, false, true, QRAW, true>(A, num_sms, st, msg)
+                : run<128, 1, 64, false, false, QRAW, true>(A, num_sms, st, msg);
+    return bf ? run<64, 1, 64, false, true, QRAW, true>(A, num_sms, st, msg)
+              : run<64, 1, 64, false, false, QRAW, true>(A, num_sms, st, msg);
+  }
   if (A.mask != nullptr) {
     if (p.D == 128)
-      return bf ? run<128, 1, 64, true, true, QRAW>(A, num_sms, st, msg)
-                : run<128, 1, 64, true, false, QRAW>(A, num_sms, st, msg);
-    return bf ? run<64, 1, 64, true, true, QRAW>(A, num_sms, st, msg)
-              : run<64, 1, 64, true, false, QRAW>(A, num_sms, st, msg);
+      return bf ? run<128, 1, 64, true, true, QRAW, false>(A, num_sms, st, msg)
+                : run<128, 1, 64, true, false, QRAW, false>(A, num_sms, st, msg);
+    return bf ? run<64, 1, 64, true, true, QRAW, false>(A, num_sms, st, msg)
+              : run<64, 1, 64, true, false, QRAW, false>(A, num_sms, st, msg);
   }
   if (p.D == 128)
-    return bf ? run<128, 2, 128, false, true, QRAW>(A, num_sms, st, msg)
-              : run<128, 2, 128, false, false, QRAW>(A, num_sms, st, msg);
-  return bf ? run<64, 2, 128, false, true, QRAW>(A, num_sms, st, msg)
-            : run<64, 2, 128, false, false, QRAW>(A, num_sms, st, msg);
+    return bf ? run<128, 2, 128, false, true, QRAW, false>(A, num_sms, st, msg)
+              : run<128, 2, 128, false, false, QRAW, false>(A, num_sms, st, msg);
+  return bf ? run<64, 2, 128, false, true, QRAW, false>(A, num_sms, st, msg)
+            : run<64, 2, 128, false, false, QRAW, false>(A, num_sms, st, msg);
 }
 
 }  // namespace

@@ -65,8 +65,11 @@ struct AttnLaunch {
   const float* q_scale;
   const float* k_scale;
   const void* v;
-  const float* bias;
-  const uint8_t* mask;
+  const void* bias;        // per-key offsets (fp32 bias, or a general mask with q stride 0)
+  int bias_dtype;          // ia_mask_dtype of `bias`
+  int64_t bias_sb, bias_sh;  // element strides of its per-(b,h) rows
+  int row_mask;            // p.mask varies per query row: read by TMA (p.mask, p.mask_*)
+  const uint8_t* mask;     // block mask
   void* out;
   float* lse;
   ia_attn_params p;

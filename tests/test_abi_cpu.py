@@ -36,9 +36,10 @@ def test_params_struct_layout_matches_header(lib):
 #include <stdio.h>
 #include "ia.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu\n", sizeof(ia_attn_params), offsetof(ia_attn_params, q_strides),
+  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(ia_attn_params), offsetof(ia_attn_params, q_strides),
          offsetof(ia_attn_params, lse_strides), offsetof(ia_attn_params, v_scale),
-         offsetof(ia_attn_params, kv_valid));
+         offsetof(ia_attn_params, kv_valid), offsetof(ia_attn_params, mask),
+         offsetof(ia_attn_params, mask_strides));
   return 0;
 }
 '''
@@ -50,7 +51,8 @@ int main(void) {
         out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()
     P = ia.AttnParams
     assert [int(x) for x in out] == [ctypes.sizeof(P), P.q_strides.offset, P.lse_strides.offset,
-                                     P.v_scale.offset, P.kv_valid.offset]
+                                     P.v_scale.offset, P.kv_valid.offset, P.mask.offset,
+                                     P.mask_strides.offset]
 
 
 def test_params_init_contiguous_strides(lib):
@@ -150,3 +152,28 @@ def test_static_workspace_limit_checked_before_any_work(lib):
     assert b"fixed workspace" in lib.ia_last_error_message()
     assert lib.ia_attention_fwd_static_workspace(fake, fake, fake, fake, fake, None, None, fake,
                                                  None, None, None) == 1
+
+
+def test_mask_argument_errors(lib):
+    fake = ctypes.c_void_p(0x1000)
+    p = _params(lib)
+    p.mask = 0x1000
+    p.mask_strides[:] = [0, 0, 256, 1]
+    assert lib.ia_attention_fwd(fake, fake, fake, fake, fake, fake, None, fake, None,
+                                ctypes.byref(p), None) == 1
+    assert b"either" in lib.ia_last_error_message()
+    p.mask_dtype = 9
+    assert lib.ia_attention_fwd(fake, fake, fake, fake, fake, None, None, fake, None,
+                                ctypes.byref(p), None) == 1
+    p.mask_dtype = 0
+    p.mask_strides[:] = [0, 0, 256, 2]
+    assert lib.ia_attention_fwd(fake, fake, fake, fake, fake, None, None, fake, None,
+                                ctypes.byref(p), None) == 1
+    assert b"key stride" in lib.ia_last_error_message()
+    p.mask_strides[:] = [0, 0, 255, 1]  # per-row rows of 1020 bytes: not 16-byte aligned
+    assert lib.ia_attention_fwd(fake, fake, fake, fake, fake, None, None, fake, None,
+                                ctypes.byref(p), None) == 1
+    assert b"16-byte" in lib.ia_last_error_message()
+    p.mask_strides[:] = [0, 0, 256, 1]
+    assert lib.ia_attention_fwd(fake, fake, fake, fake, fake, None, fake, fake, None,
+                                ctypes.byref(p), None) == 2  # per-row mask with a block mask

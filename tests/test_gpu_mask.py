@@ -1,0 +1,142 @@
+"""General attention masks on the GPU against the oracle.
+
+The forms are those of "int8_attention: masked path costs ~1.8x unmasked,
+and a request for optional return_lse", The measurement: fp32, bf16 and fp16
+additive masks and bool keep-masks, shaped [1,1,1,K], expanded to [1,1,Q,K]
+(stride 0 along queries: the per-key path) or materialised per query row
+(the per-row path, mask tiles by TMA).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from util import assert_lse_close, assert_out_close, ensure_built, to_np
+from workloads import WORKLOADS, make_inputs, skirt_bias, validity_vector
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16, "bool": torch.bool}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+
+
+def make_mask(shape, kind, seed):
+    g = torch.Generator().manual_seed(seed)
+    if kind == "bool":
+        return torch.rand(shape, generator=g) > 0.25
+    return (torch.randn(shape, generator=g) * 2.0).to(DT[kind])
+
+
+def run_and_check(wl, inp, mask, *, quant_q=False, kv_splits=1, expand=False):
+    import int8_qk_quantized_gb300 as ia
+    q8, qs, k8, ks = ia.quantize_qk(inp.q, inp.k, granularity=wl.granularity, kv_valid=inp.kv_valid)
+    md = mask.cuda()
+    if expand:  # a stride-0 view on the device (moving a view copies it densely)
+        md = md.expand(wl.B, wl.H, wl.Sq, wl.Sk)
+    args = dict(mask=md, v_scale=inp.v_scale, kv_valid=inp.kv_valid, granularity=wl.granularity,
+                return_lse=True, kv_splits=kv_splits)
+    if quant_q:
+        o, l = ia.attention_quant_q(inp.q, k8, ks, inp.v, **args)
+    else:
+        o, l = ia.attention(q8, k8, qs, ks, inp.v, **args)
+    ia.device_status()
+    vbs = None if inp.kv_valid is None else inp.kv_valid.cpu().numpy()
+    ro, rl, _ = oracle.quantize_and_attend(
+        to_np(inp.q), to_np(inp.k), to_np(inp.v), granularity=wl.granularity, kv_valid=vbs,
+        v_scale=None if inp.v_scale is None else to_np(inp.v_scale), mask=to_np(mask))
+    valid = None if vbs is None else oracle.row_validity(wl.Sq, vbs)
+    assert_out_close(to_np(o), ro, valid=valid)
+    assert_lse_close(to_np(l), rl, valid=valid)
+    return o, l
+
+
+BASE = WORKLOADS["anima4k"].with_(H=2, Sq=300, Sk=1100, v_scale=True)
+
+
+@pytest.mark.parametrize("kind", ["f32", "bf16", "f16", "bool"])
+def test_per_key_mask_dtypes(kind):
+    inp = make_inputs(BASE, "cuda")
+    if kind == "bool":
+        m = torch.from_numpy(skirt_bias(BASE.Sk, 300) > np.log(1e-3)).view(1, 1, 1, -1)
+    else:
+        m = torch.from_numpy(skirt_bias(BASE.Sk, 300)).to(DT[kind]).view(1, 1, 1, -1)
+    run_and_check(BASE, inp, m)
+
+
+def test_expanded_mask_takes_per_key_path_and_equals_1x1x1xK():
+    import int8_qk_quantized_gb300 as ia
+    inp = make_inputs(BASE, "cuda")
+    m = torch.from_numpy(skirt_bias(BASE.Sk, 300)).to(torch.bfloat16).view(1, 1, 1, -1)
+    o1, l1 = run_and_check(BASE, inp, m, expand=True)
+    o2, l2 = run_and_check(BASE, inp, m)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("shape", ["B1HK", "BH1K"])
+def test_per_batch_head_key_rows(shape):
+    wl = BASE.with_(B=2, H=3)
+    inp = make_inputs(wl, "cuda")
+    dims = (2, 1, 1, wl.Sk) if shape == "B1HK" else (2, 3, 1, wl.Sk)
+    run_and_check(wl, inp, make_mask(dims, "f32", 3))
+
+
+@pytest.mark.parametrize("kind", ["f32", "bf16", "f16", "bool"])
+def test_per_row_mask_dtypes(kind):
+    wl = BASE.with_(Sq=333, Sk=1008)  # ragged query and key tails; 16-byte rows
+    inp = make_inputs(wl, "cuda")
+    run_and_check(wl, inp, make_mask((1, 1, wl.Sq, wl.Sk), kind, 4))
+
+
+def test_per_row_mask_per_batch_and_head():
+    wl = BASE.with_(B=2, H=2, Sq=200, Sk=640, D=64, dtype="fp16", granularity="block64",
+                    v_scale=False)
+    inp = make_inputs(wl, "cuda")
+    run_and_check(wl, inp, make_mask((2, 2, wl.Sq, wl.Sk), "bf16", 5))
+
+
+def test_per_row_mask_fully_masked_rows_and_validity():
+    wl = WORKLOADS["sparse"].with_(H=2, Sq=512, Sk=512, sparse=False)
+    inp = make_inputs(wl, "cuda")
+    inp.kv_valid = torch.from_numpy(validity_vector(512 // 64, 37)).cuda()
+    for t in (inp.q, inp.k, inp.v):
+        t[:, :, 512 - 64 + 37:] = 0  # tile pads are zero
+    m = make_mask((1, 2, wl.Sq, wl.Sk), "bool", 6)
+    m[0, 0, 17] = False
+    m[0, 1, 100:130] = False
+    o, l = run_and_check(wl, inp, m)
+    assert torch.all(o[0, 0, 17] == 0) and torch.isneginf(l[0, 0, 17])
+
+
+def test_per_row_mask_with_fused_q_and_split():
+    import int8_qk_quantized_gb300 as ia
+    wl = BASE.with_(Sq=260, Sk=2112)
+    inp = make_inputs(wl, "cuda")
+    m = make_mask((1, 1, wl.Sq, wl.Sk), "f16", 7)
+    o1, l1 = run_and_check(wl, inp, m)
+    o2, l2 = run_and_check(wl, inp, m, quant_q=True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    run_and_check(wl, inp, m, kv_splits=3)
+
+
+def test_materialised_equals_broadcast_within_tolerance():
+    import int8_qk_quantized_gb300 as ia
+    inp = make_inputs(BASE, "cuda")
+    m = torch.from_numpy(skirt_bias(BASE.Sk, 300)).view(1, 1, 1, -1)
+    o1, l1 = run_and_check(BASE, inp, m)
+    o2, l2 = run_and_check(BASE, inp, m.expand(1, 1, BASE.Sq, BASE.Sk).contiguous())
+    assert (o1.float() - o2.float()).abs().max().item() < 2e-2
+
+
+def test_mask_errors():
+    import int8_qk_quantized_gb300 as ia
+    inp = make_inputs(WORKLOADS["sparse"].with_(H=1, Sq=256, Sk=256), "cuda")
+    q8, qs, k8, ks = ia.quantize_qk(inp.q, inp.k)
+    m = make_mask((1, 1, 256, 256), "f32", 8).cuda()
+    with pytest.raises(ia.IAError, match="block mask"):
+        ia.attention(q8, k8, qs, ks, inp.v, mask=m, block_mask=inp.block_mask)
+    with pytest.raises(ia.IAError, match="either"):
+        ia.attention(q8, k8, qs, ks, inp.v, mask=m, bias=torch.zeros(256, device="cuda"))
