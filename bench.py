@@ -41,8 +41,8 @@ PAGE_SPLIT_MS = 11.05
 # SHA-256 of the kernel sources it was taken on. A launch's traffic is scaled
 # from it per head, with the key-proportional part scaled by the keys of the
 # launch. When the kernel sources change, the figure no longer applies.
-ATTN_TRAFFIC = {"source_sha256": "edc32c366ccc4193ffdfbeb9f8ee2c61f376c0f7c95eaffa7fd0bced7ea8c4d9",
-                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 243976704.0}
+ATTN_TRAFFIC = {"source_sha256": "bdccd35e454401511172abc1bd0cd79b0f4e1501dbc287d3cf92f8d8ea81067e",
+                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 245229824.0}
 
 
 def attn_source_sha():
@@ -231,13 +231,22 @@ def time_workloads(ia, torch, names=("tiny", "sdxl", "anima4k", "anima9k", "spar
         def tq():
             ia.quantize_qk(inp.q, inp.k, granularity=wl.granularity, kv_valid=inp.kv_valid)
 
+        def tk():
+            ia.quantize_qk(None, inp.k, granularity=wl.granularity, kv_valid=inp.kv_valid)
+
         def ta():
             ia.attention(q8, k8, qs, ks, inp.v, bias=inp.bias, block_mask=inp.block_mask,
                          v_scale=inp.v_scale, kv_valid=inp.kv_valid, granularity=wl.granularity,
                          out=out, lse=lse, return_lse=True)
 
+        def tf():
+            ia.attention_quant_q(inp.q, k8, ks, inp.v, bias=inp.bias, block_mask=inp.block_mask,
+                                 v_scale=inp.v_scale, kv_valid=inp.kv_valid,
+                                 granularity=wl.granularity, out=out, lse=lse, return_lse=True)
+
         ms = {}
-        for key, fn in (("quantize_ms", tq), ("attention_ms", ta)):
+        for key, fn in (("quantize_ms", tq), ("attention_ms", ta), ("quantize_k_ms", tk),
+                        ("fused_q_attention_ms", tf)):
             for _ in range(3):
                 fn()
             e0 = torch.cuda.Event(enable_timing=True)
@@ -251,6 +260,8 @@ def time_workloads(ia, torch, names=("tiny", "sdxl", "anima4k", "anima9k", "spar
         ia.device_status()
         ops = algorithmic_ops(wl, kept)
         ms["attention_tops"] = ops / (ms["attention_ms"] * 1e-3) / 1e12
+        ms["two_pass_path_ms"] = ms["quantize_ms"] + ms["attention_ms"]
+        ms["fused_q_path_ms"] = ms["quantize_k_ms"] + ms["fused_q_attention_ms"]
         ms["shape"] = f"B{wl.B} H{wl.H} Sq{wl.Sq} Sk{wl.Sk} D{wl.D} {wl.dtype}"
         if kept is not None:
             ms["kept_tiles_per_row"] = kept
@@ -301,6 +312,43 @@ def run_profile(args):
     ia.device_status()
     print(json.dumps({"profile": name, "workload": wl.name, "H": wl.H,
                       "ms_per_call": e0.elapsed_time(e1) / args.steps}), flush=True)
+
+
+def time_mask_forms(ia, torch, q8, k8, qs, ks, v, bias, out, n=10):
+    """The attn_mask forms of the comfy-kitchen int8_attention issue's table
+    (The measurement) on the same 4096 x 33600 x 56 x 128 problem: ms per
+    call and the ratio to the unmasked call."""
+    import math
+    Sq, Sk = q8.shape[2], k8.shape[2]
+    b16 = bias.to(torch.bfloat16).view(1, 1, 1, -1)
+    forms = {
+        "none": {},
+        "fp32 bias [K]": dict(bias=bias),
+        "bf16 [1,1,1,K]": dict(mask=b16),
+        "fp32 [1,1,1,K]": dict(mask=bias.view(1, 1, 1, -1)),
+        "fp16 [1,1,1,K]": dict(mask=bias.to(torch.float16).view(1, 1, 1, -1)),
+        "bf16 [1,1,Q,K] expanded": dict(mask=b16.expand(1, 1, Sq, Sk)),
+        "bool [1,1,1,K]": dict(mask=(bias > math.log(1e-3)).view(1, 1, 1, -1)),
+        "bf16 [1,1,Q,K] materialised (per-row path)": dict(mask=b16.expand(1, 1, Sq, Sk).contiguous()),
+    }
+    res = {}
+    for name, kw in forms.items():
+        def fn(kw=kw):
+            ia.attention(q8, k8, qs, ks, v, out=out, kv_splits=1, **kw)
+        for _ in range(3):
+            fn()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        res[name] = {"ms": e0.elapsed_time(e1) / n}
+    ia.device_status()
+    for name in res:
+        res[name]["vs_unmasked"] = res[name]["ms"] / res["none"]["ms"]
+    return res
 
 
 def main():
@@ -442,6 +490,22 @@ def main():
     bias_ms = time_call(lambda: ia.attention(q8, k8, qs, ks, v, bias=bias, out=o_full,
                                              lse=l_full, return_lse=True, stream=stream))
     quant_ms = time_call(quantize)
+
+    def step_fused_q():  # K quantized alone; each attention call quantizes Q itself
+        sk_ = (ctypes.c_int64 * 3)(*k.stride()[:3])
+        ia._check(L.ia_quantize_qk(None, ia._ptr(k), ia.BF16, B, H, Sq, Sk, D, None, sk_,
+                                   ia.PER_TOKEN, 1, None, None, None, ia._ptr(k8), None,
+                                   ia._ptr(ks), None, ia._stream(stream)))
+        for (a, b_, bt, o_, l_) in ((lo, hi, None, o_core, l_core),
+                                    (0, lo, bias[:lo], o_l, l_l),
+                                    (hi, Sk, bias[hi:], o_r, l_r)):
+            ia.attention_quant_q(q, k8[:, :, a:b_], ks[:, :, a:b_], v[:, :, a:b_], bias=bt,
+                                 out=o_, lse=l_, return_lse=True, stream=stream)
+        ia.merge_lse(o_core, l_core, o_l, l_l, out=o_core, lse_out=l_core, stream=stream)
+        ia.merge_lse(o_core, l_core, o_r, l_r, out=o_core, lse_out=l_core, stream=stream)
+
+    step_ms = time_call(step, n=10)
+    step_fused_ms = time_call(step_fused_q, n=10)
     merge_ms = time_call(lambda: ia.merge_lse(o_l, l_l, o_r, l_r, out=o_full, lse_out=l_full,
                                               stream=stream))
     ia.device_status()
@@ -490,6 +554,8 @@ def main():
             pg.destroy_process_group()
         return
     others = None if args.no_extra else time_workloads(ia, torch)
+    mask_forms = None if args.no_extra else time_mask_forms(ia, torch, q8, k8, qs, ks, v, bias,
+                                                            o_full)
     cpu = None if args.no_cpu_baseline else cpu_baseline()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -508,6 +574,7 @@ def main():
         "calls_ms": {"unmasked_all_keys": unmasked_ms, "bias_all_keys": bias_ms,
                      "bias_over_unmasked": bias_ms / unmasked_ms, "quantize_qk": quant_ms,
                      "merge_lse": merge_ms,
+                     "step_two_pass": step_ms, "step_fused_q": step_fused_ms,
                      "unmasked_tops": ops / (unmasked_ms * 1e-3) / 1e12,
                      "bias_tops": ops / (bias_ms * 1e-3) / 1e12,
                      "quantize_gbs": quant_bytes / (quant_ms * 1e-3) / 1e9},
@@ -523,6 +590,7 @@ def main():
         "e2e": {"value": weak_value(ws, ops, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "workloads": others,
+        "mask_forms": mask_forms,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
