@@ -9,5 +9,5 @@ See ``oracle/ia_oracle.py`` for the functions and the passages they follow.
 """
 from .ia_oracle import (  # noqa: F401
     k_mean, quantize, row_validity, dequantize, attention, exact_attention, merge,
-    quantize_and_attend, PARITY_STATUS,
+    quantize_and_attend, qk_prologue, round_to_16bit, PARITY_STATUS,
 )

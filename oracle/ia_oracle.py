@@ -29,6 +29,9 @@ Sources (page title, then the part of the page):
   bf16 and fp16 additive masks and bool masks, shaped [1,1,1,K] or expanded
   to [1,1,Q,K]) and the repro (the bool mask is True where the key's weight
   is kept).
+* [Passthrough], the maintainer's reply: RMSNorm + RoPE sit between the
+  projections and attention in modern DiTs (``apply_rope``, ``rms_rope``,
+  ``rms_rope_split_half``) and must run on the 16-bit values.
 * [FlyDSL] "Add optional forward LSE output": "Summary" (LSE = sm_scale*m +
   ln l, natural log), "Kernel implementation" (-inf for fully masked rows;
   split-K combine from the combined maximum and denominator) and "Public API"
@@ -56,6 +59,7 @@ PARITY_STATUS = {
     "attention(mask=)": "pinned (brute-force masked softmax, bool = 0/-inf, row shifts)",
     "exact_attention": "pinned (torch fp64 SDPA, centring invariance)",
     "merge": "pinned (split of one softmax equals the whole)",
+    "qk_prologue": "pinned (torch rms_norm, complex rotation, pair norms, layout permutation)",
 }
 
 
@@ -154,6 +158,73 @@ def quantize(x: np.ndarray, mu: np.ndarray | None = None, granularity: str = "to
     codes = np.clip(np.rint(prod), -127, 127)
     codes = np.where(nz_rows[..., None], codes, 0).astype(np.int8)
     return codes, scale
+
+
+def round_to_16bit(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Round fp32 values to bf16 or fp16 (round-half-to-even) and return the
+    rounded values as float32 (exact). torch's dtype conversion is the library
+    routine used for bf16; numpy's float16 for fp16."""
+    x = np.asarray(x, dtype=np.float32)
+    if dtype == "fp16":
+        return x.astype(np.float16).astype(np.float32)
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).float().numpy()
+
+
+def qk_prologue(x: np.ndarray, *, dtype: str, norm_weight=None, eps: float = 1e-6,
+                rope: str | None = None, cos=None, sin=None, pos0: int = 0) -> np.ndarray:
+    """RMSNorm then rotary embedding of each row of Q or K, rounded to the
+    16-bit type: the activations the unfused path hands to attention.
+
+    [Passthrough] maintainer's reply: in modern DiTs the projections go
+    through RMSNorm + RoPE before attention (``apply_rope``, ``rms_rope``,
+    ``rms_rope_split_half``), and RoPE rotates channel pairs, so it has to run
+    on the 16-bit values before they are quantized.
+
+    Reading (the page gives names, not formulas), per row x of D values:
+      1. RMSNorm (when ``norm_weight`` is given): ss = exact sum of x_d^2
+         rounded once to fp32; ms = fp32(ss / D); r = fp32(1 / fp32(sqrt(
+         fp32(ms + eps)))); y_d = fp32(fp32(x_d * r) * w_d). All fp32 steps are
+         correctly rounded.
+      2. RoPE (when ``rope`` is "interleaved" or "split_half"): pair i is
+         (y[2i], y[2i+1]) or (y[i], y[i + D/2]); with c = cos[p, i],
+         s = sin[p, i] for the row's position p = pos0 + row:
+         a' = fp32(fp32(a c) - fp32(b s)), b' = fp32(fp32(a s) + fp32(b c)),
+         the rotation of (a, b) by the angle whose cosine and sine are given.
+      3. one rounding to the 16-bit type.
+    ``cos`` / ``sin`` are fp32 ``[P, D/2]`` tables. Returns float32 holding
+    16-bit values, same shape as ``x``.
+    """
+    B, H, S, D = x.shape
+    y = np.asarray(x, dtype=np.float32).copy()
+    if norm_weight is not None:
+        w = np.asarray(norm_weight, dtype=np.float32)
+        x64 = y.astype(np.float64)
+        ss = np.empty((B, H, S), dtype=np.float32)
+        for b in range(B):
+            for h in range(H):
+                for r in range(S):
+                    ss[b, h, r] = np.float32(math.fsum((x64[b, h, r] * x64[b, h, r]).tolist()))
+        ms = (ss / np.float32(D)).astype(np.float32)
+        rr = (np.float32(1) / np.sqrt((ms + np.float32(eps)).astype(np.float32))).astype(np.float32)
+        y = ((y * rr[..., None]).astype(np.float32) * w).astype(np.float32)
+    if rope is not None:
+        c = np.asarray(cos, dtype=np.float32)[pos0:pos0 + S]        # [S, D/2]
+        sn = np.asarray(sin, dtype=np.float32)[pos0:pos0 + S]
+        if rope == "interleaved":
+            a, bb = y[..., 0::2], y[..., 1::2]
+        elif rope == "split_half":
+            a, bb = y[..., :D // 2], y[..., D // 2:]
+        else:
+            raise ValueError(rope)
+        a2 = ((a * c).astype(np.float32) - (bb * sn).astype(np.float32)).astype(np.float32)
+        b2 = ((a * sn).astype(np.float32) + (bb * c).astype(np.float32)).astype(np.float32)
+        y = np.empty_like(y)
+        if rope == "interleaved":
+            y[..., 0::2], y[..., 1::2] = a2, b2
+        else:
+            y[..., :D // 2], y[..., D // 2:] = a2, b2
+    return round_to_16bit(y, dtype)
 
 
 def dequantize(codes: np.ndarray, scale: np.ndarray, granularity: str) -> np.ndarray:
@@ -351,11 +422,26 @@ def merge(o1, lse1, o2, lse2):
 
 
 def quantize_and_attend(q, k, v, *, granularity="token", center_k=True, kv_valid=None,
-                        k_mu=None, **attn_kw):
-    """The whole path on CPU: K mean, quantise Q and K, same-quantisation
-    attention. Returns (O, LSE, (q_codes, q_scale, k_codes, k_scale, mu))."""
+                        k_mu=None, prologue=None, **attn_kw):
+    """The whole path on CPU: optional RMSNorm + RoPE of Q and K
+    (:func:`qk_prologue`; ``prologue`` holds ``dtype``, ``q_norm_weight``,
+    ``k_norm_weight``, ``eps``, ``rope``, ``cos``, ``sin``, ``q_pos0``,
+    ``k_pos0``), K mean, quantise Q and K, same-quantisation attention.
+    Returns (O, LSE, (q_codes, q_scale, k_codes, k_scale, mu))."""
     qv = np.asarray(q, dtype=np.float32)
     kv = np.asarray(k, dtype=np.float32)
+    if prologue is not None:
+        pr = dict(prologue)
+        common = dict(dtype=pr["dtype"], eps=pr.get("eps", 1e-6), rope=pr.get("rope"),
+                      cos=pr.get("cos"), sin=pr.get("sin"))
+        qv = qk_prologue(qv, norm_weight=pr.get("q_norm_weight"), pos0=pr.get("q_pos0", 0),
+                         **common)
+        kv = qk_prologue(kv, norm_weight=pr.get("k_norm_weight"), pos0=pr.get("k_pos0", 0),
+                         **common)
+        if kv_valid is not None:  # padding rows stay zero, as the contract has them
+            kv = np.where(row_validity(kv.shape[2], kv_valid)[None, None, :, None], kv, 0)
+            if qv.shape[2] == kv.shape[2]:
+                qv = np.where(row_validity(qv.shape[2], kv_valid)[None, None, :, None], qv, 0)
     mu = None
     if center_k:
         mu = k_mean(kv, kv_valid) if k_mu is None else np.asarray(k_mu, np.float32)

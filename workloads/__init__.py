@@ -128,6 +128,23 @@ def band_random_mask(H: int, T: int, band: int, n_random: int, seed: int) -> np.
     return m
 
 
+def rope_tables(positions: int, D: int, base: float = 10000.0):
+    """cos / sin tables fp32 ``[positions, D/2]`` of the usual rotary
+    frequencies: angle(p, i) = p * base^(-2i/D), computed in float64 and
+    rounded once to float32 (an input of the RoPE prologue, as a model's
+    position embedding is)."""
+    p = np.arange(positions, dtype=np.float64)[:, None]
+    i = np.arange(D // 2, dtype=np.float64)[None, :]
+    ang = p * base ** (-2.0 * i / D)
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+def norm_weight(D: int, seed: int) -> np.ndarray:
+    """A seeded RMSNorm weight fp32 ``[D]``: 1 + N(0, 0.1)."""
+    g = np.random.default_rng(seed)
+    return (1.0 + 0.1 * g.standard_normal(D)).astype(np.float32)
+
+
 def validity_vector(T: int, last_valid: int) -> np.ndarray:
     """int32 ``[T]``: 64 valid rows per tile except the last one."""
     v = np.full(T, TILE, dtype=np.int32)
