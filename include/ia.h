@@ -53,6 +53,42 @@ typedef enum ia_dtype { IA_BF16 = 0, IA_FP16 = 1 } ia_dtype;
 /* One fp32 scale per row ("per token") or per 64-row block of a head. */
 typedef enum ia_granularity { IA_PER_TOKEN = 0, IA_PER_BLOCK64 = 1 } ia_granularity;
 
+/* Channel pairing of a rotary embedding (ia_qk_prologue.rope). */
+typedef enum ia_rope_layout {
+  IA_ROPE_NONE = 0,        /* no rotation */
+  IA_ROPE_INTERLEAVED = 1, /* pairs (2i, 2i+1) */
+  IA_ROPE_SPLIT_HALF = 2   /* pairs (i, i + D/2) */
+} ia_rope_layout;
+
+/*
+ * RMSNorm + RoPE applied to each Q / K row before it is quantized: the step
+ * that "Feature Request: Direct int8 Q/K passthrough between Comfy Kitchen
+ * and SageAttention" (maintainer's reply) places between the projections and
+ * attention in modern DiTs (rms_rope, apply_rope, rms_rope_split_half). Per
+ * row x of D values, with every fp32 operation correctly rounded:
+ *   RMSNorm (weight given): ss = fp32 sum of x_d^2 in a fixed order (the
+ *     squares of each 8 consecutive channels in index order, then the D/8
+ *     partial sums added pairwise, t with t + n/2, until one remains),
+ *     r = 1 / sqrt(ss / D + eps), y_d = (x_d * r) * w_d;
+ *   RoPE (rope != NONE): pair i = (y_a, y_b), c = cos[p][i], s = sin[p][i] at
+ *     the row's position p = pos0 + row: y_a' = y_a c - y_b s, y_b' = y_a s + y_b c;
+ *   then one rounding to the input's 16-bit type; the K mean and the
+ *   quantization then see these values. Padding rows (past kv_valid) stay 0.
+ * The fixed order makes the result the same bit for bit in every kernel that
+ * applies the prologue (ia_quantize_qk_prologue, ia_attention_fwd_quant_q).
+ */
+typedef struct ia_qk_prologue {
+  const float* q_norm_weight; /* fp32 [D] RMSNorm weight of Q rows, or NULL (no norm) */
+  const float* k_norm_weight; /* fp32 [D] for K rows, or NULL */
+  float eps;                  /* RMSNorm epsilon, >= 0 */
+  ia_rope_layout rope;
+  const float* rope_cos;      /* fp32 [rope_positions][D/2], row stride rope_stride */
+  const float* rope_sin;      /* same layout; both 16-byte aligned */
+  int64_t rope_stride;        /* elements between positions: >= D/2, a multiple of 4 */
+  int rope_positions;         /* rows of the tables; pos0 + S must not exceed it */
+  int q_pos0, k_pos0;         /* position of query row 0 and key row 0 */
+} ia_qk_prologue;
+
 /* Element type of a general attention mask (ia_attn_params.mask). */
 typedef enum ia_mask_dtype {
   IA_MASK_F32 = 0,  /* additive logit offset */
@@ -106,6 +142,25 @@ IA_API ia_status ia_quantize_qk(const void* q, const void* k, ia_dtype in_dtype,
                                 int8_t* q_i8, int8_t* k_i8, float* q_scale, float* k_scale,
                                 float* k_mean_out, void* stream);
 
+/*
+ * ia_quantize_qk_prologue -- ia_quantize_qk with an RMSNorm + RoPE prologue
+ * (ia_qk_prologue) applied to each Q and K row first, fused into the same
+ * kernel: the normed, rotated 16-bit rows are never written to memory. The
+ * K mean is taken over the prologue's output. Same arguments and outputs as
+ * ia_quantize_qk; prologue may be NULL (then it is ia_quantize_qk). Errors:
+ * IA_ERR_INVALID_ARG for a negative eps, a rope layout without tables,
+ * misaligned tables, rope_stride < D/2 or not a multiple of 4, or positions
+ * past rope_positions.
+ */
+IA_API ia_status ia_quantize_qk_prologue(const void* q, const void* k, ia_dtype in_dtype, int B,
+                                         int H, int Sq, int Sk, int D,
+                                         const int64_t q_strides[3], const int64_t k_strides[3],
+                                         ia_granularity granularity, int center_k,
+                                         const int32_t* kv_valid, const float* k_mean_in,
+                                         int8_t* q_i8, int8_t* k_i8, float* q_scale,
+                                         float* k_scale, float* k_mean_out,
+                                         const ia_qk_prologue* prologue, void* stream);
+
 /* Shapes, strides and options of one attention call. */
 typedef struct ia_attn_params {
   int B, H, Sq, Sk, D;          /* D is 64 or 128; Sq, Sk >= 0 */
@@ -148,6 +203,9 @@ typedef struct ia_attn_params {
                                    of a bias. q != 0 (a row per query) is read by TMA into
                                    shared memory per key tile: base and the b, h, q strides
                                    16-byte aligned; not combinable with a block mask. */
+  const ia_qk_prologue* q_prologue; /* ia_attention_fwd_quant_q only: RMSNorm + RoPE of
+                                   the Q rows before the in-kernel quantization (its q_*
+                                   fields, eps, rope tables); NULL for none */
 } ia_attn_params;
 
 /* Fill p with contiguous BHSD strides for the given shape (no pointers set). */

@@ -35,6 +35,51 @@ class IAError(RuntimeError):
         self.status = status
 
 
+ROPE_LAYOUTS = {None: 0, "none": 0, "interleaved": 1, "split_half": 2}
+
+
+class QKPrologue(ctypes.Structure):
+    """Mirror of ``ia_qk_prologue`` (RMSNorm + RoPE before quantization)."""
+    _fields_ = [
+        ("q_norm_weight", ctypes.c_void_p), ("k_norm_weight", ctypes.c_void_p),
+        ("eps", ctypes.c_float), ("rope", ctypes.c_int),
+        ("rope_cos", ctypes.c_void_p), ("rope_sin", ctypes.c_void_p),
+        ("rope_stride", ctypes.c_int64), ("rope_positions", ctypes.c_int),
+        ("q_pos0", ctypes.c_int), ("k_pos0", ctypes.c_int),
+    ]
+
+
+def make_prologue(q_norm_weight=None, k_norm_weight=None, eps: float = 1e-6, rope=None,
+                  cos=None, sin=None, q_pos0: int = 0, k_pos0: int = 0):
+    """An ``ia_qk_prologue`` from device tensors: fp32 ``[D]`` norm weights,
+    ``rope`` in (None, "interleaved", "split_half") with fp32 ``[P, D/2]``
+    cos / sin tables. Returns (struct, tensors kept alive with it)."""
+    pr = QKPrologue()
+    keep = []
+    for name, t in (("q_norm_weight", q_norm_weight), ("k_norm_weight", k_norm_weight)):
+        if t is not None:
+            if t.dtype != torch.float32 or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous fp32 tensor")
+            setattr(pr, name, t.data_ptr())
+            keep.append(t)
+    pr.eps = float(eps)
+    pr.rope = ROPE_LAYOUTS[rope]
+    if rope not in (None, "none"):
+        if cos is None or sin is None or cos.shape != sin.shape:
+            raise ValueError("rope needs cos and sin tables of one shape [P, D/2]")
+        for t in (cos, sin):
+            if t.dtype != torch.float32 or t.dim() != 2 or t.stride(1) != 1:
+                raise ValueError("rope tables must be fp32 [P, D/2] with contiguous rows")
+        if cos.stride(0) != sin.stride(0):
+            raise ValueError("cos and sin must share the row stride")
+        pr.rope_cos, pr.rope_sin = cos.data_ptr(), sin.data_ptr()
+        pr.rope_stride = cos.stride(0)
+        pr.rope_positions = cos.shape[0]
+        keep += [cos, sin]
+    pr.q_pos0, pr.k_pos0 = int(q_pos0), int(k_pos0)
+    return pr, keep
+
+
 class AttnParams(ctypes.Structure):
     """Mirror of ``ia_attn_params``."""
     _fields_ = [
@@ -50,7 +95,7 @@ class AttnParams(ctypes.Structure):
         ("workspace_bytes", ctypes.c_size_t),
         ("wait_timeout_ns", ctypes.c_uint64), ("debug_stall", ctypes.c_int),
         ("mask", ctypes.c_void_p), ("mask_dtype", ctypes.c_int),
-        ("mask_strides", ctypes.c_int64 * 4),
+        ("mask_strides", ctypes.c_int64 * 4), ("q_prologue", ctypes.c_void_p),
     ]
 
 
@@ -71,6 +116,10 @@ def load_library():
     L.ia_quantize_qk.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i64p, i64p, i32, i32,
                                  vp, vp, vp, vp, vp, vp, vp, vp]
     L.ia_quantize_qk.restype = i32
+    L.ia_quantize_qk_prologue.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i64p, i64p, i32,
+                                          i32, vp, vp, vp, vp, vp, vp, vp,
+                                          ctypes.POINTER(QKPrologue), vp]
+    L.ia_quantize_qk_prologue.restype = i32
     L.ia_attention_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                    ctypes.POINTER(AttnParams), vp]
     L.ia_attention_fwd.restype = i32
@@ -137,9 +186,11 @@ def _strides3(t):
 
 
 def quantize_qk(q, k, granularity: str = "token", center_k: bool = True, kv_valid=None,
-                k_mean=None, return_mean: bool = False, stream=None):
+                k_mean=None, return_mean: bool = False, stream=None, prologue=None):
     """Quantise Q (may be None) and K to INT8 with symmetric fp32 scales.
 
+    ``prologue`` (from ``make_prologue``) applies RMSNorm + RoPE to each row
+    first, in the same kernel (``ia_quantize_qk_prologue``).
     Returns ``(q8, q_scale, k8, k_scale)`` (``None`` for a skipped input), plus
     the K mean ``[B,H,D]`` that was used when ``return_mean``.
     """
@@ -170,11 +221,15 @@ def quantize_qk(q, k, granularity: str = "token", center_k: bool = True, kv_vali
         kv_valid = kv_valid.to(device=dev, dtype=torch.int32).contiguous()
     if k_mean is not None:
         k_mean = k_mean.to(device=dev, dtype=torch.float32).contiguous()
-    _check(L.ia_quantize_qk(
-        _ptr(q), _ptr(k), dt, B, H, Sq, Sk, D,
-        _strides3(q) if q is not None else None, _strides3(k) if k is not None else None,
-        g, 1 if center_k else 0, _ptr(kv_valid), _ptr(k_mean),
-        _ptr(q8), _ptr(k8), _ptr(qs), _ptr(ks), _ptr(mu), _stream(stream)))
+    args = (_ptr(q), _ptr(k), dt, B, H, Sq, Sk, D,
+            _strides3(q) if q is not None else None, _strides3(k) if k is not None else None,
+            g, 1 if center_k else 0, _ptr(kv_valid), _ptr(k_mean),
+            _ptr(q8), _ptr(k8), _ptr(qs), _ptr(ks), _ptr(mu))
+    if prologue is None:
+        _check(L.ia_quantize_qk(*args, _stream(stream)))
+    else:
+        pr = prologue[0] if isinstance(prologue, tuple) else prologue
+        _check(L.ia_quantize_qk_prologue(*args, ctypes.byref(pr), _stream(stream)))
     res = (q8, qs, k8, ks)
     return res + (mu,) if return_mean else res
 
@@ -297,11 +352,13 @@ def attention(q8, k8, q_scale, k_scale, v, *, bias=None, block_mask=None, sm_sca
 def attention_quant_q(q, k8, k_scale, v, *, bias=None, block_mask=None, sm_scale=None,
                       v_scale=None, kv_valid=None, granularity: str = "token",
                       return_lse: bool = False, out=None, lse=None, stream=None, kv_splits=None,
-                      workspace=None, wait_timeout_ns: int = 0, mask=None):
+                      workspace=None, wait_timeout_ns: int = 0, mask=None, prologue=None):
     """Attention with Q quantized inside the kernel (see ``ia_attention_fwd_quant_q``).
 
     ``q`` is the 16-bit ``[B,H,Sq,D]`` query of V's dtype; ``k8``/``k_scale``
     come from ``quantize_qk(None, k, ...)`` or ``quantize_qk(q, k, ...)``.
+    ``prologue`` (from ``make_prologue``) applies its Q-side RMSNorm + RoPE to
+    the Q rows before the in-kernel quantization.
     The other arguments and the result are those of ``attention``.
     """
     L = load_library()
@@ -310,6 +367,9 @@ def attention_quant_q(q, k8, k_scale, v, *, bias=None, block_mask=None, sm_scale
     p, out, lse, bias, block_mask, _keep = _attn_setup(
         L, q, k8, None, k_scale, v, bias, block_mask, sm_scale, v_scale, kv_valid, granularity,
         return_lse, out, lse, kv_splits, workspace, wait_timeout_ns, False, mask)
+    if prologue is not None:
+        pr = prologue[0] if isinstance(prologue, tuple) else prologue
+        p.q_prologue = ctypes.addressof(pr)
     _check(L.ia_attention_fwd_quant_q(_ptr(q), _ptr(k8), _ptr(k_scale), _ptr(v), _ptr(bias),
                                       _ptr(block_mask), _ptr(out), _ptr(lse), ctypes.byref(p),
                                       _stream(stream)))

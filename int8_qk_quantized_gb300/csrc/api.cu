@@ -89,6 +89,44 @@ ia_status static_workspace(void** out) {
   return IA_OK;
 }
 
+// Checks an RMSNorm + RoPE prologue for rows of width D: Sq / Sk are the
+// row counts it will be applied to (0 when absent). for_quantize: the K half
+// applies too (ia_quantize_qk_prologue); otherwise only the Q half.
+ia_status check_prologue(const ia_qk_prologue* pro, int D, int Sq, int Sk, bool for_quantize) {
+  if (pro == nullptr) return IA_OK;
+  if (!(pro->eps >= 0.f) || !std::isfinite(pro->eps))
+    return fail(IA_ERR_INVALID_ARG, "prologue eps must be finite and >= 0");
+  if (!aligned16(pro->q_norm_weight) || (for_quantize && !aligned16(pro->k_norm_weight)))
+    return fail(IA_ERR_INVALID_ARG, "norm weights must be 16-byte aligned");
+  if (pro->rope != IA_ROPE_NONE) {
+    if (pro->rope != IA_ROPE_INTERLEAVED && pro->rope != IA_ROPE_SPLIT_HALF)
+      return fail(IA_ERR_INVALID_ARG, "rope layout");
+    if (pro->rope_cos == nullptr || pro->rope_sin == nullptr || !aligned16(pro->rope_cos) ||
+        !aligned16(pro->rope_sin))
+      return fail(IA_ERR_INVALID_ARG, "rope tables must be given and 16-byte aligned");
+    if (pro->rope_stride < D / 2 || (pro->rope_stride % 4) != 0)
+      return fail(IA_ERR_INVALID_ARG, "rope_stride must be >= D/2 and a multiple of 4");
+    if (pro->q_pos0 < 0 || pro->k_pos0 < 0 || pro->rope_positions < 0)
+      return fail(IA_ERR_INVALID_ARG, "negative rope position");
+    if (static_cast<int64_t>(pro->q_pos0) + Sq > pro->rope_positions ||
+        (for_quantize && static_cast<int64_t>(pro->k_pos0) + Sk > pro->rope_positions))
+      return fail(IA_ERR_INVALID_ARG, "rows past the rope tables (rope_positions=%d)",
+                  pro->rope_positions);
+  }
+  return IA_OK;
+}
+
+void set_prologue(ia::QuantArgs* a, const ia_qk_prologue* pro, bool is_q) {
+  if (pro == nullptr) return;
+  a->norm_w = is_q ? pro->q_norm_weight : pro->k_norm_weight;
+  a->eps = pro->eps;
+  a->rope = pro->rope;
+  a->rcos = pro->rope_cos;
+  a->rsin = pro->rope_sin;
+  a->rstride = pro->rope_stride;
+  a->pos0 = is_q ? pro->q_pos0 : pro->k_pos0;
+}
+
 // Checks and launch shared by ia_attention_fwd (int8 Q codes and their scales)
 // and ia_attention_fwd_quant_q (16-bit Q rows of p->v_dtype, quantized inside
 // the kernel; q_scale unused).
@@ -149,6 +187,12 @@ ia_status attention(const void* q, bool q_raw, const int8_t* k_i8, const float* 
         return fail(IA_ERR_UNSUPPORTED, "a per-query-row mask cannot be combined with a block mask");
     }
   }
+  if (p->q_prologue != nullptr) {
+    if (!q_raw)
+      return fail(IA_ERR_INVALID_ARG, "params.q_prologue applies to ia_attention_fwd_quant_q only");
+    ia_status ps = check_prologue(p->q_prologue, p->D, p->Sq, 0, false);
+    if (ps != IA_OK) return ps;
+  }
   float sm = p->sm_scale;
   if (std::isnan(sm)) sm = 1.0f / std::sqrt(static_cast<float>(p->D));
   if (!std::isfinite(sm) || sm <= 0.f) return fail(IA_ERR_INVALID_ARG, "sm_scale must be positive");
@@ -181,6 +225,83 @@ ia_status attention(const void* q, bool q_raw, const int8_t* k_i8, const float* 
   const char* msg = "";
   s = ia::launch_attention(a, sms, static_cast<cudaStream_t>(stream), &msg);
   if (s != IA_OK) return fail(s, "attention: %s", msg);
+  return ok();
+}
+
+// Checks and launches of ia_quantize_qk and ia_quantize_qk_prologue.
+ia_status quantize(const void* q, const void* k, ia_dtype in_dtype, int B, int H, int Sq, int Sk,
+                   int D, const int64_t q_strides[3], const int64_t k_strides[3],
+                   ia_granularity granularity, int center_k, const int32_t* kv_valid,
+                   const float* k_mean_in, int8_t* q_i8, int8_t* k_i8, float* q_scale,
+                   float* k_scale, float* k_mean_out, const ia_qk_prologue* pro, void* stream) {
+  if (B < 0 || H < 0 || Sq < 0 || Sk < 0) return fail(IA_ERR_INVALID_ARG, "negative shape");
+  if (D != 64 && D != 128) return fail(IA_ERR_INVALID_ARG, "D must be 64 or 128 (got %d)", D);
+  if (in_dtype != IA_BF16 && in_dtype != IA_FP16) return fail(IA_ERR_INVALID_ARG, "in_dtype");
+  if (granularity != IA_PER_TOKEN && granularity != IA_PER_BLOCK64)
+    return fail(IA_ERR_INVALID_ARG, "granularity");
+  if (q == nullptr && k == nullptr) return fail(IA_ERR_INVALID_ARG, "q and k are both NULL");
+  if (q != nullptr) {
+    if (q_i8 == nullptr || q_scale == nullptr || q_strides == nullptr)
+      return fail(IA_ERR_INVALID_ARG, "q given without q_i8/q_scale/q_strides");
+    if (!aligned16(q) || !strides_ok(q_strides, 3, 2) || !aligned16(q_i8))
+      return fail(IA_ERR_INVALID_ARG, "q rows must be 16-byte aligned (base and b,h,s strides)");
+  }
+  if (k != nullptr) {
+    if (k_i8 == nullptr || k_scale == nullptr || k_strides == nullptr)
+      return fail(IA_ERR_INVALID_ARG, "k given without k_i8/k_scale/k_strides");
+    if (!aligned16(k) || !strides_ok(k_strides, 3, 2) || !aligned16(k_i8))
+      return fail(IA_ERR_INVALID_ARG, "k rows must be 16-byte aligned (base and b,h,s strides)");
+  }
+  if (kv_valid != nullptr && (Sk % 64) != 0)
+    return fail(IA_ERR_INVALID_ARG, "kv_valid requires Sk to be a multiple of 64 (Sk=%d)", Sk);
+  ia_status ps = check_prologue(pro, D, q != nullptr ? Sq : 0, k != nullptr ? Sk : 0, true);
+  if (ps != IA_OK) return ps;
+  int sms = 0;
+  ia_status s = check_device(&sms);
+  if (s != IA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (q != nullptr) {
+    ia::QuantArgs a{};
+    a.x = q;
+    a.sb = q_strides[0];
+    a.sh = q_strides[1];
+    a.ss = q_strides[2];
+    a.B = B;
+    a.H = H;
+    a.S = Sq;
+    a.D = D;
+    a.dtype = in_dtype;
+    a.gran_block = granularity == IA_PER_BLOCK64;
+    a.center = 0;
+    a.valid = (kv_valid != nullptr && Sq == Sk) ? kv_valid : nullptr;
+    a.codes = q_i8;
+    a.scales = q_scale;
+    set_prologue(&a, pro, true);
+    cudaError_t e = ia::launch_quantize(a, sms, st);
+    if (e != cudaSuccess) return fail(IA_ERR_CUDA, "quantize(q): %s", cudaGetErrorString(e));
+  }
+  if (k != nullptr) {
+    ia::QuantArgs a{};
+    a.x = k;
+    a.sb = k_strides[0];
+    a.sh = k_strides[1];
+    a.ss = k_strides[2];
+    a.B = B;
+    a.H = H;
+    a.S = Sk;
+    a.D = D;
+    a.dtype = in_dtype;
+    a.gran_block = granularity == IA_PER_BLOCK64;
+    a.center = center_k ? 1 : 0;
+    a.valid = kv_valid;
+    a.mean_in = center_k ? k_mean_in : nullptr;
+    a.mean_out = center_k ? k_mean_out : nullptr;
+    a.codes = k_i8;
+    a.scales = k_scale;
+    set_prologue(&a, pro, false);
+    cudaError_t e = ia::launch_quantize(a, sms, st);
+    if (e != cudaSuccess) return fail(IA_ERR_CUDA, "quantize(k): %s", cudaGetErrorString(e));
+  }
   return ok();
 }
 
@@ -240,71 +361,20 @@ IA_API ia_status ia_quantize_qk(const void* q, const void* k, ia_dtype in_dtype,
                                 int center_k, const int32_t* kv_valid, const float* k_mean_in,
                                 int8_t* q_i8, int8_t* k_i8, float* q_scale, float* k_scale,
                                 float* k_mean_out, void* stream) {
-  if (B < 0 || H < 0 || Sq < 0 || Sk < 0) return fail(IA_ERR_INVALID_ARG, "negative shape");
-  if (D != 64 && D != 128) return fail(IA_ERR_INVALID_ARG, "D must be 64 or 128 (got %d)", D);
-  if (in_dtype != IA_BF16 && in_dtype != IA_FP16) return fail(IA_ERR_INVALID_ARG, "in_dtype");
-  if (granularity != IA_PER_TOKEN && granularity != IA_PER_BLOCK64)
-    return fail(IA_ERR_INVALID_ARG, "granularity");
-  if (q == nullptr && k == nullptr) return fail(IA_ERR_INVALID_ARG, "q and k are both NULL");
-  if (q != nullptr) {
-    if (q_i8 == nullptr || q_scale == nullptr || q_strides == nullptr)
-      return fail(IA_ERR_INVALID_ARG, "q given without q_i8/q_scale/q_strides");
-    if (!aligned16(q) || !strides_ok(q_strides, 3, 2) || !aligned16(q_i8))
-      return fail(IA_ERR_INVALID_ARG, "q rows must be 16-byte aligned (base and b,h,s strides)");
-  }
-  if (k != nullptr) {
-    if (k_i8 == nullptr || k_scale == nullptr || k_strides == nullptr)
-      return fail(IA_ERR_INVALID_ARG, "k given without k_i8/k_scale/k_strides");
-    if (!aligned16(k) || !strides_ok(k_strides, 3, 2) || !aligned16(k_i8))
-      return fail(IA_ERR_INVALID_ARG, "k rows must be 16-byte aligned (base and b,h,s strides)");
-  }
-  if (kv_valid != nullptr && (Sk % 64) != 0)
-    return fail(IA_ERR_INVALID_ARG, "kv_valid requires Sk to be a multiple of 64 (Sk=%d)", Sk);
-  int sms = 0;
-  ia_status s = check_device(&sms);
-  if (s != IA_OK) return s;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (q != nullptr) {
-    ia::QuantArgs a{};
-    a.x = q;
-    a.sb = q_strides[0];
-    a.sh = q_strides[1];
-    a.ss = q_strides[2];
-    a.B = B;
-    a.H = H;
-    a.S = Sq;
-    a.D = D;
-    a.dtype = in_dtype;
-    a.gran_block = granularity == IA_PER_BLOCK64;
-    a.center = 0;
-    a.valid = (kv_valid != nullptr && Sq == Sk) ? kv_valid : nullptr;
-    a.codes = q_i8;
-    a.scales = q_scale;
-    cudaError_t e = ia::launch_quantize(a, sms, st);
-    if (e != cudaSuccess) return fail(IA_ERR_CUDA, "quantize(q): %s", cudaGetErrorString(e));
-  }
-  if (k != nullptr) {
-    ia::QuantArgs a{};
-    a.x = k;
-    a.sb = k_strides[0];
-    a.sh = k_strides[1];
-    a.ss = k_strides[2];
-    a.B = B;
-    a.H = H;
-    a.S = Sk;
-    a.D = D;
-    a.dtype = in_dtype;
-    a.gran_block = granularity == IA_PER_BLOCK64;
-    a.center = center_k ? 1 : 0;
-    a.valid = kv_valid;
-    a.mean_in = center_k ? k_mean_in : nullptr;
-    a.mean_out = center_k ? k_mean_out : nullptr;
-    a.codes = k_i8;
-    a.scales = k_scale;
-    cudaError_t e = ia::launch_quantize(a, sms, st);
-    if (e != cudaSuccess) return fail(IA_ERR_CUDA, "quantize(k): %s", cudaGetErrorString(e));
-  }
-  return ok();
+  return quantize(q, k, in_dtype, B, H, Sq, Sk, D, q_strides, k_strides, granularity, center_k,
+                  kv_valid, k_mean_in, q_i8, k_i8, q_scale, k_scale, k_mean_out, nullptr, stream);
+}
+
+IA_API ia_status ia_quantize_qk_prologue(const void* q, const void* k, ia_dtype in_dtype, int B,
+                                         int H, int Sq, int Sk, int D,
+                                         const int64_t q_strides[3], const int64_t k_strides[3],
+                                         ia_granularity granularity, int center_k,
+                                         const int32_t* kv_valid, const float* k_mean_in,
+                                         int8_t* q_i8, int8_t* k_i8, float* q_scale,
+                                         float* k_scale, float* k_mean_out,
+                                         const ia_qk_prologue* prologue, void* stream) {
+  return quantize(q, k, in_dtype, B, H, Sq, Sk, D, q_strides, k_strides, granularity, center_k,
+                  kv_valid, k_mean_in, q_i8, k_i8, q_scale, k_scale, k_mean_out, prologue, stream);
 }
 
 IA_API ia_status ia_attention_fwd(const int8_t* q_i8, const int8_t* k_i8, const float* q_scale,

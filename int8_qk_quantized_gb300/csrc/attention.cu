@@ -109,6 +109,15 @@ struct Params {
   float* ws_o;       // nsplit >= 2: fp32 partial O [nsplit][B][H][Sq][D]
   float* ws_l;       //              fp32 partial LSE [nsplit][B][H][Sq]
   int B;
+  // QRAW kernels: RMSNorm + RoPE of the Q rows before the in-kernel quantization
+  int q_pro;          // 1: apply the fields below
+  const float* qp_w;   // fp32 [D] or null
+  float qp_eps;
+  int qp_rope;         // ia_rope_layout
+  const float* qp_cos;
+  const float* qp_sin;
+  int64_t qp_stride;
+  int qp_pos0;
 };
 
 template <int D, int QS, int BN, bool SPARSE, bool ROWMASK = false>
@@ -341,6 +350,110 @@ __device__ __forceinline__ void row_mask4(const uint8_t* buf, int r, int c, int 
       out[0] = lo.x, out[1] = lo.y, out[2] = hi.x, out[3] = hi.y;
     }
   }
+}
+
+// RMSNorm + RoPE of one raw 16-bit Q row in shared memory, in place, before
+// the fused quantization ("Feature Request: Direct int8 Q/K passthrough
+// between Comfy Kitchen and SageAttention", maintainer's reply: rms_rope /
+// apply_rope / rms_rope_split_half run on the 16-bit rows before attention):
+// ss = fp32 sum of squares (each 8-channel chunk in index order, then the D/8
+// chunk sums added pairwise, t with t + n/2), r = 1/sqrt(ss/D + eps),
+// y = (x r) w, the rotation a' = ac - bs, b' = as + bc of each channel pair
+// with the tables at position `pos`, one rounding to the 16-bit type. The same
+// fp32 sequence as the quantize kernel's prologue, so the codes agree bit for
+// bit with ia_quantize_qk_prologue. Chunks are visited from chunk r on, which
+// spreads a warp's 32 rows over the shared-memory banks.
+template <int D, bool BF16>
+__device__ __noinline__ void q_prologue_row(uint8_t* row, int r, int64_t pos, const Params& a) {
+  constexpr int CPR = D / 8;  // 16-byte chunks per row
+  const bool split = a.qp_rope == IA_ROPE_SPLIT_HALF;
+  float rf = 1.f;
+  if (a.qp_w != nullptr) {
+    float part[CPR];
+    for (int c = 0; c < CPR; ++c) {
+      const int cc = (c + r) & (CPR - 1);
+      const uint4 w = *reinterpret_cast<const uint4*>(row + cc * 16);
+      const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+      float sum = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = unpack_16x2<BF16>(in[e]);
+        sum = e == 0 ? __fmul_rn(f.x, f.x) : __fadd_rn(sum, __fmul_rn(f.x, f.x));
+        sum = __fadd_rn(sum, __fmul_rn(f.y, f.y));
+      }
+      part[cc] = sum;
+    }
+#pragma unroll
+    for (int n = CPR; n > 1; n >>= 1)
+#pragma unroll
+      for (int t = 0; t < n / 2; ++t) part[t] = __fadd_rn(part[t], part[t + n / 2]);
+    rf = __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(__fdiv_rn(part[0], static_cast<float>(D)), a.qp_eps)));
+  }
+  const float* cs = a.qp_cos + pos * a.qp_stride;
+  const float* sn = a.qp_sin + pos * a.qp_stride;
+  const int NU = split ? CPR / 2 : CPR;  // a chunk, or a chunk and its partner half
+  for (int c = 0; c < NU; ++c) {
+    const int u = (c + r) & (NU - 1);
+    const int ch[2] = {u, u + CPR / 2};
+    float y[2][8];
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      if (hlf == 1 && !split) break;
+      const uint4 w = *reinterpret_cast<const uint4*>(row + ch[hlf] * 16);
+      const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = unpack_16x2<BF16>(in[e]);
+        y[hlf][2 * e] = f.x, y[hlf][2 * e + 1] = f.y;
+      }
+      if (a.qp_w != nullptr) {
+        const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.qp_w + ch[hlf] * 8));
+        const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.qp_w + ch[hlf] * 8 + 4));
+        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[hlf][i] = __fmul_rn(__fmul_rn(y[hlf][i], rf), wv[i]);
+      }
+    }
+    if (a.qp_rope == IA_ROPE_INTERLEAVED) {  // pairs (2i, 2i+1): i = 4u .. 4u+3
+      const float4 c4 = __ldg(reinterpret_cast<const float4*>(cs + u * 4));
+      const float4 s4 = __ldg(reinterpret_cast<const float4*>(sn + u * 4));
+      const float cv[4] = {c4.x, c4.y, c4.z, c4.w}, sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float x0 = y[0][2 * j], x1 = y[0][2 * j + 1];
+        y[0][2 * j] = __fsub_rn(__fmul_rn(x0, cv[j]), __fmul_rn(x1, sv[j]));
+        y[0][2 * j + 1] = __fadd_rn(__fmul_rn(x0, sv[j]), __fmul_rn(x1, cv[j]));
+      }
+    } else if (split) {  // pairs (i, i + D/2): i = 8u .. 8u+7
+      const float4 c0 = __ldg(reinterpret_cast<const float4*>(cs + u * 8));
+      const float4 c1 = __ldg(reinterpret_cast<const float4*>(cs + u * 8 + 4));
+      const float4 s0 = __ldg(reinterpret_cast<const float4*>(sn + u * 8));
+      const float4 s1 = __ldg(reinterpret_cast<const float4*>(sn + u * 8 + 4));
+      const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float x0 = y[0][i], x1 = y[1][i];
+        y[0][i] = __fsub_rn(__fmul_rn(x0, cv[i]), __fmul_rn(x1, sv[i]));
+        y[1][i] = __fadd_rn(__fmul_rn(x0, sv[i]), __fmul_rn(x1, cv[i]));
+      }
+    }
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      if (hlf == 1 && !split) break;
+      uint32_t hv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if constexpr (BF16) hv[e] = cvt_bf16x2(y[hlf][2 * e], y[hlf][2 * e + 1]);
+        else hv[e] = cvt_f16x2(y[hlf][2 * e], y[hlf][2 * e + 1]);
+      }
+      *reinterpret_cast<uint4*>(row + ch[hlf] * 16) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    }
+  }
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 template <int D, int QS, int BN, bool SPARSE, bool VBF16, bool QRAW, bool ROWMASK>
@@ -696,15 +809,22 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     bool ok = true;
     if constexpr (QRAW) {
       // This thread quantizes its own row (per 64-row block: each of the
-      // block's two warps also scans the other warp's rows, so no barrier
-      // between warps is needed).
+      // block's two warps also scans the other warp's rows; without the
+      // prologue those rows are not modified, so no barrier is needed).
       ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_QFULL), 0, ctl, kErrSoftmax));
+      uint8_t* raw = smem + L::OFF_V + static_cast<size_t>(s * kM) * D * 2;
+      auto quantized = [&](int rr) {  // row rr of this stage: real and not padding
+        const int gr = q0 + s * kM + rr;
+        return gr < a.Sq && !(a.pad_query && (gr & 63) >= __ldg(a.kv_valid + (gr >> 6)));
+      };
+      if (a.q_pro) {  // RMSNorm + RoPE of the thread's own row, in place
+        if (ok && quantized(r))
+          q_prologue_row<D, VBF16>(raw + r * D * 2, r, static_cast<int64_t>(a.qp_pos0) + q0 + s * kM + r, a);
+        // a 64-row block's two warps read each other's rows below: both warps
+        // always reach this barrier (its condition is uniform over the CTA)
+        if (a.gran_block) named_bar_sync(1 + (warp >> 1), 64);
+      }
       if (ok) {
-        const uint8_t* raw = smem + L::OFF_V + static_cast<size_t>(s * kM) * D * 2;
-        auto quantized = [&](int rr) {  // row rr of this stage: real and not padding
-          const int gr = q0 + s * kM + rr;
-          return gr < a.Sq && !(a.pad_query && (gr & 63) >= __ldg(a.kv_valid + (gr >> 6)));
-        };
         const bool keep = quantized(r);
         uint32_t am = keep ? row_amax_bits<D>(raw + r * D * 2, r) : 0u;
         if (a.gran_block) {
@@ -980,6 +1100,17 @@ ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** ms
     return IA_ERR_INVALID_ARG;
   }
   Params a{};
+  if (QRAW && p.q_prologue != nullptr) {
+    const ia_qk_prologue& pr = *p.q_prologue;
+    a.q_pro = (pr.q_norm_weight != nullptr || pr.rope != IA_ROPE_NONE) ? 1 : 0;
+    a.qp_w = pr.q_norm_weight;
+    a.qp_eps = pr.eps;
+    a.qp_rope = pr.rope;
+    a.qp_cos = pr.rope_cos;
+    a.qp_sin = pr.rope_sin;
+    a.qp_stride = pr.rope_stride;
+    a.qp_pos0 = pr.q_pos0;
+  }
   a.q_scale = A.q_scale;
   a.k_scale = A.k_scale;
   a.bias = A.bias;

@@ -20,6 +20,15 @@ struct QuantArgs {
   float* mean_out;         // optional [B,H,D] mean that was used
   int8_t* codes;           // [B,H,S,D] contiguous
   float* scales;           // [B,H,S] or [B,H,ceil(S/64)] contiguous
+  // RMSNorm + RoPE prologue of each row (ia_qk_prologue); off when norm_w is
+  // null and rope is IA_ROPE_NONE
+  const float* norm_w;     // fp32 [D], 16-byte aligned
+  float eps;
+  int rope;                // ia_rope_layout
+  const float* rcos;       // fp32 [positions][rstride]
+  const float* rsin;
+  int64_t rstride;
+  int pos0;                // position of row 0
 };
 
 cudaError_t launch_quantize(const QuantArgs& a, int num_sms, cudaStream_t st);

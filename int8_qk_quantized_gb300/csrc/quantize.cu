@@ -83,9 +83,89 @@ __device__ __forceinline__ void store_codes(int8_t* dst, const float (&x)[8], fl
   *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
 }
 
+template <int DT>
+__device__ __forceinline__ float round16(float x) {
+  if constexpr (DT == IA_BF16) return __bfloat162float(__float2bfloat16_rn(x));
+  else return __half2float(__float2half_rn(x));
+}
+
+// RMSNorm + RoPE prologue ("Feature Request: Direct int8 Q/K passthrough
+// between Comfy Kitchen and SageAttention", maintainer's reply: rms_rope,
+// apply_rope, rms_rope_split_half run on the 16-bit rows before attention)
+// on this thread's 8 values of row rr; the row's TPR threads are adjacent
+// lanes of one warp and every lane of the warp calls this.
+//   ss = sum of squares in a fixed fp32 order: this thread's 8 squares in
+//        index order, then the TPR partial sums added pairwise, t with
+//        t + n/2 (a butterfly of symmetric adds: every lane ends with the
+//        same value),
+//   r = 1 / sqrt(ss / D + eps), y = (x * r) * w   (IEEE fp32 steps),
+//   pair (a, b) with cos c and sin s of position pos0 + rr:
+//        a' = a c - b s, b' = a s + b c,
+// then one rounding to the 16-bit type. Rows that are not data (ok false)
+// come out as 0 and read no table entry.
+template <int D, int DT>
+__device__ __forceinline__ void prologue8(float (&v)[8], bool ok, int rr, int tc,
+                                          const QuantArgs& a) {
+  constexpr int TPR = D / 8;
+  if (a.norm_w != nullptr) {
+    float ss = __fmul_rn(v[0], v[0]);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) ss = __fadd_rn(ss, __fmul_rn(v[i], v[i]));
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
+    const float r = __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(D)), a.eps)));
+    const float4 w0 = __ldg(reinterpret_cast<const float4*>(a.norm_w + tc * 8));
+    const float4 w1 = __ldg(reinterpret_cast<const float4*>(a.norm_w + tc * 8 + 4));
+    const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(__fmul_rn(v[i], r), w[i]);
+  }
+  if (a.rope == IA_ROPE_INTERLEAVED) {
+    float c[4] = {1.f, 1.f, 1.f, 1.f}, sn[4] = {0.f, 0.f, 0.f, 0.f};
+    if (ok) {
+      const int64_t o = static_cast<int64_t>(a.pos0 + rr) * a.rstride + tc * 4;
+      const float4 c4 = __ldg(reinterpret_cast<const float4*>(a.rcos + o));
+      const float4 s4 = __ldg(reinterpret_cast<const float4*>(a.rsin + o));
+      c[0] = c4.x, c[1] = c4.y, c[2] = c4.z, c[3] = c4.w;
+      sn[0] = s4.x, sn[1] = s4.y, sn[2] = s4.z, sn[3] = s4.w;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float x0 = v[2 * j], x1 = v[2 * j + 1];
+      v[2 * j] = __fsub_rn(__fmul_rn(x0, c[j]), __fmul_rn(x1, sn[j]));
+      v[2 * j + 1] = __fadd_rn(__fmul_rn(x0, sn[j]), __fmul_rn(x1, c[j]));
+    }
+  } else if (a.rope == IA_ROPE_SPLIT_HALF) {
+    float pv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) pv[i] = __shfl_xor_sync(0xffffffffu, v[i], TPR / 2);
+    const bool first = tc < TPR / 2;  // holds the a of its pairs, the partner the b
+    float c[8], sn[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = 1.f, sn[i] = 0.f;
+    if (ok) {
+      const int64_t o = static_cast<int64_t>(a.pos0 + rr) * a.rstride + (tc % (TPR / 2)) * 8;
+      const float4 c0 = __ldg(reinterpret_cast<const float4*>(a.rcos + o));
+      const float4 c1 = __ldg(reinterpret_cast<const float4*>(a.rcos + o + 4));
+      const float4 s0 = __ldg(reinterpret_cast<const float4*>(a.rsin + o));
+      const float4 s1 = __ldg(reinterpret_cast<const float4*>(a.rsin + o + 4));
+      c[0] = c0.x, c[1] = c0.y, c[2] = c0.z, c[3] = c0.w, c[4] = c1.x, c[5] = c1.y, c[6] = c1.z, c[7] = c1.w;
+      sn[0] = s0.x, sn[1] = s0.y, sn[2] = s0.z, sn[3] = s0.w, sn[4] = s1.x, sn[5] = s1.y, sn[6] = s1.z, sn[7] = s1.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float x0 = first ? v[i] : pv[i], x1 = first ? pv[i] : v[i];
+      v[i] = first ? __fsub_rn(__fmul_rn(x0, c[i]), __fmul_rn(x1, sn[i]))
+                   : __fadd_rn(__fmul_rn(x0, sn[i]), __fmul_rn(x1, c[i]));
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = ok ? round16<DT>(v[i]) : 0.f;
+}
+
 // grid: (chunks, H, B). Chunk c holds rows [c*chunk, min(S, (c+1)*chunk)).
 // With CLUSTER_MEAN the chunks of one head are one cluster and compute the mean.
-template <int D, int DT, bool CLUSTER_MEAN>
+template <int D, int DT, bool CLUSTER_MEAN, bool PRO>
 __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a, int chunk) {
   constexpr int TPR = D / 8;            // threads per row, 8 elements each
   constexpr int RPP = kThreads / TPR;   // rows per pass
@@ -113,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a
 #pragma unroll
       for (int i = 0; i < 8; ++i) hi[i] = lo[i] = 0.f;
       // 8 rows of 16-byte loads in flight per thread, kept packed until used
-      constexpr int U1 = 8;
+      constexpr int U1 = PRO ? 4 : 8;  // the prologue needs registers of its own
       for (int base = r0; base < r1; base += U1 * RPP) {
         uint4 w[U1];
 #pragma unroll
@@ -127,6 +207,10 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a
         for (int u = 0; u < U1; ++u) {
           float v[8];
           unpack8<DT>(w[u], v);
+          if constexpr (PRO) {
+            const int rr = base + u * RPP + tr;
+            prologue8<D, DT>(v, rr < r1 && row_valid(a.valid, rr), rr, tc, a);
+          }
 #pragma unroll
           for (int i = 0; i < 8; ++i) two_sum_acc(hi[i], lo[i], v[i]);
         }
@@ -178,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a
     // The loop bound is uniform across the CTA: every lane reaches the shuffles.
     // The chunk is walked from its end, so rows the mean pass read last are
     // read again first, while they may still sit in L2.
-    constexpr int U2 = 8;  // rows of 16-byte loads in flight per thread
+    constexpr int U2 = PRO ? 4 : 8;  // rows of 16-byte loads in flight per thread
     const int nbase = (r1 - r0 + U2 * RPP - 1) / (U2 * RPP);
     for (int ib = nbase - 1; ib >= 0; --ib) {
       const int base = r0 + ib * U2 * RPP;
@@ -196,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a
         const int rr = base + u * RPP + tr;
         float v[8];
         unpack8<DT>(w[u], v);
+        if constexpr (PRO) prologue8<D, DT>(v, ok[u], rr, tc, a);
         float m = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -230,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[p][i] = 0.f;
       }
+      if constexpr (PRO) prologue8<D, DT>(v[p], rr < r1 && row_valid(a.valid, rr), rr, tc, a);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         if (a.center && rr < r1 && row_valid(a.valid, rr)) v[p][i] = __fsub_rn(v[p][i], mu[i]);
@@ -255,14 +341,14 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a
   }
 }
 
-template <int D, int DT>
+template <int D, int DT, bool PRO>
 cudaError_t launch_typed(const QuantArgs& a, int num_sms, cudaStream_t st) {
   const int BH = a.B * a.H;
   if (a.center && a.mean_in == nullptr) {
     // One cluster per head, sized so that the grid fills two CTAs per SM in
     // one wave where the heads allow (up to the largest cluster the device
     // can place; 16 needs the non-portable cluster size attribute).
-    auto kern = quantize_kernel<D, DT, true>;
+    auto kern = quantize_kernel<D, DT, true, PRO>;
     static int max_cl = 0;
     if (max_cl == 0) {
       max_cl = 8;
@@ -300,7 +386,7 @@ cudaError_t launch_typed(const QuantArgs& a, int num_sms, cudaStream_t st) {
   // Rows split into chunks of 256 (a multiple of 64); no cluster.
   const int chunk = 256;
   dim3 grid((a.S + chunk - 1) / chunk, a.H, a.B);
-  quantize_kernel<D, DT, false><<<grid, kThreads, 0, st>>>(a, chunk);
+  quantize_kernel<D, DT, false, PRO><<<grid, kThreads, 0, st>>>(a, chunk);
   return cudaGetLastError();
 }
 
@@ -308,12 +394,20 @@ cudaError_t launch_typed(const QuantArgs& a, int num_sms, cudaStream_t st) {
 
 cudaError_t launch_quantize(const QuantArgs& a, int num_sms, cudaStream_t st) {
   if (a.S == 0 || a.B == 0 || a.H == 0) return cudaSuccess;
-  if (a.D == 128) {
-    return a.dtype == IA_BF16 ? launch_typed<128, IA_BF16>(a, num_sms, st)
-                              : launch_typed<128, IA_FP16>(a, num_sms, st);
+  const bool pro = a.norm_w != nullptr || a.rope != IA_ROPE_NONE;
+  if (pro) {
+    if (a.D == 128)
+      return a.dtype == IA_BF16 ? launch_typed<128, IA_BF16, true>(a, num_sms, st)
+                                : launch_typed<128, IA_FP16, true>(a, num_sms, st);
+    return a.dtype == IA_BF16 ? launch_typed<64, IA_BF16, true>(a, num_sms, st)
+                              : launch_typed<64, IA_FP16, true>(a, num_sms, st);
   }
-  return a.dtype == IA_BF16 ? launch_typed<64, IA_BF16>(a, num_sms, st)
-                            : launch_typed<64, IA_FP16>(a, num_sms, st);
+  if (a.D == 128) {
+    return a.dtype == IA_BF16 ? launch_typed<128, IA_BF16, false>(a, num_sms, st)
+                              : launch_typed<128, IA_FP16, false>(a, num_sms, st);
+  }
+  return a.dtype == IA_BF16 ? launch_typed<64, IA_BF16, false>(a, num_sms, st)
+                            : launch_typed<64, IA_FP16, false>(a, num_sms, st);
 }
 
 }  // namespace ia

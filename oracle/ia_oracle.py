@@ -182,10 +182,14 @@ def qk_prologue(x: np.ndarray, *, dtype: str, norm_weight=None, eps: float = 1e-
     on the 16-bit values before they are quantized.
 
     Reading (the page gives names, not formulas), per row x of D values:
-      1. RMSNorm (when ``norm_weight`` is given): ss = exact sum of x_d^2
-         rounded once to fp32; ms = fp32(ss / D); r = fp32(1 / fp32(sqrt(
-         fp32(ms + eps)))); y_d = fp32(fp32(x_d * r) * w_d). All fp32 steps are
-         correctly rounded.
+      1. RMSNorm (when ``norm_weight`` is given): ss = the fp32 sum of the
+         squares x_d^2 (each exact in fp32 for 16-bit x) in a fixed order --
+         the squares of each 8 consecutive channels summed in index order,
+         then the D/8 partial sums added pairwise, t with t + n/2, until one
+         remains; ms = fp32(ss / D); r = fp32(1 / fp32(sqrt(fp32(ms + eps))));
+         y_d = fp32(fp32(x_d * r) * w_d). All fp32 steps are correctly rounded.
+         The order is the one the GPU kernels use (the pages fix none), so the
+         16-bit results, and the codes decided from them, agree bit for bit.
       2. RoPE (when ``rope`` is "interleaved" or "split_half"): pair i is
          (y[2i], y[2i+1]) or (y[i], y[i + D/2]); with c = cos[p, i],
          s = sin[p, i] for the row's position p = pos0 + row:
@@ -199,12 +203,16 @@ def qk_prologue(x: np.ndarray, *, dtype: str, norm_weight=None, eps: float = 1e-
     y = np.asarray(x, dtype=np.float32).copy()
     if norm_weight is not None:
         w = np.asarray(norm_weight, dtype=np.float32)
-        x64 = y.astype(np.float64)
-        ss = np.empty((B, H, S), dtype=np.float32)
-        for b in range(B):
-            for h in range(H):
-                for r in range(S):
-                    ss[b, h, r] = np.float32(math.fsum((x64[b, h, r] * x64[b, h, r]).tolist()))
+        sq = (y * y).astype(np.float32)                                  # exact squares
+        part = sq[..., 0::8].copy()                                      # [B,H,S,D/8]
+        for j in range(1, 8):
+            part = (part + sq[..., j::8]).astype(np.float32)             # index order
+        n = D // 8
+        while n > 1:
+            half = n // 2
+            part = (part[..., :half] + part[..., half:n]).astype(np.float32)
+            n = half
+        ss = part[..., 0]
         ms = (ss / np.float32(D)).astype(np.float32)
         rr = (np.float32(1) / np.sqrt((ms + np.float32(eps)).astype(np.float32))).astype(np.float32)
         y = ((y * rr[..., None]).astype(np.float32) * w).astype(np.float32)

@@ -36,10 +36,12 @@ def test_params_struct_layout_matches_header(lib):
 #include <stdio.h>
 #include "ia.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(ia_attn_params), offsetof(ia_attn_params, q_strides),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(ia_attn_params), offsetof(ia_attn_params, q_strides),
          offsetof(ia_attn_params, lse_strides), offsetof(ia_attn_params, v_scale),
          offsetof(ia_attn_params, kv_valid), offsetof(ia_attn_params, mask),
-         offsetof(ia_attn_params, mask_strides));
+         offsetof(ia_attn_params, mask_strides), offsetof(ia_attn_params, q_prologue));
+  printf("%zu %zu %zu %zu\n", sizeof(ia_qk_prologue), offsetof(ia_qk_prologue, eps),
+         offsetof(ia_qk_prologue, rope_stride), offsetof(ia_qk_prologue, k_pos0));
   return 0;
 }
 '''
@@ -50,9 +52,12 @@ int main(void) {
         subprocess.run(["gcc", "-I", os.path.dirname(HEADER), c, "-o", exe], check=True)
         out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()
     P = ia.AttnParams
+    Q = ia.QKPrologue
     assert [int(x) for x in out] == [ctypes.sizeof(P), P.q_strides.offset, P.lse_strides.offset,
                                      P.v_scale.offset, P.kv_valid.offset, P.mask.offset,
-                                     P.mask_strides.offset]
+                                     P.mask_strides.offset, P.q_prologue.offset,
+                                     ctypes.sizeof(Q), Q.eps.offset, Q.rope_stride.offset,
+                                     Q.k_pos0.offset]
 
 
 def test_params_init_contiguous_strides(lib):
@@ -177,3 +182,30 @@ def test_mask_argument_errors(lib):
     p.mask_strides[:] = [0, 0, 256, 1]
     assert lib.ia_attention_fwd(fake, fake, fake, fake, fake, None, fake, fake, None,
                                 ctypes.byref(p), None) == 2  # per-row mask with a block mask
+
+
+def test_prologue_argument_errors(lib):
+    import int8_qk_quantized_gb300 as ia
+    fake = ctypes.c_void_p(0x1000)
+    st = (ctypes.c_int64 * 3)(128 * 64, 64 * 128, 128)
+    pr = ia.QKPrologue()
+    pr.eps = -1.0
+    args = (fake, fake, 0, 1, 1, 64, 64, 128, st, st, 0, 1, None, None, fake, fake, fake, fake, None)
+    assert lib.ia_quantize_qk_prologue(*args, ctypes.byref(pr), None) == 1
+    assert b"eps" in lib.ia_last_error_message()
+    pr.eps = 1e-6
+    pr.rope = 2  # split half without tables
+    assert lib.ia_quantize_qk_prologue(*args, ctypes.byref(pr), None) == 1
+    pr.rope_cos = pr.rope_sin = 0x2000
+    pr.rope_stride = 64
+    pr.rope_positions = 50  # 64 rows past a 50-position table
+    assert lib.ia_quantize_qk_prologue(*args, ctypes.byref(pr), None) == 1
+    assert b"rope" in lib.ia_last_error_message()
+    pr.rope_positions = 64
+    pr.rope_stride = 30  # < D/2
+    assert lib.ia_quantize_qk_prologue(*args, ctypes.byref(pr), None) == 1
+    p = _params(lib)
+    p.q_prologue = ctypes.addressof(pr)
+    assert lib.ia_attention_fwd(fake, fake, fake, fake, fake, None, None, fake, None,
+                                ctypes.byref(p), None) == 1
+    assert b"quant_q" in lib.ia_last_error_message()
