@@ -314,6 +314,53 @@ def run_profile(args):
                       "ms_per_call": e0.elapsed_time(e1) / args.steps}), flush=True)
 
 
+def time_prologue(ia, torch, names=("anima4k", "anima9k"), n=10):
+    """RMSNorm + RoPE (split-half pairs, both weights) fused before the
+    quantization, on the RoPE-model workloads: the quantize pass with and
+    without it, and the fused-Q attention with and without it."""
+    from workloads import WORKLOADS, make_inputs, norm_weight, rope_tables
+    res = {}
+    for name in names:
+        wl = WORKLOADS[name]
+        inp = make_inputs(wl, "cuda")
+        cos, sin = (torch.from_numpy(t).cuda() for t in rope_tables(max(wl.Sq, wl.Sk), wl.D))
+        wq, wk = (torch.from_numpy(norm_weight(wl.D, s)).cuda() for s in (1, 2))
+        pro = ia.make_prologue(q_norm_weight=wq, k_norm_weight=wk, rope="split_half", cos=cos,
+                               sin=sin)
+        q8, qs, k8, ks = ia.quantize_qk(inp.q, inp.k, prologue=pro)
+        out = torch.empty_like(inp.q)
+        fns = {
+            "quantize_qk_ms": lambda: ia.quantize_qk(inp.q, inp.k),
+            "quantize_qk_prologue_ms": lambda: ia.quantize_qk(inp.q, inp.k, prologue=pro),
+            "quantize_k_prologue_ms": lambda: ia.quantize_qk(None, inp.k, prologue=pro),
+            "attention_ms": lambda: ia.attention(q8, k8, qs, ks, inp.v, v_scale=inp.v_scale,
+                                                 out=out),
+            "fused_q_attention_ms": lambda: ia.attention_quant_q(inp.q, k8, ks, inp.v,
+                                                                 v_scale=inp.v_scale, out=out),
+            "fused_q_prologue_attention_ms": lambda: ia.attention_quant_q(
+                inp.q, k8, ks, inp.v, v_scale=inp.v_scale, out=out, prologue=pro),
+        }
+        ms = {}
+        for key, fn in fns.items():
+            for _ in range(3):
+                fn()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(n):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms[key] = e0.elapsed_time(e1) / n
+        ia.device_status()
+        ms["two_pass_path_ms"] = ms["quantize_qk_prologue_ms"] + ms["attention_ms"]
+        ms["fused_q_path_ms"] = ms["quantize_k_prologue_ms"] + ms["fused_q_prologue_attention_ms"]
+        res[name] = ms
+        del inp, q8, k8, out
+        torch.cuda.empty_cache()
+    return res
+
+
 def time_mask_forms(ia, torch, q8, k8, qs, ks, v, bias, out, n=10):
     """The attn_mask forms of the comfy-kitchen int8_attention issue's table
     (The measurement) on the same 4096 x 33600 x 56 x 128 problem: ms per
@@ -556,6 +603,7 @@ def main():
     others = None if args.no_extra else time_workloads(ia, torch)
     mask_forms = None if args.no_extra else time_mask_forms(ia, torch, q8, k8, qs, ks, v, bias,
                                                             o_full)
+    prologue = None if args.no_extra else time_prologue(ia, torch)
     cpu = None if args.no_cpu_baseline else cpu_baseline()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -591,6 +639,7 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "workloads": others,
         "mask_forms": mask_forms,
+        "prologue": prologue,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
