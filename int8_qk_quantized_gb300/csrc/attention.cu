@@ -219,11 +219,24 @@ __device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity, unsigned l
 // with a SWIZZLE_128B descriptor. 64 threads; each row belongs to one warp.
 // IN_PLACE: `raw` is the second block of `dst` (D == 128), so every lane reads
 // its chunk before any lane of the warp writes the row back.
+// A 16-byte access is served in phases of 8 lanes. For D == 128 the 32 lanes
+// of a warp take 4 rows, and each 8-lane phase takes half of one row and the
+// other half of the next: its int8 reads then cover all 32 banks once, and its
+// fp16 writes land in 8 distinct 16-byte slots of the swizzle (a phase holding
+// one whole row would write both 64-column blocks to the same slots).
 template <int D, bool IN_PLACE>
 __device__ __forceinline__ void widen_tile(const uint8_t* raw, uint8_t* dst, int rows, int ct) {
   constexpr int CPR = D / 16;  // 16-byte int8 chunks per row
   for (int idx = ct; idx < rows * CPR; idx += 64) {
-    const int r = idx / CPR, c = idx % CPR;
+    int r, c;
+    if constexpr (CPR == 8) {
+      const int lane = idx & 31, p = lane >> 3, j = lane & 7, hf = j >> 2;
+      r = ((idx & ~31) >> 3) + 2 * (p >> 1) + hf;
+      c = (((p & 1) ^ hf) << 2) | (j & 3);
+    } else {
+      r = idx / CPR;
+      c = idx % CPR;
+    }
     const uint4 w = *reinterpret_cast<const uint4*>(raw + r * D + c * 16);
     if (IN_PLACE) __syncwarp();
     uint32_t h[8];
