@@ -41,8 +41,8 @@ PAGE_SPLIT_MS = 11.05
 # SHA-256 of the kernel sources it was taken on. A launch's traffic is scaled
 # from it per head, with the key-proportional part scaled by the keys of the
 # launch. When the kernel sources change, the figure no longer applies.
-ATTN_TRAFFIC = {"source_sha256": "bdccd35e454401511172abc1bd0cd79b0f4e1501dbc287d3cf92f8d8ea81067e",
-                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 245229824.0}
+ATTN_TRAFFIC = {"source_sha256": "8d4ae1630ea2ee5e31e25a214e17567d6ebe512891f74dc7189fc7e8a88a6884",
+                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 245155328.0}
 
 
 def attn_source_sha():
