@@ -43,7 +43,7 @@ extern "C" {
 typedef enum ia_status {
   IA_OK = 0,
   IA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad shape or stride */
-  IA_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+  IA_ERR_UNSUPPORTED = 2, /* a valid request the library does not implement */
   IA_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a launch failed */
   IA_ERR_TIMEOUT = 4      /* a bounded device-side wait ran out */
 } ia_status;
