@@ -20,6 +20,7 @@
 #include <cuda_fp16.h>
 
 #include "launch.h"
+#include "ptx.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -64,23 +65,33 @@ __device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float x) {
   lo = __fadd_rn(lo, err);
 }
 
-__device__ __forceinline__ int8_t code_of(float x, float inv) {
-  int c = __float2int_rn(__fmul_rn(x, inv));
-  c = c > 127 ? 127 : (c < -127 ? -127 : c);
-  return static_cast<int8_t>(c);
+// Packed form of two_sum_acc on two columns at once (the same IEEE operations
+// lane by lane, so the same results).
+__device__ __forceinline__ void two_sum_acc2(uint64_t& hi, uint64_t& lo, uint64_t x) {
+  const uint64_t s = fadd2(hi, x);
+  const uint64_t bp = fsub2(s, hi);
+  const uint64_t err = fadd2(fsub2(hi, fsub2(s, bp)), fsub2(x, bp));
+  hi = s;
+  lo = fadd2(lo, err);
 }
 
+// code = round-half-even(fl(x * inv)) for 8 values, stored as 8 int8. Adding
+// 1.5 * 2^23 to the rounded fp32 product leaves no fraction bits, so the IEEE
+// addition rounds it to the nearest integer (ties to even, 1.5 * 2^23 being
+// even) and the low byte of the sum's bit pattern is the code in two's
+// complement. The multiply and the add are the scalar IEEE intrinsics, which
+// are never contracted into a fused multiply-add: a fused form would round
+// x * inv + 1.5 * 2^23 once and break exact ties such as 63.5 (the packed
+// f32x2 forms were contracted). No clamp is needed: |x| <= amax gives
+// x * fl(127 / amax) <= 127 (1 + 2^-24), which rounds to at most 127 + 2^-17
+// and then to the integer 127.
 __device__ __forceinline__ void store_codes(int8_t* dst, const float (&x)[8], float inv) {
-  uint32_t w[2];
+  uint32_t b[8];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint32_t acc = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      acc |= (static_cast<uint32_t>(static_cast<uint8_t>(code_of(x[4 * h + i], inv))) << (8 * i));
-    w[h] = acc;
-  }
-  *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+  for (int i = 0; i < 8; ++i) b[i] = __float_as_uint(__fadd_rn(__fmul_rn(x[i], inv), 12582912.0f));
+  const uint32_t w0 = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+  const uint32_t w1 = __byte_perm(__byte_perm(b[4], b[5], 0x0040), __byte_perm(b[6], b[7], 0x0040), 0x5410);
+  *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
 }
 
 template <int DT>
@@ -189,11 +200,11 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a
   // ---------------------------------------------------------------- mean
   if (a.center) {
     if (CLUSTER_MEAN) {
-      float hi[8], lo[8];
+      uint64_t hi[4], lo[4];  // column pairs (2i, 2i+1)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) hi[i] = lo[i] = 0.f;
+      for (int i = 0; i < 4; ++i) hi[i] = lo[i] = pack2(0.f, 0.f);
       // 8 rows of 16-byte loads in flight per thread, kept packed until used
-      constexpr int U1 = PRO ? 4 : 8;  // the prologue needs registers of its own
+      constexpr int U1 = PRO ? 4 : 6;  // within 64 registers (the prologue needs its own)
       for (int base = r0; base < r1; base += U1 * RPP) {
         uint4 w[U1];
 #pragma unroll
@@ -212,12 +223,17 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a
             prologue8<D, DT>(v, rr < r1 && row_valid(a.valid, rr), rr, tc, a);
           }
 #pragma unroll
-          for (int i = 0; i < 8; ++i) two_sum_acc(hi[i], lo[i], v[i]);
+          for (int i = 0; i < 4; ++i) two_sum_acc2(hi[i], lo[i], pack2(v[2 * i], v[2 * i + 1]));
         }
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        s_red[tr][tc * 8 + i] = static_cast<double>(hi[i]) + static_cast<double>(lo[i]);
+      for (int i = 0; i < 4; ++i) {
+        float h0, h1, l0, l1;
+        unpack2(hi[i], h0, h1);
+        unpack2(lo[i], l0, l1);
+        s_red[tr][tc * 8 + 2 * i] = static_cast<double>(h0) + static_cast<double>(l0);
+        s_red[tr][tc * 8 + 2 * i + 1] = static_cast<double>(h1) + static_cast<double>(l1);
+      }
       if (tid == 0) {
         int n = a.S;
         if (a.valid) {
@@ -281,12 +297,15 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a
         float v[8];
         unpack8<DT>(w[u], v);
         if constexpr (PRO) prologue8<D, DT>(v, ok[u], rr, tc, a);
+        if (a.center && ok[u]) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            unpack2(fsub2(pack2(v[2 * i], v[2 * i + 1]), pack2(mu[2 * i], mu[2 * i + 1])), v[2 * i],
+                    v[2 * i + 1]);
+        }
         float m = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (a.center && ok[u]) v[i] = __fsub_rn(v[i], mu[i]);
-          m = fmaxf(m, fabsf(v[i]));
-        }
+        for (int i = 0; i < 4; ++i) m = fmax3(m, fabsf(v[2 * i]), fabsf(v[2 * i + 1]));
 #pragma unroll
         for (int off = TPR / 2; off > 0; off >>= 1)
           m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
