@@ -169,3 +169,45 @@ def test_attention_full_size_sampled(name):
     v = None if valid is None else valid[rows]
     assert_out_close(o[:, :, rows], ro, re, valid=v)
     assert_lse_close(lse[:, :, rows], rl)
+
+
+def test_banded_split_step_full_size_sampled():
+    """The benchmark's step at full size: quantize Q and K once, the unmasked
+    core and the two biased skirts as key sub-range views with their LSEs, two
+    exact merges ("int8_attention: masked path costs ~1.8x unmasked, ...",
+    Question 2), against the oracle's single call over all keys on sampled
+    rows."""
+    import int8_qk_quantized_gb300 as ia
+    wl = WORKLOADS["banded"]
+    inp = make_inputs(wl, "cuda")
+    lo, hi = wl.skirt_width, wl.Sk - wl.skirt_width
+    q8, qs, k8, ks = ia.quantize_qk(inp.q, inp.k)
+    parts = []
+    for a, b, bias in ((lo, hi, None), (0, lo, inp.bias[:lo]), (hi, wl.Sk, inp.bias[hi:])):
+        parts.append(ia.attention(q8, k8[:, :, a:b], qs, ks[:, :, a:b], inp.v[:, :, a:b],
+                                  bias=bias, return_lse=True))
+    o, l = ia.merge_lse(*parts[0], *parts[1])
+    o, l = ia.merge_lse(o, l, *parts[2], out=o, lse_out=l)
+    ia.device_status()
+    rows = sample_rows(wl.Sq, 12)
+    ro, rl, re = run_oracle(inp, wl, rows=rows)
+    assert_out_close(to_np(o)[:, :, rows], ro, re)
+    assert_lse_close(to_np(l)[:, :, rows], rl)
+
+
+@pytest.mark.parametrize("name", ["anima4k", "anima9k"])
+def test_fused_q_full_size(name):
+    """The fused Q quantization at the Anima sizes: equal to quantize + attention
+    everywhere, and within the oracle's tolerance on sampled rows."""
+    import int8_qk_quantized_gb300 as ia
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl, "cuda")
+    q8, qs, k8, ks = ia.quantize_qk(inp.q, inp.k)
+    o2, l2 = ia.attention(q8, k8, qs, ks, inp.v, v_scale=inp.v_scale, return_lse=True)
+    o1, l1 = ia.attention_quant_q(inp.q, k8, ks, inp.v, v_scale=inp.v_scale, return_lse=True)
+    ia.device_status()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    rows = sample_rows(wl.Sq, 13, per_tile=1)
+    ro, rl, re = run_oracle(inp, wl, rows=rows)
+    assert_out_close(to_np(o1)[:, :, rows], ro, re)
+    assert_lse_close(to_np(l1)[:, :, rows], rl)
