@@ -557,8 +557,30 @@ def main():
 
     step_ms = time_call(step, n=10)
     step_fused_ms = time_call(step_fused_q, n=10)
-    merge_ms = time_call(lambda: ia.merge_lse(o_l, l_l, o_r, l_r, out=o_full, lse_out=l_full,
-                                              stream=stream))
+    # the merge is short enough that Python launch overhead would dominate: time
+    # 50 calls captured in a CUDA graph
+    def time_graph(fn, n=50, reps=4):
+        fn()
+        torch.cuda.synchronize()
+        gs = torch.cuda.Stream(device=dev)
+        gs.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gs):
+            for _ in range(n):
+                fn(gs)
+        graph.replay()
+        torch.cuda.synchronize()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(gs)
+        for _ in range(reps):
+            graph.replay()
+        g1.record(gs)
+        torch.cuda.synchronize()
+        return g0.elapsed_time(g1) / (n * reps)
+
+    merge_ms = time_graph(lambda st=stream: ia.merge_lse(o_l, l_l, o_r, l_r, out=o_full,
+                                                         lse_out=l_full, stream=st))
     ia.device_status()
 
     # End to end: every step copies its inputs from pinned host memory to the

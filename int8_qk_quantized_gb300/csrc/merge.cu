@@ -51,46 +51,60 @@ __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
   return make_uint4(u[0], u[1], u[2], u[3]);
 }
 
+// Each iteration handles two rows per thread group (this CTA's slot in two
+// consecutive grid strides), so a thread has four 16-byte loads in flight.
 template <int D, int DT>
 __global__ void __launch_bounds__(kThreads) merge_kernel(const MergeArgs a) {
   constexpr int TPR = D / 8;
   constexpr int RPP = kThreads / TPR;
+  constexpr int U = 2;
   const int tc = threadIdx.x % TPR;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * RPP;
   // Uniform trip count per CTA, so the warp barrier below is reached by all lanes.
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPP; base < a.rows; base += stride) {
-    const int64_t r = base + threadIdx.x / TPR;
-    const bool live = r < a.rows;
-    const int64_t rr = live ? r : 0;
-    const float l1 = a.l1[rr];
-    const float l2 = a.l2[rr];
-    const int64_t off = rr * D + tc * 8;
-    const uint4 w1 = *reinterpret_cast<const uint4*>(static_cast<const char*>(a.o1) + off * 2);
-    const uint4 w2 = *reinterpret_cast<const uint4*>(static_cast<const char*>(a.o2) + off * 2);
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPP; base < a.rows; base += U * stride) {
+    int64_t r[U];
+    bool live[U];
+    float l1[U], l2[U];
+    uint4 w1[U], w2[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      r[u] = base + u * stride + threadIdx.x / TPR;
+      live[u] = r[u] < a.rows;
+      const int64_t rr = live[u] ? r[u] : 0;
+      l1[u] = a.l1[rr];
+      l2[u] = a.l2[rr];
+      const int64_t off = rr * D + tc * 8;
+      w1[u] = *reinterpret_cast<const uint4*>(static_cast<const char*>(a.o1) + off * 2);
+      w2[u] = *reinterpret_cast<const uint4*>(static_cast<const char*>(a.o2) + off * 2);
+    }
     // Every lane of a row has read its inputs before any lane writes (outputs may alias).
     __syncwarp();
-    if (!live) continue;
-    const float m = fmaxf(l1, l2);
-    float o[8];
-    float lse;
-    if (m == -INFINITY) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = 0.f;
-      lse = -INFINITY;
-    } else {
-      const float e1 = expf(l1 - m);  // exp(-inf) = 0 for an empty partial
-      const float e2 = expf(l2 - m);
-      const float den = e1 + e2;
-      const float c1 = e1 / den, c2 = e2 / den;
-      float x1[8], x2[8];
-      unpack8<DT>(w1, x1);
-      unpack8<DT>(w2, x2);
+    for (int u = 0; u < U; ++u) {
+      if (!live[u]) continue;
+      const float m = fmaxf(l1[u], l2[u]);
+      float o[8];
+      float lse;
+      if (m == -INFINITY) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = c1 * x1[i] + c2 * x2[i];
-      lse = m + logf(den);
+        for (int i = 0; i < 8; ++i) o[i] = 0.f;
+        lse = -INFINITY;
+      } else {
+        const float e1 = expf(l1[u] - m);  // exp(-inf) = 0 for an empty partial
+        const float e2 = expf(l2[u] - m);
+        const float den = e1 + e2;
+        const float c1 = e1 / den, c2 = e2 / den;
+        float x1[8], x2[8];
+        unpack8<DT>(w1[u], x1);
+        unpack8<DT>(w2[u], x2);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = c1 * x1[i] + c2 * x2[i];
+        lse = m + logf(den);
+      }
+      const int64_t off = r[u] * D + tc * 8;
+      *reinterpret_cast<uint4*>(static_cast<char*>(a.o) + off * 2) = pack8<DT>(o);
+      if (a.l && tc == 0) a.l[r[u]] = lse;
     }
-    *reinterpret_cast<uint4*>(static_cast<char*>(a.o) + off * 2) = pack8<DT>(o);
-    if (a.l && tc == 0) a.l[r] = lse;
   }
 }
 
