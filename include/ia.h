@@ -134,6 +134,7 @@ typedef enum ia_mask_dtype {
  *   q_scale, k_scale  outputs, fp32 contiguous [B,H,Sq] / [B,H,Sk] per token,
  *               [B,H,ceil(S/64)] per block.
  *   k_mean_out  optional fp32 [B,H,D] output of the mean that was used.
+ * Limits (IA_ERR_UNSUPPORTED): H <= 65535 and B <= 65535.
  */
 IA_API ia_status ia_quantize_qk(const void* q, const void* k, ia_dtype in_dtype, int B, int H,
                                 int Sq, int Sk, int D, const int64_t q_strides[3],
@@ -245,6 +246,9 @@ IA_API void ia_attn_params_init(ia_attn_params* p, int B, int H, int Sq, int Sk,
  * multiple of 64), v + off*v_strides[2], bias + off, and Sk = len.
  * Alignment: q_i8, k_i8, v and out 16-byte aligned with 16-byte-multiple row,
  * head and batch strides (in bytes).
+ * Limits (IA_ERR_UNSUPPORTED): H <= 65535, B * max(kv_splits, 1) <= 65535,
+ * Sk <= 65535 * 64; with a block mask the CTA's key-tile list (2 bytes per
+ * 64-key tile) must fit in shared memory.
  */
 IA_API ia_status ia_attention_fwd(const int8_t* q_i8, const int8_t* k_i8, const float* q_scale,
                                   const float* k_scale, const void* v, const float* bias_or_null,

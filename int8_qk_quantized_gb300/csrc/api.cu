@@ -156,6 +156,9 @@ ia_status attention(const void* q, bool q_raw, const int8_t* k_i8, const float* 
     return fail(IA_ERR_INVALID_ARG, "kv_valid requires Sk to be a multiple of 64 (Sk=%d)", p->Sk);
   if (p->Sk > 65535 * 64)
     return fail(IA_ERR_UNSUPPORTED, "Sk too large (%d)", p->Sk);
+  // grid: (query tiles, H, B * kv_splits); the last two are at most 65535
+  if (p->H > 65535 || static_cast<int64_t>(p->B) * (p->kv_splits > 1 ? p->kv_splits : 1) > 65535)
+    return fail(IA_ERR_UNSUPPORTED, "H (%d) and B * kv_splits must be at most 65535", p->H);
   if (p->kv_splits < 0 || p->kv_splits > ia::kMaxParts)
     return fail(IA_ERR_INVALID_ARG, "kv_splits must be in [0, %d] (got %d)", ia::kMaxParts, p->kv_splits);
   if (p->kv_splits > 1) {
@@ -254,6 +257,8 @@ ia_status quantize(const void* q, const void* k, ia_dtype in_dtype, int B, int H
   }
   if (kv_valid != nullptr && (Sk % 64) != 0)
     return fail(IA_ERR_INVALID_ARG, "kv_valid requires Sk to be a multiple of 64 (Sk=%d)", Sk);
+  if (H > 65535 || B > 65535)  // grid (chunks, H, B)
+    return fail(IA_ERR_UNSUPPORTED, "H (%d) and B (%d) must be at most 65535", H, B);
   ia_status ps = check_prologue(pro, D, q != nullptr ? Sq : 0, k != nullptr ? Sk : 0, true);
   if (ps != IA_OK) return ps;
   int sms = 0;

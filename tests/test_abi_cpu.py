@@ -209,3 +209,19 @@ def test_prologue_argument_errors(lib):
     assert lib.ia_attention_fwd(fake, fake, fake, fake, fake, None, None, fake, None,
                                 ctypes.byref(p), None) == 1
     assert b"quant_q" in lib.ia_last_error_message()
+
+
+def test_grid_limits_reported(lib):
+    fake = ctypes.c_void_p(0x1000)
+    p = _params(lib)
+    p.H = 70000
+    assert lib.ia_attention_fwd(fake, fake, fake, fake, fake, None, None, fake, None,
+                                ctypes.byref(p), None) == 2
+    p = _params(lib)
+    p.B, p.kv_splits = 20000, 4
+    p.workspace, p.workspace_bytes = 0x1000, 1 << 62
+    assert lib.ia_attention_fwd(fake, fake, fake, fake, fake, None, None, fake, None,
+                                ctypes.byref(p), None) == 2
+    st = (ctypes.c_int64 * 3)(128, 128, 128)
+    assert lib.ia_quantize_qk(fake, None, 0, 1, 70000, 8, 8, 128, st, None, 0, 0, None, None,
+                              fake, None, fake, None, None, None) == 2
