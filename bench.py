@@ -41,7 +41,7 @@ PAGE_SPLIT_MS = 11.05
 # SHA-256 of the kernel sources it was taken on. A launch's traffic is scaled
 # from it per head, with the key-proportional part scaled by the keys of the
 # launch. When the kernel sources change, the figure no longer applies.
-ATTN_TRAFFIC = {"source_sha256": "8d4ae1630ea2ee5e31e25a214e17567d6ebe512891f74dc7189fc7e8a88a6884",
+ATTN_TRAFFIC = {"source_sha256": "eb1d9bcfb24828b165562f70286df0fefe20226ba95efe2736993a00f472a8dc",
                 "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 245155328.0}
 
 
@@ -572,10 +572,11 @@ def main():
         torch.cuda.synchronize()
         g0 = torch.cuda.Event(enable_timing=True)
         g1 = torch.cuda.Event(enable_timing=True)
-        g0.record(gs)
+        cur = torch.cuda.current_stream()  # replay() launches on the current stream
+        g0.record(cur)
         for _ in range(reps):
             graph.replay()
-        g1.record(gs)
+        g1.record(cur)
         torch.cuda.synchronize()
         return g0.elapsed_time(g1) / (n * reps)
 
