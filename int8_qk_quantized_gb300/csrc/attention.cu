@@ -214,43 +214,59 @@ __device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity, unsigned l
   }
 }
 
-// int8 tile [rows x D] row-major -> fp16 [rows x D] in 128-byte-swizzled
-// K-major blocks of 64 columns (block stride rows*128 bytes), as tcgen05 reads
+// int8 tile [ROWS x D] row-major -> fp16 [ROWS x D] in 128-byte-swizzled
+// K-major blocks of 64 columns (block stride ROWS*128 bytes), as tcgen05 reads
 // with a SWIZZLE_128B descriptor. 64 threads; each row belongs to one warp.
 // IN_PLACE: `raw` is the second block of `dst` (D == 128), so every lane reads
-// its chunk before any lane of the warp writes the row back.
+// its chunks before any lane of the warp writes a row back.
 // A 16-byte access is served in phases of 8 lanes. For D == 128 the 32 lanes
 // of a warp take 4 rows, and each 8-lane phase takes half of one row and the
 // other half of the next: its int8 reads then cover all 32 banks once, and its
 // fp16 writes land in 8 distinct 16-byte slots of the swizzle (a phase holding
 // one whole row would write both 64-column blocks to the same slots).
-template <int D, bool IN_PLACE>
-__device__ __forceinline__ void widen_tile(const uint8_t* raw, uint8_t* dst, int rows, int ct) {
-  constexpr int CPR = D / 16;  // 16-byte int8 chunks per row
-  for (int idx = ct; idx < rows * CPR; idx += 64) {
-    int r, c;
-    if constexpr (CPR == 8) {
-      const int lane = idx & 31, p = lane >> 3, j = lane & 7, hf = j >> 2;
-      r = ((idx & ~31) >> 3) + 2 * (p >> 1) + hf;
-      c = (((p & 1) ^ hf) << 2) | (j & 3);
-    } else {
-      r = idx / CPR;
-      c = idx % CPR;
+template <int D, int ROWS, bool IN_PLACE>
+__device__ __forceinline__ void widen_tile(const uint8_t* raw, uint8_t* dst, int ct) {
+  constexpr int CPR = D / 16;              // 16-byte int8 chunks per row
+  constexpr int NI = ROWS * CPR / 64;      // chunks per thread
+  // Chunks loaded before any is stored. In place, all of them: a warp owns
+  // whole rows and a row's fp16 output overwrites only its own int8 row, so one
+  // warp barrier after the loads suffices (instead of a load-barrier-store
+  // round trip per chunk). From a staging buffer, one at a time; the loop is
+  // kept rolled, as unrolling it cost the masked softmax registers.
+  constexpr int NB = IN_PLACE ? NI : 1;
+  static_assert(ROWS * CPR % 64 == 0 && NI % NB == 0, "widen layout");
+#pragma unroll 1
+  for (int i0 = 0; i0 < NI; i0 += NB) {
+    uint4 w[NB];
+    int rr[NB], cc[NB];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const int idx = ct + 64 * (i0 + j);
+      if constexpr (CPR == 8) {
+        const int lane = idx & 31, p = lane >> 3, q = lane & 7, hf = q >> 2;
+        rr[j] = ((idx & ~31) >> 3) + 2 * (p >> 1) + hf;
+        cc[j] = (((p & 1) ^ hf) << 2) | (q & 3);
+      } else {
+        rr[j] = idx / CPR;
+        cc[j] = idx % CPR;
+      }
+      w[j] = *reinterpret_cast<const uint4*>(raw + rr[j] * D + cc[j] * 16);
     }
-    const uint4 w = *reinterpret_cast<const uint4*>(raw + r * D + c * 16);
     if (IN_PLACE) __syncwarp();
-    uint32_t h[8];
-    i8x4_to_f16x4(w.x, h[0], h[1]);
-    i8x4_to_f16x4(w.y, h[2], h[3]);
-    i8x4_to_f16x4(w.z, h[4], h[5]);
-    i8x4_to_f16x4(w.w, h[6], h[7]);
-    const int blk = c >> 2;          // 64-column block
-    const int k0 = (c & 3) * 2;      // first 16-byte chunk within the 128-byte row
-    uint8_t* rowp = dst + blk * (rows * 128) + r * 128;
-    const int sw = r & 7;
-    *reinterpret_cast<uint4*>(rowp + ((k0 ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(rowp + (((k0 + 1) ^ sw) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
-    if (IN_PLACE) __syncwarp();
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      uint32_t h[8];
+      i8x4_to_f16x4(w[j].x, h[0], h[1]);
+      i8x4_to_f16x4(w[j].y, h[2], h[3]);
+      i8x4_to_f16x4(w[j].z, h[4], h[5]);
+      i8x4_to_f16x4(w[j].w, h[6], h[7]);
+      const int blk = cc[j] >> 2;          // 64-column block
+      const int k0 = (cc[j] & 3) * 2;      // first 16-byte chunk within the 128-byte row
+      uint8_t* rowp = dst + blk * (ROWS * 128) + rr[j] * 128;
+      const int sw = rr[j] & 7;
+      *reinterpret_cast<uint4*>(rowp + ((k0 ^ sw) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(rowp + (((k0 + 1) ^ sw) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+    }
   }
 }
 
@@ -727,7 +743,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     bool ok = QRAW ? true : wait_bar(bar(L::B_QFULL), 0, ctl, kErrConverter);
     if (ok && !QRAW) {
       for (int s = 0; s < QS; ++s)
-        widen_tile<D, false>(smem + L::OFF_V + s * L::QR, smem + L::OFF_QH + s * L::QH, kM, ct);
+        widen_tile<D, kM, false>(smem + L::OFF_V + s * L::QR, smem + L::OFF_QH + s * L::QH, ct);
       fence_proxy_async_smem();
       mbar_arrive(bar(L::B_QCONV));
     }
@@ -765,12 +781,12 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       if (ct == 0) IA_TRACE_POINT(12, it);
       if constexpr (L::INPLACE) {
         uint8_t* kh = smem + L::OFF_KH + kst * L::KH;
-        widen_tile<D, true>(kh + BN * 128, kh, BN, ct);
+        widen_tile<D, BN, true>(kh + BN * 128, kh, ct);
       } else {
         const int rs = it % L::NRS;
         if (it >= L::NKS) ok = wait_bar(bar(L::B_KCE + kst), ((it / L::NKS) - 1) & 1, ctl, kErrConverter);
         if (!ok) break;
-        widen_tile<D, false>(smem + L::OFF_KR + rs * L::KR, smem + L::OFF_KH + kst * L::KH, BN, ct);
+        widen_tile<D, BN, false>(smem + L::OFF_KR + rs * L::KR, smem + L::OFF_KH + kst * L::KH, ct);
         mbar_arrive(bar(L::B_KRE + rs));
       }
       if (ct == 0) IA_TRACE_POINT(13, it);
