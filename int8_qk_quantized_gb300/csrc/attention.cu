@@ -29,7 +29,7 @@
 //    shared memory and read by all query rows (the [1,1,1,K] broadcast).
 //  * Block-sparse: one 128-row stage (two 64-row query tiles) walks the
 //    union of its tiles' kept key tiles (64 keys each); rows whose own query
-//    tile dropped a key tile see -inf there.
+//    tile dropped a key tile write P = 0 for it without reading S.
 //  * Every mbarrier wait is bounded. When one runs out the kernel records it
 //    in a device status word, stops issuing work, drains what is in flight,
 //    frees TMEM and returns.
@@ -817,7 +817,6 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
           const uint32_t k0 = mrow0[kt] ? 1u : 0u;
           const uint32_t k1 = (mrow1 != nullptr && mrow1[kt]) ? 1u : 0u;
           f |= (k0 << 1) | (k1 << 2);
-          if (!(k0 && k1)) f |= 1u;
         } else {
           f |= 6u;
         }
@@ -891,101 +890,113 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       const bool fast = (flags & 1u) == 0;
       const bool keep = SPARSE ? ((flags >> (1 + half)) & 1u) != 0 : true;
       const uint64_t cq2 = pack2(cq, cq);
-      // The whole S row of this thread in one TMEM round trip.
-      uint32_t sv[BN];
-      if constexpr (BN == 128) {
-        tmem_ld128(tS, sv);
-      } else {
-        tmem_ld64(tS, sv);
-      }
-      tmem_wait_ld(sv);
-      if (r == 0) IA_TRACE_POINT(2 + 4 * s, it);
-      // u = acc * k_scale (fast tiles) or t = u * cq + bias*log2e / -inf
-      // (masked tiles), in place, and the row maximum.
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (fast) {
+      if (SPARSE && !keep) {
+        // This row's query tile dropped the key tile: P = 0, the row's maximum
+        // and sum stay as they are, and S need not be read.
+        uint32_t z[BN / 2];
 #pragma unroll
-        for (int c = 0; c < BN; c += 8) {
-          const float4 ka = *reinterpret_cast<const float4*>(ksm + c);
-          const float4 kb = *reinterpret_cast<const float4*>(ksm + c + 4);
-          float f[8];
-          unpack2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(ka.x, ka.y)), f[0], f[1]);
-          unpack2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(ka.z, ka.w)), f[2], f[3]);
-          unpack2(fmul2(pack2(__uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5])), pack2(kb.x, kb.y)), f[4], f[5]);
-          unpack2(fmul2(pack2(__uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7])), pack2(kb.z, kb.w)), f[6], f[7]);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) mx[q] = fmax3(mx[q], f[2 * q], f[2 * q + 1]);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) sv[c + q] = __float_as_uint(f[q]);
+        for (int e = 0; e < BN / 2; ++e) z[e] = 0u;
+        if constexpr (BN == 128) {
+          tmem_st64(tS, z);
+        } else {
+          tmem_st32(tS, z);
         }
       } else {
-#pragma unroll
-        for (int c = 0; c < BN; c += 4) {
-          const float4 k4 = *reinterpret_cast<const float4*>(ksm + c);
-          const float4 b4 = *reinterpret_cast<const float4*>(b2m + c);
-          float f[4];
-          unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(k4.x, k4.y)),
-                        cq2, pack2(b4.x, b4.y)), f[0], f[1]);
-          unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(k4.z, k4.w)),
-                        cq2, pack2(b4.z, b4.w)), f[2], f[3]);
-          if constexpr (ROWMASK) {
-            float mk[4];
-            row_mask4(smem + L::OFF_MK + ss * L::MB, r, c, a.rm_dtype, mk);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) f[e] = fmaf(mk[e], kLog2e, f[e]);
+        // The whole S row of this thread in one TMEM round trip.
+        uint32_t sv[BN];
+        if constexpr (BN == 128) {
+          tmem_ld128(tS, sv);
+        } else {
+          tmem_ld64(tS, sv);
+        }
+        tmem_wait_ld(sv);
+        if (r == 0) IA_TRACE_POINT(2 + 4 * s, it);
+        // u = acc * k_scale (fast tiles) or t = u * cq + bias*log2e / -inf
+        // (masked tiles), in place, and the row maximum.
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (fast) {
+  #pragma unroll
+          for (int c = 0; c < BN; c += 8) {
+            const float4 ka = *reinterpret_cast<const float4*>(ksm + c);
+            const float4 kb = *reinterpret_cast<const float4*>(ksm + c + 4);
+            float f[8];
+            unpack2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(ka.x, ka.y)), f[0], f[1]);
+            unpack2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(ka.z, ka.w)), f[2], f[3]);
+            unpack2(fmul2(pack2(__uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5])), pack2(kb.x, kb.y)), f[4], f[5]);
+            unpack2(fmul2(pack2(__uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7])), pack2(kb.z, kb.w)), f[6], f[7]);
+  #pragma unroll
+            for (int q = 0; q < 4; ++q) mx[q] = fmax3(mx[q], f[2 * q], f[2 * q + 1]);
+  #pragma unroll
+            for (int q = 0; q < 8; ++q) sv[c + q] = __float_as_uint(f[q]);
           }
-          if (!keep) f[0] = f[1] = f[2] = f[3] = -INFINITY;
-          const int q = (c >> 2) & 3;
-          mx[q] = fmax3(mx[q], fmaxf(f[0], f[1]), fmaxf(f[2], f[3]));
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sv[c + e] = __float_as_uint(f[e]);
-        }
-      }
-      const float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      const float tmax = fast ? cq * rmax : rmax;
-      const float m_new = fmaxf(m, tmax);
-      const bool need = m_new > m + kRescaleLog2;
-      if (__any_sync(0xffffffffu, need)) {
-        const float alpha = need ? ex2(m - m_new) : 1.f;
-        if (it > 0) {
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t rr[32];
-            tmem_ld32(tO + c0, rr);
-            tmem_wait_ld(rr);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-            tmem_st32(tO + c0, rr);
+        } else {
+  #pragma unroll
+          for (int c = 0; c < BN; c += 4) {
+            const float4 k4 = *reinterpret_cast<const float4*>(ksm + c);
+            const float4 b4 = *reinterpret_cast<const float4*>(b2m + c);
+            float f[4];
+            unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(k4.x, k4.y)),
+                          cq2, pack2(b4.x, b4.y)), f[0], f[1]);
+            unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(k4.z, k4.w)),
+                          cq2, pack2(b4.z, b4.w)), f[2], f[3]);
+            if constexpr (ROWMASK) {
+              float mk[4];
+              row_mask4(smem + L::OFF_MK + ss * L::MB, r, c, a.rm_dtype, mk);
+  #pragma unroll
+              for (int e = 0; e < 4; ++e) f[e] = fmaf(mk[e], kLog2e, f[e]);
+            }
+            const int q = (c >> 2) & 3;
+            mx[q] = fmax3(mx[q], fmaxf(f[0], f[1]), fmaxf(f[2], f[3]));
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) sv[c + e] = __float_as_uint(f[e]);
           }
         }
-        l *= alpha;
-        if (need) m = m_new;
+        const float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        const float tmax = fast ? cq * rmax : rmax;
+        const float m_new = fmaxf(m, tmax);
+        const bool need = m_new > m + kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ex2(m - m_new) : 1.f;
+          if (it > 0) {
+  #pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t rr[32];
+              tmem_ld32(tO + c0, rr);
+              tmem_wait_ld(rr);
+  #pragma unroll
+              for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+              tmem_st32(tO + c0, rr);
+            }
+          }
+          l *= alpha;
+          if (need) m = m_new;
+        }
+        const float mref = (m == -INFINITY) ? 0.f : m;
+        const float k1 = fast ? cq : 1.f;
+        const uint64_t k1v = pack2(k1, k1);
+        const uint64_t nm = pack2(-mref, -mref);
+        uint64_t lsum[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
+        // p = 2^(t - m) with the row sum in fp32; P packed to 16 bits in place
+        // (pair i lands in word i, whose value is already consumed) and written
+        // to the first BN/2 columns of S in one store.
+  #pragma unroll
+        for (int e = 0; e < BN / 2; ++e) {
+          float t0, t1;
+          unpack2(ffma2(pack2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), k1v, nm), t0, t1);
+          const float p0 = ex2(t0), p1 = ex2(t1);
+          lsum[e & 1] = fadd2(lsum[e & 1], pack2(p0, p1));
+          sv[e] = VBF16 ? cvt_bf16x2(p0, p1) : cvt_f16x2(p0, p1);
+        }
+        if constexpr (BN == 128) {
+          tmem_st64(tS, *reinterpret_cast<uint32_t(*)[64]>(sv));
+        } else {
+          tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(sv));
+        }
+        float la, lb, lc, ld;
+        unpack2(lsum[0], la, lb);
+        unpack2(lsum[1], lc, ld);
+        l += (la + lb) + (lc + ld);
       }
-      const float mref = (m == -INFINITY) ? 0.f : m;
-      const float k1 = fast ? cq : 1.f;
-      const uint64_t k1v = pack2(k1, k1);
-      const uint64_t nm = pack2(-mref, -mref);
-      uint64_t lsum[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
-      // p = 2^(t - m) with the row sum in fp32; P packed to 16 bits in place
-      // (pair i lands in word i, whose value is already consumed) and written
-      // to the first BN/2 columns of S in one store.
-#pragma unroll
-      for (int e = 0; e < BN / 2; ++e) {
-        float t0, t1;
-        unpack2(ffma2(pack2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), k1v, nm), t0, t1);
-        const float p0 = ex2(t0), p1 = ex2(t1);
-        lsum[e & 1] = fadd2(lsum[e & 1], pack2(p0, p1));
-        sv[e] = VBF16 ? cvt_bf16x2(p0, p1) : cvt_f16x2(p0, p1);
-      }
-      if constexpr (BN == 128) {
-        tmem_st64(tS, *reinterpret_cast<uint32_t(*)[64]>(sv));
-      } else {
-        tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(sv));
-      }
-      float la, lb, lc, ld;
-      unpack2(lsum[0], la, lb);
-      unpack2(lsum[1], lc, ld);
-      l += (la + lb) + (lc + ld);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(L::B_PF + s));

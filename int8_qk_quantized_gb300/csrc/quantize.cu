@@ -56,17 +56,8 @@ __device__ __forceinline__ bool row_valid(const int32_t* valid, int r) {
   return valid == nullptr || (r % kTile) < __ldg(valid + r / kTile);
 }
 
-// Error-free accumulation: (hi, lo) += x with hi + lo exact when it fits.
-__device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float x) {
-  const float s = __fadd_rn(hi, x);
-  const float bp = __fsub_rn(s, hi);
-  const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(x, bp));
-  hi = s;
-  lo = __fadd_rn(lo, err);
-}
-
-// Packed form of two_sum_acc on two columns at once (the same IEEE operations
-// lane by lane, so the same results).
+// Error-free accumulation of two columns at once: (hi, lo) += x lane by lane,
+// with hi + lo exact whenever it fits (Knuth's two-sum in packed f32x2 form).
 __device__ __forceinline__ void two_sum_acc2(uint64_t& hi, uint64_t& lo, uint64_t x) {
   const uint64_t s = fadd2(hi, x);
   const uint64_t bp = fsub2(s, hi);
