@@ -799,20 +799,30 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       float* ksm = reinterpret_cast<float*>(smem + L::OFF_SC + ss * L::SC);
       float* b2m = ksm + BN;
       uint32_t* flg = reinterpret_cast<uint32_t*>(b2m + BN);
+      bool nonzero = false;  // a valid key of this thread has a nonzero offset
 #pragma unroll
       for (int e = 0; e < KPT; ++e) {
         if (ct + 64 * e < BN) {
-          ksm[ct + 64 * e] = kv[e];
-          b2m[ct + 64 * e] =
+          const float off =
               kval[e] ? (brow ? key_bias_value(braw[e], a.bias_dtype) * kLog2e : 0.f) : -INFINITY;
+          ksm[ct + 64 * e] = kv[e];
+          b2m[ct + 64 * e] = off;
+          nonzero |= kval[e] && off != 0.f;
         }
+      }
+      // Each converter warp records whether its keys carry any offset: a tile
+      // whose offsets are all zero (e.g. the core of a window's bias) keeps the
+      // softmax's fast path. Separate words, so the warps need no barrier.
+      {
+        const bool any_nz = __any_sync(__activemask(), nonzero);
+        if ((ct & 31) == 0) flg[1 + (ct >> 5)] = any_nz ? 1u : 0u;
       }
       if (ct == 0) {
         bool partial = kt * BN + BN > a.Sk;
         if (a.kv_valid)
           for (int t = (kt * BN) >> 6; t < ((kt + 1) * BN) >> 6 && t * 64 < a.Sk; ++t)
             partial |= __ldg(a.kv_valid + t) < 64;
-        uint32_t f = (a.bias != nullptr || ROWMASK || partial) ? 1u : 0u;
+        uint32_t f = (ROWMASK || partial) ? 1u : 0u;
         if (SPARSE) {
           const uint32_t k0 = mrow0[kt] ? 1u : 0u;
           const uint32_t k1 = (mrow1 != nullptr && mrow1[kt]) ? 1u : 0u;
@@ -886,8 +896,11 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       if (r == 0) IA_TRACE_POINT(1 + 4 * s, it);
       const float* ksm = reinterpret_cast<const float*>(smem + L::OFF_SC + ss * L::SC);
       const float* b2m = ksm + BN;
-      const uint32_t flags = *reinterpret_cast<const volatile uint32_t*>(b2m + BN);
-      const bool fast = (flags & 1u) == 0;
+      const volatile uint32_t* fw = reinterpret_cast<const volatile uint32_t*>(b2m + BN);
+      const uint32_t flags = fw[0];
+      // the masked path is needed for a partial tile, a per-row mask or a
+      // nonzero per-key offset in either converter warp's keys
+      const bool fast = ((flags & 1u) | fw[1] | fw[2]) == 0;
       const bool keep = SPARSE ? ((flags >> (1 + half)) & 1u) != 0 : true;
       const uint64_t cq2 = pack2(cq, cq);
       if (SPARSE && !keep) {
