@@ -41,8 +41,8 @@ PAGE_SPLIT_MS = 11.05
 # SHA-256 of the kernel sources it was taken on. A launch's traffic is scaled
 # from it per head, with the key-proportional part scaled by the keys of the
 # launch. When the kernel sources change, the figure no longer applies.
-ATTN_TRAFFIC = {"source_sha256": "7389a414f2b97272bd67a632984b015acfc375cd115f894776bd9447d60d8079",
-                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 245272576.0}
+ATTN_TRAFFIC = {"source_sha256": "befbf57134c4fd691c9c668ab56b7fd06b19f1b2f3bfe93e0d16adaeae754249",
+                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 245016832.0}
 
 
 def attn_source_sha():
