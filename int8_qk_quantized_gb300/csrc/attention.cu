@@ -120,7 +120,7 @@ struct Params {
   int qp_pos0;
 };
 
-template <int D, int QS, int BN, bool SPARSE, bool ROWMASK = false>
+template <int D, int QS, int BN, bool SPARSE, bool ROWMASK = false, bool PAIR = false>
 struct Layout {
   // Block-sparse, D == 128: the int8 K tile lands (by TMA) in the second
   // 64-column block of its fp16 K buffer and is widened in place, which keeps
@@ -128,11 +128,18 @@ struct Layout {
   static constexpr bool INPLACE = SPARSE && D == 128;
   static constexpr int NKS = 2, NVS = 2, NSC = 2;
   static constexpr int NRS = INPLACE ? 0 : 2;
-  static constexpr int QH = kM * D * 2;   // fp16 Q stage
-  static constexpr int KH = BN * D * 2;   // fp16 K tile
-  static constexpr int VB = BN * D * 2;   // 16-bit V tile
-  static constexpr int KR = BN * D;       // int8 K tile
-  static constexpr int QR = kM * D;       // int8 Q stage
+  // A CTA pair (PAIR) holds half of each key tile's K rows and half of V's
+  // columns per CTA; the 256-row MMA reads the other halves from the peer.
+  static constexpr int KROWS = PAIR ? BN / 2 : BN;  // keys of a K tile held here
+  static constexpr int VCOLS = PAIR ? D / 2 : D;    // V columns held here
+  static constexpr int QH = kM * D * 2;      // fp16 Q stage
+  static constexpr int KH = KROWS * D * 2;   // fp16 K tile
+  static constexpr int VB = BN * VCOLS * 2;  // 16-bit V tile
+  static constexpr int KR = KROWS * D;       // int8 K tile
+  static constexpr int QR = kM * D;          // int8 Q stage
+  // Q staging: the V buffers, or (PAIR, whose V buffers are too small) a
+  // region of its own sized for 16-bit rows.
+  static constexpr int QST = PAIR ? QS * kM * D * 2 : 0;
   static constexpr int SC = BN * 8 + 16;  // k scales, bias*log2e, flags
   // Per-row mask tile (ROWMASK): kM rows x BN keys as TMA boxes of 128-byte
   // rows with the 128-byte swizzle; 32 fp32, 64 16-bit or 128 bool keys per box.
@@ -141,7 +148,9 @@ struct Layout {
   static constexpr int OFF_KH = OFF_QH + QS * QH;
   static constexpr int OFF_V = OFF_KH + NKS * KH;
   static constexpr int OFF_KR = OFF_V + NVS * VB;
-  static constexpr int OFF_MK = OFF_KR + NRS * KR;
+  static constexpr int OFF_QST = OFF_KR + NRS * KR;
+  static constexpr int OFF_QIN = PAIR ? OFF_QST : OFF_V;  // where Q lands before conversion
+  static constexpr int OFF_MK = OFF_QST + QST;
   static constexpr int OFF_SC = OFF_MK + NSC * MB;
   static constexpr int OFF_VS = OFF_SC + NSC * SC;
   static constexpr int OFF_BAR = (OFF_VS + D * 4 + 7) / 8 * 8;
@@ -160,13 +169,15 @@ struct Layout {
                                    : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
   static constexpr int NWARPS = 4 * QS + 4;
   static constexpr int W_PROD = 4 * QS, W_MMA = 4 * QS + 1, W_CONV = 4 * QS + 2;
-  static_assert(QS * QR <= VB, "int8 Q is staged in the first V buffer");
-  static_assert(QS * QR * 2 <= NVS * VB, "16-bit Q is staged in the V buffers");
+  static_assert(PAIR || QS * QR <= VB, "int8 Q is staged in the first V buffer");
+  static_assert(PAIR || QS * QR * 2 <= NVS * VB, "16-bit Q is staged in the V buffers");
   static_assert(TMEM_NEED <= 512, "TMEM budget");
   static_assert(OFF_QH % 1024 == 0 && OFF_KH % 1024 == 0 && OFF_V % 1024 == 0 &&
-                    OFF_MK % 1024 == 0, "swizzle align");
+                    OFF_MK % 1024 == 0 && OFF_QST % 1024 == 0, "swizzle align");
   static_assert(!ROWMASK || (QS == 1 && BN == 64 && !SPARSE), "row-mask shape");
   static_assert(!INPLACE || KR == BN * 128, "the int8 tile fills one 64-column fp16 block");
+  // the pair's V half is one 64-column swizzle block; dense tiles only
+  static_assert(!PAIR || (D == 128 && QS == 2 && BN == 128 && !SPARSE && !ROWMASK), "pair shape");
 };
 
 struct Ctl {
@@ -177,11 +188,13 @@ struct Ctl {
 // Bounded wait on an mbarrier phase. Returns false when the wait ran out here
 // (the status word and the CTA's abort flag are set) or another thread of
 // the CTA has already aborted.
+// `cluster`: the phase includes arrivals from the peer CTA of a pair, whose
+// writes this thread then reads (acquire at cluster scope).
 __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, const Ctl& c,
-                                           unsigned code) {
+                                           unsigned code, bool cluster) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if (*c.abort) return false;
     if ((n & 15u) == 0 && *reinterpret_cast<volatile unsigned*>(&g_attn_status) != 0u) {
       *c.abort = 1;  // another CTA already timed out: stop waiting as well
@@ -198,7 +211,12 @@ __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, const 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c,
                                          unsigned code) {
   if (mbar_try_wait(bar, parity)) return true;
-  return wait_bar_slow(bar, parity, c, code);
+  return wait_bar_slow(bar, parity, c, code, false);
+}
+__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, const Ctl& c,
+                                                 unsigned code) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  return wait_bar_slow(bar, parity, c, code, true);
 }
 
 // Bounded wait that ignores the abort flag: used to let copies and MMAs that
@@ -485,13 +503,17 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-template <int D, int QS, int BN, bool SPARSE, bool VBF16, bool QRAW, bool ROWMASK>
+// PAIR: the grid's CTAs run as clusters of two along x. Each CTA owns its
+// QS x 128 query rows; the pair walks the same key tiles, each CTA loading
+// and widening half of every K tile and half of V's columns, and the
+// even-ranked CTA issues 256-row MMAs over both (cta_group::2).
+template <int D, int QS, int BN, bool SPARSE, bool VBF16, bool QRAW, bool ROWMASK, bool PAIR>
 __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_m, const Params a) {
-  using L = Layout<D, QS, BN, SPARSE, ROWMASK>;
+  using L = Layout<D, QS, BN, SPARSE, ROWMASK, PAIR>;
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x;
@@ -510,18 +532,28 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   const Ctl ctl{abort_flag, a.timeout_ns};
   auto bar = [&](int i) -> uint32_t { return smem_u32(bars + i); };
+  // Pair roles: the leader (even rank) issues the MMAs; the peer's threads
+  // arrive on the leader's barriers through these addresses.
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = crank == 0u;
+  auto lbar = [&](int i) -> uint32_t { return mapa_shared(bar(i), crank & ~1u); };
+  // arrivals the leader's MMA barriers take from the peer (one per peer warp
+  // for K and P; one forwarded arrival for Q and V)
+  const uint32_t peer_k = (PAIR && leader) ? 2u : 0u;
+  const uint32_t peer_p = (PAIR && leader) ? 4u : 0u;
+  const uint32_t peer_f = (PAIR && leader) ? 1u : 0u;
 
   if (tid == 0) {
     mbar_init(bar(L::B_QFULL), 1);
-    mbar_init(bar(L::B_QCONV), QRAW ? QS * kM : 64);
+    mbar_init(bar(L::B_QCONV), (QRAW ? QS * kM : 64) + peer_f);
     for (int i = 0; i < L::NKS; ++i) {
       mbar_init(bar(L::B_KRF + i), 1);
-      mbar_init(bar(L::B_KCF + i), 64);
+      mbar_init(bar(L::B_KCF + i), 64 + peer_k);
       mbar_init(bar(L::B_KCE + i), 1);
     }
     for (int i = 0; i < L::NRS; ++i) mbar_init(bar(L::B_KRE + i), 64);
     for (int i = 0; i < L::NVS; ++i) {
-      mbar_init(bar(L::B_VF + i), 1);
+      mbar_init(bar(L::B_VF + i), 1 + peer_f);
       mbar_init(bar(L::B_VE + i), 1);
     }
     for (int i = 0; i < L::NSC; ++i) {
@@ -530,7 +562,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     }
     for (int s = 0; s < QS; ++s) {
       mbar_init(bar(L::B_SF + s), 1);
-      mbar_init(bar(L::B_PF + s), kM);
+      mbar_init(bar(L::B_PF + s), kM + peer_p);
       mbar_init(bar(L::B_OF + s), 1);
     }
     for (int i = 0; i < L::NSC; ++i) mbar_init(bar(L::B_MF + i), 1);
@@ -540,8 +572,13 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     fence_mbar_init();
   }
   if (warp == L::W_MMA) {
-    tmem_alloc(smem_u32(misc), L::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(misc), L::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(misc), L::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   float* vsc = reinterpret_cast<float*>(smem + L::OFF_VS);
   for (int i = tid; i < D; i += blockDim.x) vsc[i] = a.v_scale ? __ldg(a.v_scale + h * D + i) : 1.f;
@@ -580,6 +617,8 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
   }
   tc_fence_before();
   __syncthreads();
+  // a pair's barriers take arrivals from both CTAs: both are initialised first
+  if constexpr (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = misc[0];
 
@@ -606,9 +645,10 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       // int8 Q codes, or 16-bit Q rows that the softmax warps quantize; either
       // way they are staged in the V buffers until converted
       constexpr int QB = QRAW ? 2 : 1;
+      const uint32_t sm_qin = smem_u32(smem + L::OFF_QIN);
       mbar_arrive_expect_tx(bar(L::B_QFULL), QS * kM * D * QB);
       for (int s = 0; s < QS; ++s)
-        tma_load_4d(sm_v + s * L::QR * QB, &tm_q, bar(L::B_QFULL), 0, q0 + s * kM, h, b);
+        tma_load_4d(sm_qin + s * L::QR * QB, &tm_q, bar(L::B_QFULL), 0, q0 + s * kM, h, b);
       bool ok = true;
       for (int it = 0; it < n_it; ++it) {
         const int kt = SPARSE ? static_cast<int>(list[it0 + it]) : it0 + it;
@@ -624,19 +664,20 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
           kdst = sm_kr + rs * L::KR;
         }
         if (!ok) break;
-        mbar_arrive_expect_tx(bar(L::B_KRF + ks), BN * D);
-        tma_load_4d(kdst, &tm_k, bar(L::B_KRF + ks), 0, kt * BN, h, b);
+        mbar_arrive_expect_tx(bar(L::B_KRF + ks), L::KROWS * D);
+        tma_load_4d(kdst, &tm_k, bar(L::B_KRF + ks), 0, kt * BN + static_cast<int>(crank) * L::KROWS, h, b);
         kr_last[ks] = it;
         const int vs = it % L::NVS;
-        if (it == 0 || (QRAW && it < L::NVS))  // raw Q sits in V buffer 0 (all of them)
+        if (!PAIR && (it == 0 || (QRAW && it < L::NVS)))  // raw Q sits in V buffer 0 (all of them)
           ok = wait_bar(bar(L::B_QCONV), 0, ctl, kErrProducer);
         else if (it >= L::NVS)
           ok = wait_bar(bar(L::B_VE + vs), ((it / L::NVS) - 1) & 1, ctl, kErrProducer);
         if (!ok) break;
-        mbar_arrive_expect_tx(bar(L::B_VF + vs), BN * D * 2);
+        mbar_arrive_expect_tx(bar(L::B_VF + vs), BN * L::VCOLS * 2);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sm_v + vs * L::VB + c * BN * 128, &tm_v, bar(L::B_VF + vs), c * 64, kt * BN, h, b);
+        for (int c = 0; c < L::VCOLS / 64; ++c)
+          tma_load_4d(sm_v + vs * L::VB + c * BN * 128, &tm_v, bar(L::B_VF + vs),
+                      static_cast<int>(crank) * L::VCOLS + c * 64, kt * BN, h, b);
         v_last[vs] = it;
         if constexpr (ROWMASK) {  // the tile's mask rows, released with the tile's k scales
           const int ms = it % L::NSC;
@@ -648,6 +689,12 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
                         bar(L::B_MF + ms), kt * BN + x * m_kpb, q0, m_h, m_b);
           m_last[ms] = it;
         }
+      }
+      if (PAIR && !leader && ok) {
+        // The leader's last V-empty commits arrive here too and nothing else
+        // waits for them: take them before this CTA may exit.
+        for (int t = max(0, n_it - L::NVS); t < n_it - 1; ++t)
+          drain_bar(bar(L::B_VE + t % L::NVS), (t / L::NVS) & 1, a.timeout_ns);
       }
       if (!ok) {  // let issued copies land before the CTA's shared memory goes away
         drain_bar(bar(L::B_QFULL), 0, a.timeout_ns);
@@ -661,9 +708,20 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     }
   } else if (warp == L::W_MMA) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idq = idesc_f16(kM, BN, 0, 0, 0, 0);                  // f16 x f16, K-major
-      constexpr uint32_t idv = idesc_f16(kM, D, VBF16 ? 1 : 0, VBF16 ? 1 : 0, 0, 1);  // V MN-major
+    if (lane == 0 && PAIR && !leader) {
+      // The peer issues no MMA: its lane forwards the completion of its Q
+      // conversion and of each V tile's copy to the leader's barriers.
+      bool ok = wait_bar(bar(L::B_QCONV), 0, ctl, kErrMma);
+      if (ok) mbar_arrive_cluster(lbar(L::B_QCONV));
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int vs = it % L::NVS;
+        ok = wait_bar(bar(L::B_VF + vs), (it / L::NVS) & 1, ctl, kErrMma);
+        if (ok) mbar_arrive_cluster(lbar(L::B_VF + vs));
+      }
+    } else if (lane == 0) {
+      constexpr int MM = PAIR ? 2 * kM : kM;  // rows of one MMA
+      constexpr uint32_t idq = idesc_f16(MM, BN, 0, 0, 0, 0);                  // f16 x f16, K-major
+      constexpr uint32_t idv = idesc_f16(MM, D, VBF16 ? 1 : 0, VBF16 ? 1 : 0, 0, 1);  // V MN-major
       // Descriptors are built once; a k-step or buffer offset is added to the
       // 14-bit start-address field (16-byte units), which cannot overflow for
       // addresses inside the CTA's shared memory. This keeps the issuing
@@ -671,6 +729,14 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       const uint64_t qdesc = sdesc_sw128(sm_qh, 16, 1024);
       const uint64_t kdesc = sdesc_sw128(sm_kh, 16, 1024);
       const uint64_t vdesc = sdesc_sw128(sm_v, BN * 128, 1024);
+      // a barrier that also counts the peer's arrivals
+      auto wait_in = [&](int i, uint32_t parity) {
+        return PAIR ? wait_bar_cluster(bar(i), parity, ctl, kErrMma) : wait_bar(bar(i), parity, ctl, kErrMma);
+      };
+      auto commit = [&](int i) {
+        if constexpr (PAIR) mma_commit_pair(bar(i), 3);
+        else mma_commit(bar(i));
+      };
       auto issue_qk = [&](int s, int kst) {
         const uint64_t qa = qdesc + static_cast<uint64_t>((s * L::QH) >> 4);
         const uint64_t kb = kdesc + static_cast<uint64_t>((kst * L::KH) >> 4);
@@ -678,8 +744,9 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t ad = qa + static_cast<uint64_t>(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
-          const uint64_t bd = kb + static_cast<uint64_t>(((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4);
-          mma_ss(dt, ad, bd, idq, kk > 0 ? 1u : 0u);
+          const uint64_t bd = kb + static_cast<uint64_t>(((kk >> 2) * (L::KROWS * 128) + (kk & 3) * 32) >> 4);
+          if constexpr (PAIR) mma_ss_pair(dt, ad, bd, idq, kk > 0 ? 1u : 0u);
+          else mma_ss(dt, ad, bd, idq, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int s, int vs, bool first) {
@@ -687,23 +754,25 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         const uint32_t dt = tmem + QS * BN + s * D;
         const uint32_t pt = tmem + s * BN;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(dt, pt + kk * 8, vb + static_cast<uint64_t>((kk * 16 * 128) >> 4), idv,
-                 (first && kk == 0) ? 0u : 1u);
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t bd = vb + static_cast<uint64_t>((kk * 16 * 128) >> 4);
+          if constexpr (PAIR) mma_ts_pair(dt, pt + kk * 8, bd, idv, (first && kk == 0) ? 0u : 1u);
+          else mma_ts(dt, pt + kk * 8, bd, idv, (first && kk == 0) ? 0u : 1u);
+        }
       };
-      bool ok = wait_bar(bar(L::B_QCONV), 0, ctl, kErrMma);
+      bool ok = wait_in(L::B_QCONV, 0);
       if (ok && a.debug_stall) ok = wait_bar(bar(L::B_STALL), 0, ctl, kErrMma);
       tc_fence_after();
       for (int it = 0; it < n_it && ok; ++it) {
         const int kst = it % L::NKS;
         IA_TRACE_POINT(8, it);
-        ok = wait_bar(bar(L::B_KCF + kst), (it / L::NKS) & 1, ctl, kErrMma);
+        ok = wait_in(L::B_KCF + kst, (it / L::NKS) & 1);
         if (!ok) break;
         IA_TRACE_POINT(9, it);
         tc_fence_after();
         const int pvs = (it + L::NVS - 1) % L::NVS;
         if (it > 0) {
-          ok = wait_bar(bar(L::B_VF + pvs), ((it - 1) / L::NVS) & 1, ctl, kErrMma);
+          ok = wait_in(L::B_VF + pvs, ((it - 1) / L::NVS) & 1);
           if (!ok) break;
           tc_fence_after();
         }
@@ -715,35 +784,40 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
             issue_pv(s, pvs, it == 1);
           }
           issue_qk(s, kst);
-          mma_commit(bar(L::B_SF + s));
+          commit(L::B_SF + s);
           IA_TRACE_POINT(10 + s, it);
         }
         if (!ok) break;
-        mma_commit(bar(L::B_KCE + kst));
-        if (it > 0) mma_commit(bar(L::B_VE + pvs));
+        commit(L::B_KCE + kst);
+        if (it > 0) commit(L::B_VE + pvs);
       }
       if (ok && n_it > 0) {
         const int pvs = (n_it - 1) % L::NVS;
-        ok = wait_bar(bar(L::B_VF + pvs), ((n_it - 1) / L::NVS) & 1, ctl, kErrMma);
+        ok = wait_in(L::B_VF + pvs, ((n_it - 1) / L::NVS) & 1);
         if (ok) tc_fence_after();
         for (int s = 0; s < QS && ok; ++s) {
           ok = wait_bar(bar(L::B_PF + s), (n_it - 1) & 1, ctl, kErrMma);
           if (!ok) break;
           tc_fence_after();
           issue_pv(s, pvs, n_it == 1);
-          mma_commit(bar(L::B_OF + s));
+          commit(L::B_OF + s);
         }
       }
-      mma_commit(bar(L::B_DRAIN));  // every MMA issued above has completed once this arrives
+      // every MMA issued above has completed once this arrives (here only)
+      if constexpr (PAIR) mma_commit_pair(bar(L::B_DRAIN), 1);
+      else mma_commit(bar(L::B_DRAIN));
       drain_bar(bar(L::B_DRAIN), 0, a.timeout_ns);
+      // after an abort, commits to the peer may still be in flight
+      if (PAIR && !ok) __nanosleep(20000);
     }
   } else if (warp >= L::W_CONV) {
     // ---------------------------------------------- int8 -> fp16 converters
     const int ct = tid - L::W_CONV * 32;
     bool ok = QRAW ? true : wait_bar(bar(L::B_QFULL), 0, ctl, kErrConverter);
+    if constexpr (PAIR) ok = __all_sync(0xffffffffu, ok);
     if (ok && !QRAW) {
       for (int s = 0; s < QS; ++s)
-        widen_tile<D, kM, false>(smem + L::OFF_V + s * L::QR, smem + L::OFF_QH + s * L::QH, ct);
+        widen_tile<D, kM, false>(smem + L::OFF_QIN + s * L::QR, smem + L::OFF_QH + s * L::QH, ct);
       fence_proxy_async_smem();
       mbar_arrive(bar(L::B_QCONV));
     }
@@ -777,6 +851,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       // K tile: int8 -> fp16 codes in the swizzled layout the MMA reads
       const int kst = it % L::NKS;
       ok = wait_bar(bar(L::B_KRF + kst), (it / L::NKS) & 1, ctl, kErrConverter);
+      if constexpr (PAIR) ok = __all_sync(0xffffffffu, ok);  // warps stay converged
       if (!ok) break;
       if (ct == 0) IA_TRACE_POINT(12, it);
       if constexpr (L::INPLACE) {
@@ -785,16 +860,23 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       } else {
         const int rs = it % L::NRS;
         if (it >= L::NKS) ok = wait_bar(bar(L::B_KCE + kst), ((it / L::NKS) - 1) & 1, ctl, kErrConverter);
+        if constexpr (PAIR) ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        widen_tile<D, BN, false>(smem + L::OFF_KR + rs * L::KR, smem + L::OFF_KH + kst * L::KH, ct);
+        widen_tile<D, L::KROWS, false>(smem + L::OFF_KR + rs * L::KR, smem + L::OFF_KH + kst * L::KH, ct);
         mbar_arrive(bar(L::B_KRE + rs));
       }
       if (ct == 0) IA_TRACE_POINT(13, it);
       fence_proxy_async_smem();
-      mbar_arrive(bar(L::B_KCF + kst));
+      if (PAIR && !leader) {  // the leader's MMA reads this half: one arrival per warp
+        __syncwarp();
+        if ((ct & 31) == 0) mbar_arrive_cluster(lbar(L::B_KCF + kst));
+      } else {
+        mbar_arrive(bar(L::B_KCF + kst));
+      }
       // k scales, bias * log2(e) (-inf past the valid keys) and tile flags
       const int ss = it % L::NSC;
       if (it >= L::NSC) ok = wait_bar(bar(L::B_SCE + ss), ((it / L::NSC) - 1) & 1, ctl, kErrConverter);
+      if constexpr (PAIR) ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       float* ksm = reinterpret_cast<float*>(smem + L::OFF_SC + ss * L::SC);
       float* b2m = ksm + BN;
@@ -834,6 +916,11 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       }
       mbar_arrive(bar(L::B_SCF + ss));
     }
+    if (PAIR && !leader && ok) {
+      // the leader's last K-empty commits arrive here too; take them before exit
+      for (int t = max(0, n_it - L::NKS); t < n_it; ++t)
+        drain_bar(bar(L::B_KCE + t % L::NKS), (t / L::NKS) & 1, a.timeout_ns);
+    }
   } else {
     // ------------------------------------------------------------- softmax
     const int s = warp >> 2;
@@ -850,7 +937,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       // block's two warps also scans the other warp's rows; without the
       // prologue those rows are not modified, so no barrier is needed).
       ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_QFULL), 0, ctl, kErrSoftmax));
-      uint8_t* raw = smem + L::OFF_V + static_cast<size_t>(s * kM) * D * 2;
+      uint8_t* raw = smem + L::OFF_QIN + static_cast<size_t>(s * kM) * D * 2;
       auto quantized = [&](int rr) {  // row rr of this stage: real and not padding
         const int gr = q0 + s * kM + rr;
         return gr < a.Sq && !(a.pad_query && (gr & 63) >= __ldg(a.kv_valid + (gr >> 6)));
@@ -1012,7 +1099,15 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(L::B_PF + s));
+      if (PAIR && !leader) {
+        // The leader's MMA reads this P from this CTA's TMEM: one arrival per
+        // warp. The tcgen05 wait and fence above order the stores; a
+        // cluster-scope release here would stall the warp ~1,000 cycles.
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(lbar(L::B_PF + s));
+      } else {
+        mbar_arrive(bar(L::B_PF + s));
+      }
       if (r == 0) IA_TRACE_POINT(3 + 4 * s, it);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::B_SCE + ss));
@@ -1075,9 +1170,13 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
   // ------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
+  // Neither CTA of a pair leaves while the leader's MMAs may still read the
+  // peer's shared memory or TMEM, or the peer's arrivals reach the leader.
+  if constexpr (PAIR) cluster_sync();
   if (warp == L::W_MMA) {
     tc_fence_after();
-    tmem_dealloc(tmem, L::TMEM_COLS);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, L::TMEM_COLS);
+    else tmem_dealloc(tmem, L::TMEM_COLS);
   }
 }
 
@@ -1117,9 +1216,9 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int esiz
   return r == CUDA_SUCCESS;
 }
 
-template <int D, int QS, int BN, bool SPARSE, bool VBF16, bool QRAW, bool ROWMASK>
+template <int D, int QS, int BN, bool SPARSE, bool VBF16, bool QRAW, bool ROWMASK, bool PAIR = false>
 ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** msg) {
-  using L = Layout<D, QS, BN, SPARSE, ROWMASK>;
+  using L = Layout<D, QS, BN, SPARSE, ROWMASK, PAIR>;
   const ia_attn_params& p = A.p;
   CUtensorMap tq, tk, tv, tm;
   std::memset(&tm, 0, sizeof(tm));
@@ -1143,7 +1242,7 @@ ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** ms
   const bool okq = make_map(&tq, qdt, A.q, QRAW ? 2 : 1, D, p.Sq, p.H, p.B, p.q_strides[2],
                             p.q_strides[1], p.q_strides[0], D, kM, CU_TENSOR_MAP_SWIZZLE_NONE);
   const bool okk = make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, A.k, 1, D, p.Sk, p.H, p.B,
-                            p.k_strides[2], p.k_strides[1], p.k_strides[0], D, BN,
+                            p.k_strides[2], p.k_strides[1], p.k_strides[0], D, L::KROWS,
                             CU_TENSOR_MAP_SWIZZLE_NONE);
   const bool okv = make_map(&tv, VBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                             A.v, 2, D, p.Sk, p.H, p.B, p.v_strides[2], p.v_strides[1],
@@ -1210,7 +1309,7 @@ ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** ms
     a.ws_l = a.ws_o + static_cast<int64_t>(nsplit) * rows * D;
   }
   const size_t smem = L::SMEM_FIXED + (SPARSE ? static_cast<size_t>(a.Tk) * 2 : 0);
-  auto kern = attn_fwd_kernel<D, QS, BN, SPARSE, VBF16, QRAW, ROWMASK>;
+  auto kern = attn_fwd_kernel<D, QS, BN, SPARSE, VBF16, QRAW, ROWMASK, PAIR>;
   if (smem > 232448) {
     *msg = "key-tile list does not fit in shared memory (too many key tiles)";
     return IA_ERR_UNSUPPORTED;
@@ -1221,8 +1320,30 @@ ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** ms
     *msg = cudaGetErrorString(e);
     return IA_ERR_CUDA;
   }
-  dim3 grid((p.Sq + kM * QS - 1) / (kM * QS), p.H, p.B * nsplit);
-  kern<<<grid, L::NWARPS * 32, smem, st>>>(tq, tk, tv, tm, a);
+  int gx = (p.Sq + kM * QS - 1) / (kM * QS);
+  if (PAIR) gx = (gx + 1) & ~1;  // whole pairs; a surplus CTA's rows are all past Sq
+  dim3 grid(gx, p.H, p.B * nsplit);
+  if constexpr (PAIR) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(L::NWARPS * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tm, a);
+    if (e != cudaSuccess) {
+      *msg = cudaGetErrorString(e);
+      return IA_ERR_CUDA;
+    }
+  } else {
+    kern<<<grid, L::NWARPS * 32, smem, st>>>(tq, tk, tv, tm, a);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     *msg = cudaGetErrorString(e);
@@ -1275,9 +1396,9 @@ ia_status dispatch(const AttnLaunch& A, int num_sms, cudaStream_t st, const char
     return bf ? run<64, 1, 64, true, true, QRAW, false>(A, num_sms, st, msg)
               : run<64, 1, 64, true, false, QRAW, false>(A, num_sms, st, msg);
   }
-  if (p.D == 128)
-    return bf ? run<128, 2, 128, false, true, QRAW, false>(A, num_sms, st, msg)
-              : run<128, 2, 128, false, false, QRAW, false>(A, num_sms, st, msg);
+  if (p.D == 128)  // CTA pairs with 256-row MMAs
+    return bf ? run<128, 2, 128, false, true, QRAW, false, true>(A, num_sms, st, msg)
+              : run<128, 2, 128, false, false, QRAW, false, true>(A, num_sms, st, msg);
   return bf ? run<64, 2, 128, false, true, QRAW, false>(A, num_sms, st, msg)
             : run<64, 2, 128, false, false, QRAW, false>(A, num_sms, st, msg);
 }
