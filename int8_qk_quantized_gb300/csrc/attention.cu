@@ -188,13 +188,11 @@ struct Ctl {
 // Bounded wait on an mbarrier phase. Returns false when the wait ran out here
 // (the status word and the CTA's abort flag are set) or another thread of
 // the CTA has already aborted.
-// `cluster`: the phase includes arrivals from the peer CTA of a pair, whose
-// writes this thread then reads (acquire at cluster scope).
 __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, const Ctl& c,
-                                           unsigned code, bool cluster) {
+                                           unsigned code) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
-    if (cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (*c.abort) return false;
     if ((n & 15u) == 0 && *reinterpret_cast<volatile unsigned*>(&g_attn_status) != 0u) {
       *c.abort = 1;  // another CTA already timed out: stop waiting as well
@@ -211,12 +209,7 @@ __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, const 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c,
                                          unsigned code) {
   if (mbar_try_wait(bar, parity)) return true;
-  return wait_bar_slow(bar, parity, c, code, false);
-}
-__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, const Ctl& c,
-                                                 unsigned code) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  return wait_bar_slow(bar, parity, c, code, true);
+  return wait_bar_slow(bar, parity, c, code);
 }
 
 // Bounded wait that ignores the abort flag: used to let copies and MMAs that
@@ -242,16 +235,17 @@ __device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity, unsigned l
 // other half of the next: its int8 reads then cover all 32 banks once, and its
 // fp16 writes land in 8 distinct 16-byte slots of the swizzle (a phase holding
 // one whole row would write both 64-column blocks to the same slots).
-template <int D, int ROWS, bool IN_PLACE>
+template <int D, int ROWS, bool IN_PLACE, bool LOAD_ALL = false>
 __device__ __forceinline__ void widen_tile(const uint8_t* raw, uint8_t* dst, int ct) {
   constexpr int CPR = D / 16;              // 16-byte int8 chunks per row
   constexpr int NI = ROWS * CPR / 64;      // chunks per thread
   // Chunks loaded before any is stored. In place, all of them: a warp owns
   // whole rows and a row's fp16 output overwrites only its own int8 row, so one
   // warp barrier after the loads suffices (instead of a load-barrier-store
-  // round trip per chunk). From a staging buffer, one at a time; the loop is
-  // kept rolled, as unrolling it cost the masked softmax registers.
-  constexpr int NB = IN_PLACE ? NI : 1;
+  // round trip per chunk). From a staging buffer, one at a time unless
+  // LOAD_ALL; the loop is kept rolled, as unrolling it cost the masked
+  // softmax registers.
+  constexpr int NB = (IN_PLACE || LOAD_ALL) ? NI : 1;
   static_assert(ROWS * CPR % 64 == 0 && NI % NB == 0, "widen layout");
 #pragma unroll 1
   for (int i0 = 0; i0 < NI; i0 += NB) {
@@ -712,11 +706,11 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       // The peer issues no MMA: its lane forwards the completion of its Q
       // conversion and of each V tile's copy to the leader's barriers.
       bool ok = wait_bar(bar(L::B_QCONV), 0, ctl, kErrMma);
-      if (ok) mbar_arrive_cluster(lbar(L::B_QCONV));
+      if (ok) mbar_arrive_remote(lbar(L::B_QCONV));
       for (int it = 0; it < n_it && ok; ++it) {
         const int vs = it % L::NVS;
         ok = wait_bar(bar(L::B_VF + vs), (it / L::NVS) & 1, ctl, kErrMma);
-        if (ok) mbar_arrive_cluster(lbar(L::B_VF + vs));
+        if (ok) mbar_arrive_remote(lbar(L::B_VF + vs));
       }
     } else if (lane == 0) {
       constexpr int MM = PAIR ? 2 * kM : kM;  // rows of one MMA
@@ -730,9 +724,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       const uint64_t kdesc = sdesc_sw128(sm_kh, 16, 1024);
       const uint64_t vdesc = sdesc_sw128(sm_v, BN * 128, 1024);
       // a barrier that also counts the peer's arrivals
-      auto wait_in = [&](int i, uint32_t parity) {
-        return PAIR ? wait_bar_cluster(bar(i), parity, ctl, kErrMma) : wait_bar(bar(i), parity, ctl, kErrMma);
-      };
+      auto wait_in = [&](int i, uint32_t parity) { return wait_bar(bar(i), parity, ctl, kErrMma); };
       auto commit = [&](int i) {
         if constexpr (PAIR) mma_commit_pair(bar(i), 3);
         else mma_commit(bar(i));
@@ -869,7 +861,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       fence_proxy_async_smem();
       if (PAIR && !leader) {  // the leader's MMA reads this half: one arrival per warp
         __syncwarp();
-        if ((ct & 31) == 0) mbar_arrive_cluster(lbar(L::B_KCF + kst));
+        if ((ct & 31) == 0) mbar_arrive_remote(lbar(L::B_KCF + kst));
       } else {
         mbar_arrive(bar(L::B_KCF + kst));
       }
@@ -1101,8 +1093,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       tc_fence_before();
       if (PAIR && !leader) {
         // The leader's MMA reads this P from this CTA's TMEM: one arrival per
-        // warp. The tcgen05 wait and fence above order the stores; a
-        // cluster-scope release here would stall the warp ~1,000 cycles.
+        // warp, ordered by the tcgen05 wait and fence above.
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(lbar(L::B_PF + s));
       } else {
