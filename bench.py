@@ -41,8 +41,8 @@ PAGE_SPLIT_MS = 11.05
 # SHA-256 of the kernel sources it was taken on. A launch's traffic is scaled
 # from it per head, with the key-proportional part scaled by the keys of the
 # launch. When the kernel sources change, the figure no longer applies.
-ATTN_TRAFFIC = {"source_sha256": "befbf57134c4fd691c9c668ab56b7fd06b19f1b2f3bfe93e0d16adaeae754249",
-                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 245016832.0}
+ATTN_TRAFFIC = {"source_sha256": "e0fe8f7e0d26e2fabf337c59d89a5ee4ca9b2610016557e4c2fdde6e4f6338f3",
+                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 245157632.0}
 
 
 def attn_source_sha():
@@ -694,7 +694,7 @@ def main():
                      "traffic": attn_traffic_per_launch(H, Sq, [hi - lo, lo, Sk - hi], D),
                      "algorithmic_bytes": sum(H * (Sq * D * 3 + Sq * 8 + n * (D * 3 + 4))
                                               for n in (hi - lo, lo, Sk - hi)) / 3,
-                     "kernel": "attn_fwd_kernel (QS=2, BN=128, D=128); per launch = mean of "
+                     "kernel": "attn_fwd_kernel (CTA pairs, QS=2, BN=128, D=128); per launch = mean of "
                                "the step's three attention launches",
                      "peak_source": f"{peak_kind} bf16 dense burst (MEASURED_PEAKS.json)",
                      "frac_of_sustained": achieved / bf16_sus if bf16_sus else None},
