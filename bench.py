@@ -41,16 +41,22 @@ PAGE_SPLIT_MS = 11.05
 # SHA-256 of the kernel sources it was taken on. A launch's traffic is scaled
 # from it per head, with the key-proportional part scaled by the keys of the
 # launch. When the kernel sources change, the figure no longer applies.
-ATTN_TRAFFIC = {"source_sha256": "e0fe8f7e0d26e2fabf337c59d89a5ee4ca9b2610016557e4c2fdde6e4f6338f3",
+ATTN_TRAFFIC = {"source_sha256": "664d8114ab1ef98f13da8e8d15cf62d1b1ec6c7860a8d3511de126b4e438202c",
                 "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 245157632.0}
 
 
 def attn_source_sha():
+    """SHA-256 of the attention kernel's code: attention.cu and ptx.cuh with their
+    comments and whitespace removed, so that a comment edit keeps the figure."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in ("attention.cu", "ptx.cuh"):
-        with open(os.path.join(ROOT, "int8_qk_quantized_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "int8_qk_quantized_gb300", "csrc", f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()
 
 

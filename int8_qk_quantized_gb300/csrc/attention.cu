@@ -19,6 +19,10 @@
 //    S_s = Q_s K_j^T into TMEM, then O_s += P_s V_j with P_s read from TMEM.
 //    While the softmax warpgroup of one stage works on its S tile, the tensor
 //    core runs the other stage's MMAs.
+//  * Dense D = 128 runs as CTA pairs (clusters of two): the even CTA issues
+//    256-row MMAs (cta_group::2) over both CTAs' query rows; each CTA holds and
+//    widens half of every K tile and half of V's columns, which cuts each SM's
+//    operand reads from shared memory by a third and its widening by half.
 //  * Softmax warpgroups own one query row per thread (TMEM lane = row). They
 //    apply k_scale (and bias, masks) to the FP32 logits, keep a running
 //    maximum in log2 units, rescale O in TMEM only when the maximum grew by
