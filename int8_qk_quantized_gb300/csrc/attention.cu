@@ -134,6 +134,11 @@ struct Layout {
   static constexpr int NRS = INPLACE ? 0 : 2;
   // A CTA pair (PAIR) holds half of each key tile's K rows and half of V's
   // columns per CTA; the 256-row MMA reads the other halves from the peer.
+  // One query stage (QS == 1): S is double-buffered in TMEM, so the QK^T of
+  // key tile j+1 runs while the softmax works on tile j; B_OF then counts the
+  // P V of every tile (the softmax waits on it before rescaling O).
+  static constexpr bool DBS = QS == 1;
+  static constexpr int NSB = DBS ? 2 : QS;  // S buffers in TMEM
   static constexpr int KROWS = PAIR ? BN / 2 : BN;  // keys of a K tile held here
   static constexpr int VCOLS = PAIR ? D / 2 : D;    // V columns held here
   static constexpr int QH = kM * D * 2;      // fp16 Q stage
@@ -162,13 +167,13 @@ struct Layout {
   static constexpr int B_QFULL = 0, B_QCONV = 1, B_KRF = 2, B_KRE = B_KRF + NKS,
                        B_KCF = B_KRE + NRS, B_KCE = B_KCF + NKS, B_VF = B_KCE + NKS,
                        B_VE = B_VF + NVS, B_SCF = B_VE + NVS, B_SCE = B_SCF + NSC,
-                       B_SF = B_SCE + NSC, B_PF = B_SF + QS, B_OF = B_PF + QS,
+                       B_SF = B_SCE + NSC, B_PF = B_SF + NSB, B_OF = B_PF + NSB,
                        B_DRAIN = B_OF + QS, B_STALL = B_DRAIN + 1, B_MF = B_STALL + 1,
                        NBAR = B_MF + NSC;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;       // tmem base, abort, count, pad
   static constexpr int OFF_LIST = OFF_MISC + 16 + 32;       // + warp counts for the list scan
   static constexpr int SMEM_FIXED = OFF_LIST;
-  static constexpr int TMEM_NEED = QS * BN + QS * D;
+  static constexpr int TMEM_NEED = NSB * BN + QS * D;
   static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64
                                    : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
   static constexpr int NWARPS = 4 * QS + 4;
@@ -558,11 +563,11 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       mbar_init(bar(L::B_SCF + i), 64);
       mbar_init(bar(L::B_SCE + i), 4 * QS);
     }
-    for (int s = 0; s < QS; ++s) {
+    for (int s = 0; s < L::NSB; ++s) {
       mbar_init(bar(L::B_SF + s), 1);
       mbar_init(bar(L::B_PF + s), kM + peer_p);
-      mbar_init(bar(L::B_OF + s), 1);
     }
+    for (int s = 0; s < QS; ++s) mbar_init(bar(L::B_OF + s), 1);
     for (int i = 0; i < L::NSC; ++i) mbar_init(bar(L::B_MF + i), 1);
     mbar_init(bar(L::B_DRAIN), 1);
     mbar_init(bar(L::B_STALL), 1);  // never signalled: the timeout test hook waits on it
@@ -733,10 +738,11 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         if constexpr (PAIR) mma_commit_pair(bar(i), 3);
         else mma_commit(bar(i));
       };
-      auto issue_qk = [&](int s, int kst) {
+      // S buffer sb <- Q_s K^T (K from stage kst)
+      auto issue_qk = [&](int s, int kst, int sb) {
         const uint64_t qa = qdesc + static_cast<uint64_t>((s * L::QH) >> 4);
         const uint64_t kb = kdesc + static_cast<uint64_t>((kst * L::KH) >> 4);
-        const uint32_t dt = tmem + s * BN;
+        const uint32_t dt = tmem + sb * BN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t ad = qa + static_cast<uint64_t>(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
@@ -745,10 +751,11 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
           else mma_ss(dt, ad, bd, idq, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int s, int vs, bool first) {
+      // O_s += P V (P from S buffer sb, V from stage vs)
+      auto issue_pv = [&](int s, int vs, bool first, int sb) {
         const uint64_t vb = vdesc + static_cast<uint64_t>((vs * L::VB) >> 4);
-        const uint32_t dt = tmem + QS * BN + s * D;
-        const uint32_t pt = tmem + s * BN;
+        const uint32_t dt = tmem + L::NSB * BN + s * D;
+        const uint32_t pt = tmem + sb * BN;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           const uint64_t bd = vb + static_cast<uint64_t>((kk * 16 * 128) >> 4);
@@ -759,7 +766,32 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       bool ok = wait_in(L::B_QCONV, 0);
       if (ok && a.debug_stall) ok = wait_bar(bar(L::B_STALL), 0, ctl, kErrMma);
       tc_fence_after();
-      for (int it = 0; it < n_it && ok; ++it) {
+      if constexpr (L::DBS) {
+        // QK^T of tiles 0 and 1, then per tile j: P_j V_j, and the QK^T of
+        // tile j+2 into the S buffer that P_j V_j has just read
+        auto qk_step = [&](int j) -> bool {
+          const int kst = j % L::NKS;
+          if (!wait_in(L::B_KCF + kst, (j / L::NKS) & 1)) return false;
+          tc_fence_after();
+          issue_qk(0, kst, j & 1);
+          commit(L::B_SF + (j & 1));
+          commit(L::B_KCE + kst);
+          return true;
+        };
+        for (int j = 0; j < 2 && j < n_it && ok; ++j) ok = qk_step(j);
+        for (int it = 0; it < n_it && ok; ++it) {
+          const int vs = it % L::NVS;
+          ok = wait_in(L::B_VF + vs, (it / L::NVS) & 1);
+          if (ok) ok = wait_bar(bar(L::B_PF + (it & 1)), (it >> 1) & 1, ctl, kErrMma);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(0, vs, it == 0, it & 1);
+          commit(L::B_OF);  // one phase per tile
+          commit(L::B_VE + vs);
+          if (it + 2 < n_it) ok = qk_step(it + 2);
+        }
+      }
+      for (int it = 0; it < n_it && ok && !L::DBS; ++it) {
         const int kst = it % L::NKS;
         IA_TRACE_POINT(8, it);
         ok = wait_in(L::B_KCF + kst, (it / L::NKS) & 1);
@@ -777,9 +809,9 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
             ok = wait_bar(bar(L::B_PF + s), (it - 1) & 1, ctl, kErrMma);
             if (!ok) break;
             tc_fence_after();
-            issue_pv(s, pvs, it == 1);
+            issue_pv(s, pvs, it == 1, s);
           }
-          issue_qk(s, kst);
+          issue_qk(s, kst, s);
           commit(L::B_SF + s);
           IA_TRACE_POINT(10 + s, it);
         }
@@ -787,7 +819,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         commit(L::B_KCE + kst);
         if (it > 0) commit(L::B_VE + pvs);
       }
-      if (ok && n_it > 0) {
+      if (ok && n_it > 0 && !L::DBS) {
         const int pvs = (n_it - 1) % L::NVS;
         ok = wait_in(L::B_VF + pvs, ((n_it - 1) / L::NVS) & 1);
         if (ok) tc_fence_after();
@@ -795,7 +827,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
           ok = wait_bar(bar(L::B_PF + s), (n_it - 1) & 1, ctl, kErrMma);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(s, pvs, n_it == 1);
+          issue_pv(s, pvs, n_it == 1, s);
           commit(L::B_OF + s);
         }
       }
@@ -922,8 +954,8 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     const int s = warp >> 2;
     const int r = tid & (kM - 1);
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + s * BN + lane_off;
-    const uint32_t tO = tmem + QS * BN + s * D + lane_off;
+    const uint32_t tS0 = tmem + s * BN + lane_off;
+    const uint32_t tO = tmem + L::NSB * BN + s * D + lane_off;
     const int row = q0 + s * kM + r;
     const bool row_ok = row < a.Sq;
     float cq = 0.f;
@@ -967,10 +999,19 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     const int half = (r >= 64) ? 1 : 0;
     float m = -INFINITY;  // reference maximum (log2 units) that P is relative to
     float l = 0.f;
+    // One query stage: this tile's P is stored (and O rescaled) only once the
+    // previous tile's P V has completed. Stores that overlapped it corrupted O
+    // on some rows (128-dim block-sparse parity test), although they target
+    // the other S buffer; with the wait the outputs match exactly. A wait
+    // that runs out (voted across the warp) clears `ok`, which ends the loop
+    // after this tile.
     for (int it = 0; it < n_it && ok; ++it) {
       const int ss = it % L::NSC;
       if (r == 0) IA_TRACE_POINT(4 * s, it);
-      bool w = wait_bar(bar(L::B_SF + s), it & 1, ctl, kErrSoftmax);
+      // this tile's S buffer (alternating with one query stage)
+      const int sb = L::DBS ? (it & 1) : s;
+      const uint32_t tS = L::DBS ? tS0 + sb * BN : tS0;
+      bool w = wait_bar(bar(L::B_SF + sb), L::DBS ? (it >> 1) & 1 : it & 1, ctl, kErrSoftmax);
       w = w && wait_bar(bar(L::B_SCF + ss), (it / L::NSC) & 1, ctl, kErrSoftmax);
       if (ROWMASK) w = w && wait_bar(bar(L::B_MF + ss), (it / L::NSC) & 1, ctl, kErrSoftmax);
       ok = __all_sync(0xffffffffu, w);
@@ -992,6 +1033,10 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         uint32_t z[BN / 2];
 #pragma unroll
         for (int e = 0; e < BN / 2; ++e) z[e] = 0u;
+        if (L::DBS && it > 0) {
+          if (!__all_sync(0xffffffffu, wait_bar(bar(L::B_OF), (it - 1) & 1, ctl, kErrSoftmax))) ok = false;
+          tc_fence_after();
+        }
         if constexpr (BN == 128) {
           tmem_st64(tS, z);
         } else {
@@ -1053,6 +1098,11 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         const bool need = m_new > m + kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
           const float alpha = need ? ex2(m - m_new) : 1.f;
+          if (L::DBS && it > 0) {  // the previous tile's P V may still be adding into O
+            ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_OF), (it - 1) & 1, ctl, kErrSoftmax));
+            if (!ok) break;
+            tc_fence_after();
+          }
           if (it > 0) {
   #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
@@ -1083,6 +1133,10 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
           lsum[e & 1] = fadd2(lsum[e & 1], pack2(p0, p1));
           sv[e] = VBF16 ? cvt_bf16x2(p0, p1) : cvt_f16x2(p0, p1);
         }
+        if (L::DBS && it > 0) {
+          if (!__all_sync(0xffffffffu, wait_bar(bar(L::B_OF), (it - 1) & 1, ctl, kErrSoftmax))) ok = false;
+          tc_fence_after();
+        }
         if constexpr (BN == 128) {
           tmem_st64(tS, *reinterpret_cast<uint32_t(*)[64]>(sv));
         } else {
@@ -1099,16 +1153,17 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         // The leader's MMA reads this P from this CTA's TMEM: one arrival per
         // warp, ordered by the tcgen05 wait and fence above.
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(lbar(L::B_PF + s));
+        if (lane == 0) mbar_arrive_remote(lbar(L::B_PF + sb));
       } else {
-        mbar_arrive(bar(L::B_PF + s));
+        mbar_arrive(bar(L::B_PF + sb));
       }
       if (r == 0) IA_TRACE_POINT(3 + 4 * s, it);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::B_SCE + ss));
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && n_it > 0) ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_OF + s), 0, ctl, kErrSoftmax));
+    if (ok && n_it > 0)
+      ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_OF + s), L::DBS ? (n_it - 1) & 1 : 0, ctl, kErrSoftmax));
     if (ok) {
       tc_fence_after();
       bool pad = false;
