@@ -244,17 +244,17 @@ __device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity, unsigned l
 // other half of the next: its int8 reads then cover all 32 banks once, and its
 // fp16 writes land in 8 distinct 16-byte slots of the swizzle (a phase holding
 // one whole row would write both 64-column blocks to the same slots).
-template <int D, int ROWS, bool IN_PLACE, bool LOAD_ALL = false>
+template <int D, int ROWS, bool IN_PLACE>
 __device__ __forceinline__ void widen_tile(const uint8_t* raw, uint8_t* dst, int ct) {
   constexpr int CPR = D / 16;              // 16-byte int8 chunks per row
   constexpr int NI = ROWS * CPR / 64;      // chunks per thread
   // Chunks loaded before any is stored. In place, all of them: a warp owns
   // whole rows and a row's fp16 output overwrites only its own int8 row, so one
   // warp barrier after the loads suffices (instead of a load-barrier-store
-  // round trip per chunk). From a staging buffer, one at a time unless
-  // LOAD_ALL; the loop is kept rolled, as unrolling it cost the masked
-  // softmax registers.
-  constexpr int NB = (IN_PLACE || LOAD_ALL) ? NI : 1;
+  // round trip per chunk). From a staging buffer, one at a time; the loop is
+  // kept rolled, as unrolling it cost the masked softmax registers (and
+  // loading all of a thread's chunks first measured slower in the pairs).
+  constexpr int NB = IN_PLACE ? NI : 1;
   static_assert(ROWS * CPR % 64 == 0 && NI % NB == 0, "widen layout");
 #pragma unroll 1
   for (int i0 = 0; i0 < NI; i0 += NB) {
