@@ -998,6 +998,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     }
     const int half = (r >= 64) ? 1 : 0;
     float m = -INFINITY;  // reference maximum (log2 units) that P is relative to
+    float m_pend = -INFINITY;  // one-pass tiles: the reference the next tile takes
     float l = 0.f;
     // One query stage: this tile's P is stored (and O rescaled) only once the
     // previous tile's P V has completed. Stores that overlapped it corrupted O
@@ -1052,6 +1053,93 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         }
         tmem_wait_ld(sv);
         if (r == 0) IA_TRACE_POINT(2 + 4 * s, it);
+        uint64_t lsum[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
+        // One pass for bf16 P (two query stages, a reference already set): P is
+        // taken relative to the reference the previous tiles set (bf16 keeps
+        // fp32's exponent range, so P may exceed 1), the tile's maximum is taken
+        // in the same pass, and a reference that grew by more than 2^8 is applied
+        // at the start of the next tile (O and l rescaled there, before this
+        // stage's next P V). The k-scale loads then overlap the exp2 work instead
+        // of preceding it. A row whose maximum exceeds the reference by more than
+        // 2^64 redoes the tile in two passes from S, which is still in TMEM.
+        constexpr bool OP = VBF16 && !L::DBS;
+        bool one = false;
+        if constexpr (OP) {
+          if (__any_sync(0xffffffffu, m_pend > m)) {  // the reference grew on the last tile
+            const float alpha = m_pend > m ? ex2(m - m_pend) : 1.f;
+  #pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t rr[32];
+              tmem_ld32(tO + c0, rr);
+              tmem_wait_ld(rr);
+  #pragma unroll
+              for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+              tmem_st32(tO + c0, rr);
+            }
+            l *= alpha;
+            m = fmaxf(m, m_pend);
+          }
+          one = __all_sync(0xffffffffu, m > -INFINITY);
+          if (one) {
+            const uint64_t cq2o = pack2(cq, cq);
+            const uint64_t nmo = pack2(-m, -m);
+            float mo[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (!fast) {  // t = acc k cq + offset (log2 units; -inf for invalid keys)
+  #pragma unroll
+              for (int c = 0; c < BN; c += 4) {
+                const float4 k4 = *reinterpret_cast<const float4*>(ksm + c);
+                const float4 b4 = *reinterpret_cast<const float4*>(b2m + c);
+                float t[4];
+                unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(k4.x, k4.y)),
+                              cq2o, pack2(b4.x, b4.y)), t[0], t[1]);
+                unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(k4.z, k4.w)),
+                              cq2o, pack2(b4.z, b4.w)), t[2], t[3]);
+                const int q = (c >> 2) & 3;
+                mo[q] = fmax3(mo[q], fmaxf(t[0], t[1]), fmaxf(t[2], t[3]));
+  #pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                  float t0, t1;
+                  unpack2(fadd2(pack2(t[2 * h2], t[2 * h2 + 1]), nmo), t0, t1);
+                  const float p0 = ex2(t0), p1 = ex2(t1);
+                  lsum[h2] = fadd2(lsum[h2], pack2(p0, p1));
+                  sv[(c >> 1) + h2] = cvt_bf16x2(p0, p1);
+                }
+              }
+            } else {
+  #pragma unroll
+            for (int c = 0; c < BN; c += 8) {
+              const float4 ka = *reinterpret_cast<const float4*>(ksm + c);
+              const float4 kb = *reinterpret_cast<const float4*>(ksm + c + 4);
+              float u[8];
+              unpack2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(ka.x, ka.y)), u[0], u[1]);
+              unpack2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(ka.z, ka.w)), u[2], u[3]);
+              unpack2(fmul2(pack2(__uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5])), pack2(kb.x, kb.y)), u[4], u[5]);
+              unpack2(fmul2(pack2(__uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7])), pack2(kb.z, kb.w)), u[6], u[7]);
+  #pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                mo[q] = fmax3(mo[q], u[2 * q], u[2 * q + 1]);
+                float t0, t1;
+                unpack2(ffma2(pack2(u[2 * q], u[2 * q + 1]), cq2o, nmo), t0, t1);
+                const float p0 = ex2(t0), p1 = ex2(t1);
+                lsum[q & 1] = fadd2(lsum[q & 1], pack2(p0, p1));
+                sv[(c >> 1) + q] = cvt_bf16x2(p0, p1);
+              }
+            }
+            }
+            const float rmo = fmaxf(fmaxf(mo[0], mo[1]), fmaxf(mo[2], mo[3]));
+            const float tmx = fast ? cq * rmo : rmo;
+            if (__any_sync(0xffffffffu, tmx > m + 64.f)) {
+              one = false;  // redo exactly: S is still in TMEM
+              if constexpr (BN == 128) tmem_ld128(tS, sv);
+              else tmem_ld64(tS, sv);
+              tmem_wait_ld(sv);
+              lsum[0] = lsum[1] = pack2(0.f, 0.f);
+            } else {
+              m_pend = tmx > m + kRescaleLog2 ? tmx : m;
+            }
+          }
+        }
+        if (!one) {  // ---- two passes: the row maximum, then P
         // u = acc * k_scale (fast tiles) or t = u * cq + bias*log2e / -inf
         // (masked tiles), in place, and the row maximum.
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -1121,7 +1209,6 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         const float k1 = fast ? cq : 1.f;
         const uint64_t k1v = pack2(k1, k1);
         const uint64_t nm = pack2(-mref, -mref);
-        uint64_t lsum[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
         // p = 2^(t - m) with the row sum in fp32; P packed to 16 bits in place
         // (pair i lands in word i, whose value is already consumed) and written
         // to the first BN/2 columns of S in one store.
@@ -1133,6 +1220,8 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
           lsum[e & 1] = fadd2(lsum[e & 1], pack2(p0, p1));
           sv[e] = VBF16 ? cvt_bf16x2(p0, p1) : cvt_f16x2(p0, p1);
         }
+        if (OP) m_pend = m;
+        }  // ---- two passes
         if (L::DBS && it > 0) {
           if (!__all_sync(0xffffffffu, wait_bar(bar(L::B_OF), (it - 1) & 1, ctl, kErrSoftmax))) ok = false;
           tc_fence_after();
