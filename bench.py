@@ -41,8 +41,8 @@ PAGE_SPLIT_MS = 11.05
 # SHA-256 of the kernel sources it was taken on. A launch's traffic is scaled
 # from it per head, with the key-proportional part scaled by the keys of the
 # launch. When the kernel sources change, the figure no longer applies.
-ATTN_TRAFFIC = {"source_sha256": "2d25b188cfadd1b82ad7e2d974841c1c2ed03a3c968e0c4f47e2a756b5ba129c",
-                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 245097984.0}
+ATTN_TRAFFIC = {"source_sha256": "3e9c22877fd961c236d1f7416637c5b33b9ece6aa36f09dd2a35746390f79eb1",
+                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 246484480.0}
 
 
 def attn_source_sha():
