@@ -1054,15 +1054,17 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         tmem_wait_ld(sv);
         if (r == 0) IA_TRACE_POINT(2 + 4 * s, it);
         uint64_t lsum[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
-        // One pass for bf16 P (two query stages, a reference already set): P is
-        // taken relative to the reference the previous tiles set (bf16 keeps
-        // fp32's exponent range, so P may exceed 1), the tile's maximum is taken
-        // in the same pass, and a reference that grew by more than 2^8 is applied
-        // at the start of the next tile (O and l rescaled there, before this
-        // stage's next P V). The k-scale loads then overlap the exp2 work instead
-        // of preceding it. A row whose maximum exceeds the reference by more than
-        // 2^64 redoes the tile in two passes from S, which is still in TMEM.
-        constexpr bool OP = VBF16 && !L::DBS;
+        // One pass (two query stages, a reference already set): P is taken
+        // relative to the reference the previous tiles set (P may exceed 1: up to
+        // 2^64 in bf16, 2^15 in fp16), the tile's maximum is taken in the same
+        // pass, and a reference that grew by more than 2^8 is applied at the
+        // start of the next tile (O and l rescaled there, before this stage's
+        // next P V). The k-scale loads then overlap the exp2 work instead of
+        // preceding it. A row whose maximum exceeds the reference by more than
+        // that bound redoes the tile in two passes from S, still in TMEM.
+        constexpr bool OP = !L::DBS;
+        // fp16 P holds values below 2^16, bf16 P those below 2^128
+        constexpr float kRedo = VBF16 ? 64.f : 15.f;
         bool one = false;
         if constexpr (OP) {
           if (__any_sync(0xffffffffu, m_pend > m)) {  // the reference grew on the last tile
@@ -1102,7 +1104,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
                   unpack2(fadd2(pack2(t[2 * h2], t[2 * h2 + 1]), nmo), t0, t1);
                   const float p0 = ex2(t0), p1 = ex2(t1);
                   lsum[h2] = fadd2(lsum[h2], pack2(p0, p1));
-                  sv[(c >> 1) + h2] = cvt_bf16x2(p0, p1);
+                  sv[(c >> 1) + h2] = VBF16 ? cvt_bf16x2(p0, p1) : cvt_f16x2(p0, p1);
                 }
               }
             } else {
@@ -1122,13 +1124,13 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
                 unpack2(ffma2(pack2(u[2 * q], u[2 * q + 1]), cq2o, nmo), t0, t1);
                 const float p0 = ex2(t0), p1 = ex2(t1);
                 lsum[q & 1] = fadd2(lsum[q & 1], pack2(p0, p1));
-                sv[(c >> 1) + q] = cvt_bf16x2(p0, p1);
+                sv[(c >> 1) + q] = VBF16 ? cvt_bf16x2(p0, p1) : cvt_f16x2(p0, p1);
               }
             }
             }
             const float rmo = fmaxf(fmaxf(mo[0], mo[1]), fmaxf(mo[2], mo[3]));
             const float tmx = fast ? cq * rmo : rmo;
-            if (__any_sync(0xffffffffu, tmx > m + 64.f)) {
+            if (__any_sync(0xffffffffu, tmx > m + kRedo)) {
               one = false;  // redo exactly: S is still in TMEM
               if constexpr (BN == 128) tmem_ld128(tS, sv);
               else tmem_ld64(tS, sv);
