@@ -41,8 +41,8 @@ PAGE_SPLIT_MS = 11.05
 # SHA-256 of the kernel sources it was taken on. A launch's traffic is scaled
 # from it per head, with the key-proportional part scaled by the keys of the
 # launch. When the kernel sources change, the figure no longer applies.
-ATTN_TRAFFIC = {"source_sha256": "3e9c22877fd961c236d1f7416637c5b33b9ece6aa36f09dd2a35746390f79eb1",
-                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 246484480.0}
+ATTN_TRAFFIC = {"source_sha256": "8bf02c4e7352cc98f9e16bc107a4180be5cfe93b121c2fd8e71b6142e102aa7c",
+                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 246631680.0}
 
 
 def attn_source_sha():
