@@ -1059,9 +1059,10 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         // 2^64 in bf16, 2^15 in fp16), the tile's maximum is taken in the same
         // pass, and a reference that grew by more than 2^8 is applied at the
         // start of the next tile (O and l rescaled there, before this stage's
-        // next P V). The k-scale loads then overlap the exp2 work instead of
-        // preceding it. A row whose maximum exceeds the reference by more than
-        // that bound redoes the tile in two passes from S, still in TMEM.
+        // next P V; that stage's previous P V has completed by then). This
+        // saves the separate pass over the row for its maximum. A row whose
+        // maximum exceeds the reference by more than that bound redoes the tile
+        // in two passes from S, still in TMEM.
         constexpr bool OP = !L::DBS;
         // fp16 P holds values below 2^16, bf16 P those below 2^128
         constexpr float kRedo = VBF16 ? 64.f : 15.f;
