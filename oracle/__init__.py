@@ -5,9 +5,11 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
 library never calls, links or falls back to this code, and this code shares
 nothing with it: no kernels, headers, tables or helpers.
 
-See ``oracle/ia_oracle.py`` for the functions and the passages they follow.
+The arithmetic is plain C++ in ``oracle/ia_oracle.cpp`` (float64 attention,
+IEEE float32 quantiser decisions, exact sums, ``std::thread`` over heads and
+rows); ``oracle/ia_oracle.py`` marshals numpy arrays into it.
 """
 from .ia_oracle import (  # noqa: F401
-    k_mean, quantize, row_validity, dequantize, attention, exact_attention, merge,
-    quantize_and_attend, qk_prologue, round_to_16bit, PARITY_STATUS,
+    k_mean, quantize, row_validity, attention, exact_attention, merge, quantize_and_attend,
+    qk_prologue, round_to_16bit, exact_sum, set_threads, hardware_threads, PARITY_STATUS,
 )

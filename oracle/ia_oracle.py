@@ -1,11 +1,15 @@
 """Plain, slow CPU oracle of INT8-QK quantised attention. TEST INFRASTRUCTURE ONLY.
 
-Nothing in the product path imports this module; only the tests, the smoke
-check and the benchmark's CPU-baseline leg do. It shares no code with the CUDA
-library. Arrays are numpy; 16-bit inputs arrive as float32 arrays holding the
-exact bf16/fp16 values.
+The arithmetic is C++ (``oracle/ia_oracle.cpp``, built by
+``oracle/build_oracle.py`` with g++ into ``oracle/_build/libia_oracle.so``, on
+first use if needed); this module marshals numpy arrays into it and composes
+the steps. Nothing in the product path imports this module; only the tests,
+the smoke check and the benchmark's CPU-baseline legs do. It shares no code
+with the CUDA library. Arrays are numpy; 16-bit inputs arrive as float32
+arrays holding the exact bf16/fp16 values.
 
-Sources (page title, then the part of the page):
+Sources (page title, then the part of the page), restated at each C++
+function with the step it defines:
 
 * [FastVideo] "minimax_h3_sparse_int8" (FastVideo API page): the module
   description (per-token Q/K scales, K centring as a softmax-invariant shift,
@@ -17,27 +21,21 @@ Sources (page title, then the part of the page):
   entry per 64-row tile).
 * [Passthrough] "Feature Request: Direct int8 Q/K passthrough between Comfy
   Kitchen and SageAttention": section 2.1 (mean_seq, quant_qk_int8, then an
-  int8 QK product with a 16-bit PV) and section 3.1 (per-block int8 Q/K with
-  fp32 scales).
+  int8 QK product with a 16-bit PV), section 3.1 (per-block int8 Q/K with
+  fp32 scales) and the maintainer's reply (RMSNorm + RoPE on the 16-bit
+  values before quantization).
 * [model-kernels] "[attention-int8] Multiple build issues and numerical
   accuracy problem": the maintainer's point 1 (symmetric range [-127, 127]).
 * [comfy-kitchen] "int8_attention: masked path costs ~1.8x unmasked, and a
   request for optional return_lse": the opening paragraph (one additive bias
-  per key, shape [1,1,1,K]) and "Question 2" (merging two partial softmaxes
-  exactly through their log-sum-exp).
-* [comfy-kitchen] "The measurement" (the attn_mask forms callers pass: fp32,
-  bf16 and fp16 additive masks and bool masks, shaped [1,1,1,K] or expanded
-  to [1,1,Q,K]) and the repro (the bool mask is True where the key's weight
-  is kept).
-* [Passthrough], the maintainer's reply: RMSNorm + RoPE sit between the
-  projections and attention in modern DiTs (``apply_rope``, ``rms_rope``,
-  ``rms_rope_split_half``) and must run on the 16-bit values.
+  per key, shape [1,1,1,K]), "The measurement" (fp32, bf16 and fp16 additive
+  masks and bool masks, [1,1,1,K] or expanded to [1,1,Q,K]), "Question 2"
+  (merging two partial softmaxes exactly through their log-sum-exp) and the
+  repro (the bool mask is True where the key's weight is kept).
 * [FlyDSL] "Add optional forward LSE output": "Summary" (LSE = sm_scale*m +
   ln l, natural log), "Kernel implementation" (-inf for fully masked rows;
   split-K combine from the combined maximum and denominator) and "Public API"
   (fp32 ``[B,H,Sq]``, includes the softmax scale).
-
-Readings where the pages leave a step open are stated at each function.
 
 Parity status: every function below is pinned by ``tests/test_oracle_*.py``
 against closed forms, brute force, library routines or invariants; none is
@@ -45,12 +43,14 @@ against closed forms, brute force, library routines or invariants; none is
 """
 from __future__ import annotations
 
-import math
+import ctypes
+import os
 
 import numpy as np
 
+from . import build_oracle
+
 TILE = 64
-QMAX = np.float32(127.0)
 
 PARITY_STATUS = {
     "k_mean": "pinned (exact rational sum on small inputs, translation property)",
@@ -59,8 +59,65 @@ PARITY_STATUS = {
     "attention(mask=)": "pinned (brute-force masked softmax, bool = 0/-inf, row shifts)",
     "exact_attention": "pinned (torch fp64 SDPA, centring invariance)",
     "merge": "pinned (split of one softmax equals the whole)",
-    "qk_prologue": "pinned (torch rms_norm, complex rotation, pair norms, layout permutation)",
+    "qk_prologue": "pinned (torch rms_norm, exact rational sum of squares, complex rotation, "
+                   "pair norms, layout permutation, library 16-bit rounding)",
 }
+
+_lib = None
+_F32P = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+_F64P = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+_I8P = np.ctypeslib.ndpointer(dtype=np.int8, flags="C_CONTIGUOUS")
+_VP = ctypes.c_void_p
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(build_oracle.build())
+        i32, i64, f32, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_double
+        L.or_k_mean.argtypes = [_F32P, i32, i32, i32, i32, _VP, _F32P, i32]
+        L.or_quantize.argtypes = [_F32P, i32, i32, i32, i32, _VP, i32, _VP, _I8P, _F32P, i32]
+        L.or_qk_prologue.argtypes = [_F32P, i32, i32, i32, i32, i32, _VP, f32, i32, _VP, _VP,
+                                     i32, _F32P, i32]
+        L.or_attention.argtypes = [i32, i32, i32, i32, i32, _VP, i32, _VP, _VP, i32, _VP, i32,
+                                   _VP, i32, f64, _VP, _VP, i32, _VP, _VP, _VP, _VP, i32, _VP,
+                                   i64, _F64P, _F64P, i32]
+        L.or_merge.argtypes = [_F64P, _F64P, _F64P, _F64P, i64, i32, _F64P, _F64P]
+        L.or_exact_sum.argtypes = [_F64P, i64, i32]
+        L.or_exact_sum.restype = f64
+        L.or_hardware_threads.restype = i32
+        _lib = L
+    return _lib
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+_THREADS = 0  # 0: every hardware thread
+
+
+def set_threads(n: int) -> None:
+    """Threads the oracle's C++ loops use (0: all hardware threads)."""
+    global _THREADS
+    _THREADS = int(n)
+
+
+def hardware_threads() -> int:
+    """std::thread::hardware_concurrency() as the oracle library sees it."""
+    return int(_load().or_hardware_threads())
+
+
+def exact_sum(x, bits: int = 53) -> float:
+    """The exact sum of the float64 values ``x`` rounded once to nearest-even
+    binary64 (bits=53) or binary32 (bits=24): the summation the K mean and
+    the RMSNorm sum of squares are defined with."""
+    x = _c(x, np.float64).reshape(-1)
+    return float(_load().or_exact_sum(x, x.size, int(bits)))
 
 
 # --------------------------------------------------------------------------- #
@@ -81,92 +138,63 @@ def row_validity(S: int, kv_valid) -> np.ndarray:
     return (s % TILE) < vbs[s // TILE]
 
 
+def _vbs(kv_valid, S):
+    if kv_valid is None:
+        return None
+    v = _c(kv_valid, np.int32).reshape(-1)
+    assert S == TILE * v.size
+    return v
+
+
 def k_mean(k: np.ndarray, kv_valid=None) -> np.ndarray:
-    """K's mean over the sequence, fp32 ``[B,H,D]``.
+    """K's mean over the sequence, fp32 ``[B,H,D]`` (``or_k_mean``).
 
     [FastVideo] ``sparse_sm89_attention``: the sum of K over the sequence
-    divided by the number of valid rows (tile pads are zero, so the sum over
-    all rows is the sum over the valid ones). [Passthrough] 2.1 calls this
-    step mean_seq (smooth_k).
-
-    Reading: the page sums in fp32 in an unspecified order. Here the sum is
-    exact (``math.fsum`` gives the exact sum rounded once to float64), divided
-    by the count in float64 and rounded once to float32.
+    divided by the number of valid rows. Reading: the sum is exact, rounded
+    once to float64, divided by the count in float64, rounded once to fp32.
     """
-    B, H, S, D = k.shape
-    valid = row_validity(S, kv_valid)
-    n = int(valid.sum())
+    kk = _c(k, np.float32)
+    B, H, S, D = kk.shape
+    vbs = _vbs(kv_valid, S)
     mu = np.zeros((B, H, D), dtype=np.float32)
-    kv = np.asarray(k, dtype=np.float64)
-    for b in range(B):
-        for h in range(H):
-            for d in range(D):
-                col = kv[b, h, valid, d]
-                total = math.fsum(col.tolist())
-                mu[b, h, d] = np.float32(total / max(n, 1))
+    _load().or_k_mean(kk, B, H, S, D, _ptr(vbs), mu, _THREADS)
     return mu
 
 
 def quantize(x: np.ndarray, mu: np.ndarray | None = None, granularity: str = "token",
              kv_valid=None):
-    """Symmetric INT8 quantisation of Q or K.
+    """Symmetric INT8 quantisation of Q or K (``or_quantize``).
 
     Returns (codes int8 ``[B,H,S,D]``, scales fp32 ``[B,H,S]`` per token or
-    ``[B,H,ceil(S/64)]`` per 64-row block).
-
-    Steps, per row (per token) or per 64-row block:
-      1. centre: x' = fp32(x - mu) when ``mu`` is given (K only)
-         [FastVideo] module description, K centring;
-      2. amax = max |x'| over the row or block (exact);
-      3. scale = fp32(amax / 127); codes = round-half-even(fp32(x' * fp32(127 /
-         amax))) clamped to [-127, 127] -- symmetric range, [model-kernels]
-         maintainer point 1; per-token scales [FastVideo]; per-block scales
-         [Passthrough] 3.1.
-      4. amax == 0 gives codes 0 and scale 0. Rows past the validity vector
-         are not data: codes 0, and they do not enter a block's amax; a
-         per-token scale of such a row is 0.
-
-    Reading: the pages fix neither the rounding mode nor divide versus
-    reciprocal. This uses round-half-to-even of the product with the
-    correctly rounded fp32 reciprocal 127/amax.
+    ``[B,H,ceil(S/64)]`` per 64-row block). Per row or 64-row block: x' =
+    fp32(x - mu) (K only); amax = max |x'|; scale = fp32(amax / 127); codes =
+    round-half-even(fp32(x' * fp32(127 / amax))) clamped to [-127, 127];
+    amax = 0 gives codes 0, scale 0; rows past the validity vector are not
+    data ([FastVideo]; [model-kernels] point 1; [Passthrough] 3.1).
     """
-    B, H, S, D = x.shape
-    xc = np.asarray(x, dtype=np.float32)
-    if mu is not None:
-        xc = (xc - np.asarray(mu, dtype=np.float32)[:, :, None, :]).astype(np.float32)
-    valid = row_validity(S, kv_valid)
-    xc = np.where(valid[None, None, :, None], xc, np.float32(0)).astype(np.float32)
-    absx = np.abs(xc)
-    if granularity == "token":
-        amax = absx.max(axis=3)                                   # [B,H,S]
-        amax_rows = amax
-    elif granularity == "block64":
-        nb = -(-S // TILE)
-        amax = np.zeros((B, H, nb), dtype=np.float32)
-        for t in range(nb):
-            amax[:, :, t] = absx[:, :, t * TILE:(t + 1) * TILE, :].max(axis=(2, 3))
-        amax_rows = np.repeat(amax, TILE, axis=2)[:, :, :S]
-    else:
+    xx = _c(x, np.float32)
+    B, H, S, D = xx.shape
+    if granularity not in ("token", "block64"):
         raise ValueError(granularity)
-    nz = amax > 0
-    safe = np.where(nz, amax, np.float32(1)).astype(np.float32)
-    scale = np.where(nz, (safe / QMAX).astype(np.float32), np.float32(0)).astype(np.float32)
-    nz_rows = amax_rows > 0
-    safe_rows = np.where(nz_rows, amax_rows, np.float32(1)).astype(np.float32)
-    inv_rows = (QMAX / safe_rows).astype(np.float32)              # fp32(127 / amax)
-    prod = (xc * inv_rows[..., None]).astype(np.float32)         # fp32 product
-    codes = np.clip(np.rint(prod), -127, 127)
-    codes = np.where(nz_rows[..., None], codes, 0).astype(np.int8)
-    return codes, scale
+    m = None if mu is None else _c(mu, np.float32).reshape(B, H, D)
+    vbs = _vbs(kv_valid, S)
+    nb = S if granularity == "token" else -(-S // TILE)
+    codes = np.zeros((B, H, S, D), dtype=np.int8)
+    scales = np.zeros((B, H, nb), dtype=np.float32)
+    _load().or_quantize(xx, B, H, S, D, _ptr(m), 0 if granularity == "token" else 1, _ptr(vbs),
+                        codes, scales, _THREADS)
+    return codes, scales
 
 
 def round_to_16bit(x: np.ndarray, dtype: str) -> np.ndarray:
     """Round fp32 values to bf16 or fp16 (round-half-to-even) and return the
-    rounded values as float32 (exact). torch's dtype conversion is the library
-    routine used for bf16; numpy's float16 for fp16."""
+    rounded values as float32 (exact). A library routine: torch's dtype
+    conversion for bf16, numpy's float16 for fp16. The tests build 16-bit
+    inputs with it and pin the C++ rounding inside :func:`qk_prologue` to it."""
     x = np.asarray(x, dtype=np.float32)
     if dtype == "fp16":
-        return x.astype(np.float16).astype(np.float32)
+        with np.errstate(over="ignore"):  # values past the fp16 range become inf, as they should
+            return x.astype(np.float16).astype(np.float32)
     import torch
     return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).float().numpy()
 
@@ -174,198 +202,125 @@ def round_to_16bit(x: np.ndarray, dtype: str) -> np.ndarray:
 def qk_prologue(x: np.ndarray, *, dtype: str, norm_weight=None, eps: float = 1e-6,
                 rope: str | None = None, cos=None, sin=None, pos0: int = 0) -> np.ndarray:
     """RMSNorm then rotary embedding of each row of Q or K, rounded to the
-    16-bit type: the activations the unfused path hands to attention.
-
-    [Passthrough] maintainer's reply: in modern DiTs the projections go
-    through RMSNorm + RoPE before attention (``apply_rope``, ``rms_rope``,
-    ``rms_rope_split_half``), and RoPE rotates channel pairs, so it has to run
-    on the 16-bit values before they are quantized.
+    16-bit type (``or_qk_prologue``): the activations the unfused path hands
+    to attention ([Passthrough] maintainer's reply).
 
     Reading (the page gives names, not formulas), per row x of D values:
-      1. RMSNorm (when ``norm_weight`` is given): ss = the fp32 sum of the
-         squares x_d^2 (each exact in fp32 for 16-bit x) in a fixed order --
-         the squares of each 8 consecutive channels summed in index order,
-         then the D/8 partial sums added pairwise, t with t + n/2, until one
-         remains; ms = fp32(ss / D); r = fp32(1 / fp32(sqrt(fp32(ms + eps))));
-         y_d = fp32(fp32(x_d * r) * w_d). All fp32 steps are correctly rounded.
-         The order is the one the GPU kernels use (the pages fix none), so the
-         16-bit results, and the codes decided from them, agree bit for bit.
-      2. RoPE (when ``rope`` is "interleaved" or "split_half"): pair i is
-         (y[2i], y[2i+1]) or (y[i], y[i + D/2]); with c = cos[p, i],
-         s = sin[p, i] for the row's position p = pos0 + row:
-         a' = fp32(fp32(a c) - fp32(b s)), b' = fp32(fp32(a s) + fp32(b c)),
-         the rotation of (a, b) by the angle whose cosine and sine are given.
-      3. one rounding to the 16-bit type.
-    ``cos`` / ``sin`` are fp32 ``[P, D/2]`` tables. Returns float32 holding
-    16-bit values, same shape as ``x``.
+    ss = the exact sum of x_d^2 rounded once to fp32; ms = fp32(ss / D);
+    r = fp32(1 / fp32(sqrt(fp32(ms + eps)))); y_d = fp32(fp32(x_d r) w_d);
+    then pair i = (y[2i], y[2i+1]) ("interleaved") or (y[i], y[i + D/2])
+    ("split_half") is rotated: a' = fp32(fp32(a c) - fp32(b s)), b' =
+    fp32(fp32(a s) + fp32(b c)) with c = cos[p, i], s = sin[p, i] at position
+    p = pos0 + row; one rounding to the 16-bit type at the end. ``cos`` /
+    ``sin`` are fp32 ``[P, D/2]``. Returns float32 holding 16-bit values.
     """
-    B, H, S, D = x.shape
-    y = np.asarray(x, dtype=np.float32).copy()
-    if norm_weight is not None:
-        w = np.asarray(norm_weight, dtype=np.float32)
-        sq = (y * y).astype(np.float32)                                  # exact squares
-        part = sq[..., 0::8].copy()                                      # [B,H,S,D/8]
-        for j in range(1, 8):
-            part = (part + sq[..., j::8]).astype(np.float32)             # index order
-        n = D // 8
-        while n > 1:
-            half = n // 2
-            part = (part[..., :half] + part[..., half:n]).astype(np.float32)
-            n = half
-        ss = part[..., 0]
-        ms = (ss / np.float32(D)).astype(np.float32)
-        rr = (np.float32(1) / np.sqrt((ms + np.float32(eps)).astype(np.float32))).astype(np.float32)
-        y = ((y * rr[..., None]).astype(np.float32) * w).astype(np.float32)
-    if rope is not None:
-        c = np.asarray(cos, dtype=np.float32)[pos0:pos0 + S]        # [S, D/2]
-        sn = np.asarray(sin, dtype=np.float32)[pos0:pos0 + S]
-        if rope == "interleaved":
-            a, bb = y[..., 0::2], y[..., 1::2]
-        elif rope == "split_half":
-            a, bb = y[..., :D // 2], y[..., D // 2:]
-        else:
-            raise ValueError(rope)
-        a2 = ((a * c).astype(np.float32) - (bb * sn).astype(np.float32)).astype(np.float32)
-        b2 = ((a * sn).astype(np.float32) + (bb * c).astype(np.float32)).astype(np.float32)
-        y = np.empty_like(y)
-        if rope == "interleaved":
-            y[..., 0::2], y[..., 1::2] = a2, b2
-        else:
-            y[..., :D // 2], y[..., D // 2:] = a2, b2
-    return round_to_16bit(y, dtype)
-
-
-def dequantize(codes: np.ndarray, scale: np.ndarray, granularity: str) -> np.ndarray:
-    """code * scale in float64, ``[B,H,S,D]``."""
-    S = codes.shape[2]
-    if granularity == "token":
-        s = np.asarray(scale, dtype=np.float64)
-    else:
-        s = np.repeat(np.asarray(scale, dtype=np.float64), TILE, axis=2)[:, :, :S]
-    return codes.astype(np.float64) * s[..., None]
+    xx = _c(x, np.float32)
+    B, H, S, D = xx.shape
+    w = None if norm_weight is None else _c(norm_weight, np.float32).reshape(D)
+    code = {None: 0, "none": 0, "interleaved": 1, "split_half": 2}[rope]
+    c = s = None
+    if code:
+        c = _c(cos, np.float32)
+        s = _c(sin, np.float32)
+        assert c.shape == s.shape and c.shape[1] == D // 2 and pos0 + S <= c.shape[0]
+    y = np.empty_like(xx)
+    _load().or_qk_prologue(xx, B, H, S, D, 0 if dtype == "bf16" else 1, _ptr(w), float(eps),
+                           code, _ptr(c), _ptr(s), int(pos0), y, _THREADS)
+    return y
 
 
 # --------------------------------------------------------------------------- #
 # Attention
 # --------------------------------------------------------------------------- #
 
-def _softmax_rows(s: np.ndarray, v: np.ndarray):
-    """Per-row softmax of the logits ``s`` [n, Sk] (natural log units) applied to
-    ``v`` [Sk, D]. Returns (O [n, D], LSE [n]). A row whose logits are all -inf
-    gives O = 0 and LSE = -inf ([FlyDSL] "Kernel implementation")."""
-    m = s.max(axis=1)
-    dead = ~np.isfinite(m)
-    m_safe = np.where(dead, 0.0, m)
-    p = np.exp(s - m_safe[:, None])
-    p[dead] = 0.0
-    l = p.sum(axis=1)
-    o = p @ v
-    with np.errstate(divide="ignore", invalid="ignore"):
-        o = np.where(dead[:, None], 0.0, o / np.where(dead, 1.0, l)[:, None])
-        lse = np.where(dead, -np.inf, m_safe + np.log(np.where(dead, 1.0, l)))
-    return o, lse
-
-
-def _key_mask(b, h, rows, Sk, block_mask, kv_valid):
-    """Boolean [len(rows), Sk]: key j is visible to query row i."""
-    vis = np.ones((len(rows), Sk), dtype=bool)
-    if block_mask is not None:
-        bm = np.asarray(block_mask)[b, h]                        # [Tq, Tk]
-        tiles = bm[np.asarray(rows) // TILE]                     # [n, Tk]
-        vis &= np.repeat(tiles, TILE, axis=1)[:, :Sk]
-    if kv_valid is not None:
-        vis &= row_validity(Sk, kv_valid)[None, :]
-    return vis
-
-
-def _mask_rows(mask, B, H, Sq, Sk, b, h, rows):
-    """Rows ``rows`` of head (b, h) of a general attention mask.
-
-    ``mask`` is broadcastable to [B,H,Sq,Sk] (numpy broadcasting, as the
-    [1,1,1,K] and [1,1,Q,K] views of [comfy-kitchen] "The measurement"). A
-    float mask holds additive logit offsets (the exact bf16/fp16/fp32 values,
-    widened to float64); a bool mask keeps a key where it is True and
-    excludes it (logit -inf) where it is False.
-    Returns ("add", float64 [n, Sk]) or ("keep", bool [n, Sk])."""
+def _mask_args(mask, B, H, Sq, Sk):
+    """A general attention mask broadcastable to [B,H,Sq,Sk] (the [1,1,1,K] and
+    [1,1,Q,K] views of [comfy-kitchen] "The measurement") as the C++ call
+    takes it: (kind, array, element strides with 0 on broadcast dims). A float
+    mask holds additive logit offsets (the exact bf16/fp16/fp32 values, widened
+    to float64); a bool mask keeps a key where it is True."""
+    if mask is None:
+        return 0, None, None
     m = np.asarray(mask)
     while m.ndim < 4:
         m = m[None]
-    full = np.broadcast_to(m, (B, H, Sq, Sk))[b, h][np.asarray(rows)]
-    if full.dtype == np.bool_:
-        return "keep", full
-    return "add", full.astype(np.float64)
+    if m.dtype == np.bool_:
+        kind, arr = 2, _c(m, np.uint8)
+    else:
+        kind, arr = 1, _c(m.astype(np.float64), np.float64)
+    full = (B, H, Sq, Sk)
+    st = []
+    for ax in range(4):
+        if arr.shape[ax] == full[ax]:
+            st.append(arr.strides[ax] // arr.itemsize)
+        elif arr.shape[ax] == 1:
+            st.append(0)
+        else:
+            raise ValueError(f"mask shape {m.shape} does not broadcast to {full}")
+    return kind, arr, np.array(st, dtype=np.int64)
 
 
-def _apply_mask(s, kind_rows):
-    kind, mr = kind_rows
-    if kind == "keep":
-        return np.where(mr, s, -np.inf)
-    return s + mr
+def _values(a):
+    """A float operand as the C++ call takes it: (kind, array); float32 stays
+    float32 (16-bit values are exact in it), anything else becomes float64."""
+    a = np.asarray(a)
+    if a.dtype == np.float32:
+        return 1, _c(a, np.float32)
+    return 2, _c(a, np.float64)
+
+
+def _attend(q, q_kind, q_scale, k, k_kind, k_scale, v, *, sm_scale, bias, block_mask, kv_valid,
+            v_scale, granularity, rows, mask, pad_query):
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    if sm_scale is None:
+        sm_scale = D ** -0.5
+    rows = np.arange(Sq, dtype=np.int64) if rows is None else _c(rows, np.int64).reshape(-1)
+    v_kind, vv = _values(v)
+    bias64 = None if bias is None else _c(bias, np.float64).reshape(-1)
+    assert bias64 is None or bias64.size == Sk
+    bm = None if block_mask is None else _c(block_mask, np.uint8)
+    vbs = _vbs(kv_valid, Sk)
+    vs = None if v_scale is None else _c(v_scale, np.float64).reshape(H, D)
+    kind, marr, mst = _mask_args(mask, B, H, Sq, Sk)
+    out = np.zeros((B, H, rows.size, D), dtype=np.float64)
+    lse = np.zeros((B, H, rows.size), dtype=np.float64)
+    if rows.size == 0:
+        return out, lse
+    _load().or_attention(B, H, Sq, Sk, D, _ptr(q), q_kind, _ptr(q_scale), _ptr(k), k_kind,
+                         _ptr(k_scale), 0 if granularity == "token" else 1, _ptr(vv), v_kind,
+                         float(sm_scale), _ptr(bias64), _ptr(marr), kind, _ptr(mst), _ptr(bm),
+                         _ptr(vbs), _ptr(vs), 1 if pad_query else 0, _ptr(rows), rows.size, out,
+                         lse, _THREADS)
+    return out, lse
 
 
 def attention(q_codes, q_scale, k_codes, k_scale, v, *, sm_scale=None, bias=None,
               block_mask=None, kv_valid=None, v_scale=None, granularity="token",
               rows=None, row_chunk=256, mask=None):
-    """Same-quantisation FP64 attention reference.
+    """Same-quantisation FP64 attention reference (``or_attention``).
 
     q_hat = code * scale and k_hat likewise (float64);
-    s_ij = sm_scale * <q_hat_i, k_hat_j> + bias_j, with s_ij = -inf where the
-    tile-64 block mask drops key tile j//64 for query tile i//64 or key row j
-    lies past the validity vector;
-    O_i = v_scale (*) sum_j softmax_j(s_i.) v_j;  LSE_i = m_i + ln sum_j e^(s_ij - m_i).
+    s_ij = sm_scale * <q_hat_i, k_hat_j> + bias_j (+ a float mask), with
+    s_ij = -inf where the tile-64 block mask drops key tile j//64 for query
+    tile i//64, key row j lies past the validity vector or a bool mask is
+    False; O_i = v_scale (*) sum_j softmax_j(s_i.) v_j; LSE_i = m_i +
+    ln sum_j e^(s_ij - m_i). A fully masked row gives O = 0, LSE = -inf.
 
-    [Passthrough] 2.1 (int8 QK, 16-bit PV); [FastVideo] module description
-    (FP32 accumulation, V scale per head and channel applied once at the end,
-    masked partial key tiles) and ``sparse_sm89_attention`` (mask layout);
-    [comfy-kitchen] opening paragraph (bias [1,1,1,K]); [FlyDSL] "Summary" and
-    "Public API" (LSE in natural log including the softmax scale).
-
-    Reading: the bias is added after the softmax scale, as an additive
-    ``attn_mask`` is in SDPA, which [comfy-kitchen] compares against.
-
-    Reading: with a validity vector and Sq == Sk, query rows past it are
-    padding; they give O = 0 and LSE = -inf (the pages leave them undefined).
-
-    ``mask`` is the general form of the bias (see :func:`_mask_rows`): a float
-    mask broadcastable to [B,H,Sq,Sk] is added where ``bias`` would be; a bool
-    mask excludes the keys where it is False.
-
-    ``rows`` optionally restricts the query rows (a 1-D index array); rows are
-    independent, so they are processed in chunks of ``row_chunk``.
+    Readings: the bias and masks enter after the softmax scale (SDPA's
+    additive ``attn_mask``, which [comfy-kitchen] compares against); with a
+    validity vector and Sq == Sk, query rows past it are padding and give
+    O = 0 and LSE = -inf. ``rows`` optionally restricts the query rows (a
+    1-D index array). ``row_chunk`` is accepted for compatibility and unused.
     Returns (O float64 [B,H,n,D], LSE float64 [B,H,n]).
     """
-    B, H, Sq, D = q_codes.shape
-    Sk = k_codes.shape[2]
-    if sm_scale is None:
-        sm_scale = D ** -0.5
-    qh = dequantize(q_codes, q_scale, granularity)
-    kh = dequantize(k_codes, k_scale, granularity)
-    vv = np.asarray(v, dtype=np.float64)
-    rows = np.arange(Sq) if rows is None else np.asarray(rows)
-    out = np.zeros((B, H, len(rows), D))
-    lse = np.zeros((B, H, len(rows)))
-    bias64 = None if bias is None else np.asarray(bias, dtype=np.float64).reshape(-1)
-    for b in range(B):
-        for h in range(H):
-            for c0 in range(0, len(rows), row_chunk):
-                r = rows[c0:c0 + row_chunk]
-                s = sm_scale * (qh[b, h, r] @ kh[b, h].T)
-                if bias64 is not None:
-                    s = s + bias64[None, :]
-                if mask is not None:
-                    s = _apply_mask(s, _mask_rows(mask, B, H, Sq, Sk, b, h, r))
-                vis = _key_mask(b, h, r, Sk, block_mask, kv_valid)
-                s = np.where(vis, s, -np.inf)
-                o, l = _softmax_rows(s, vv[b, h])
-                if v_scale is not None:
-                    o = o * np.asarray(v_scale, dtype=np.float64)[h][None, :]
-                if kv_valid is not None and Sq == Sk:
-                    pad = ~row_validity(Sq, kv_valid)[r]
-                    o[pad] = 0.0
-                    l[pad] = -np.inf
-                out[b, h, c0:c0 + len(r)] = o
-                lse[b, h, c0:c0 + len(r)] = l
-    return out, lse
+    qc = _c(q_codes, np.int8)
+    kc = _c(k_codes, np.int8)
+    Sq, Sk = qc.shape[2], kc.shape[2]
+    return _attend(qc, 0, _c(q_scale, np.float32), kc, 0, _c(k_scale, np.float32), v,
+                   sm_scale=sm_scale, bias=bias, block_mask=block_mask, kv_valid=kv_valid,
+                   v_scale=v_scale, granularity=granularity, rows=rows, mask=mask,
+                   pad_query=kv_valid is not None and Sq == Sk)
 
 
 def exact_attention(q, k, v, *, sm_scale=None, bias=None, block_mask=None, kv_valid=None,
@@ -373,60 +328,31 @@ def exact_attention(q, k, v, *, sm_scale=None, bias=None, block_mask=None, kv_va
     """Textbook softmax attention in float64 on the unquantised inputs (no
     centring, no quantisation): the yardstick the INT8 path is measured
     against ([model-kernels] "5. Numerical accuracy" compares against SDPA).
-    Same masking, bias, V scale and LSE conventions as :func:`attention`."""
-    B, H, Sq, D = q.shape
-    Sk = k.shape[2]
-    if sm_scale is None:
-        sm_scale = D ** -0.5
-    qq = np.asarray(q, dtype=np.float64)
-    kk = np.asarray(k, dtype=np.float64)
-    vv = np.asarray(v, dtype=np.float64)
-    rows = np.arange(Sq) if rows is None else np.asarray(rows)
-    out = np.zeros((B, H, len(rows), D))
-    lse = np.zeros((B, H, len(rows)))
-    bias64 = None if bias is None else np.asarray(bias, dtype=np.float64).reshape(-1)
-    for b in range(B):
-        for h in range(H):
-            for c0 in range(0, len(rows), row_chunk):
-                r = rows[c0:c0 + row_chunk]
-                s = sm_scale * (qq[b, h, r] @ kk[b, h].T)
-                if bias64 is not None:
-                    s = s + bias64[None, :]
-                if mask is not None:
-                    s = _apply_mask(s, _mask_rows(mask, B, H, Sq, Sk, b, h, r))
-                vis = _key_mask(b, h, r, Sk, block_mask, kv_valid)
-                s = np.where(vis, s, -np.inf)
-                o, l = _softmax_rows(s, vv[b, h])
-                if v_scale is not None:
-                    o = o * np.asarray(v_scale, dtype=np.float64)[h][None, :]
-                out[b, h, c0:c0 + len(r)] = o
-                lse[b, h, c0:c0 + len(r)] = l
-    return out, lse
+    Same masking, bias, V scale and LSE conventions as :func:`attention`
+    (padding query rows are not zeroed here)."""
+    qk, qa = _values(q)
+    kk, ka = _values(k)
+    return _attend(qa, qk, None, ka, kk, None, v,
+                   sm_scale=sm_scale, bias=bias, block_mask=block_mask, kv_valid=kv_valid,
+                   v_scale=v_scale, granularity="token", rows=rows, mask=mask, pad_query=False)
 
 
 def merge(o1, lse1, o2, lse2):
-    """Exact merge of two partial softmax attentions over disjoint key sets.
-
-    M = max(L1, L2); w_k = e^(L_k - M); L = M + ln(w1 + w2);
-    O = (w1 O1 + w2 O2) / (w1 + w2); if both are -inf, O = 0 and L = -inf.
-    [comfy-kitchen] "Question 2"; [FlyDSL] "Kernel implementation" (split-K
-    combine from the combined maximum and denominator). float64.
-    """
-    l1 = np.asarray(lse1, dtype=np.float64)
-    l2 = np.asarray(lse2, dtype=np.float64)
-    o1 = np.asarray(o1, dtype=np.float64)
-    o2 = np.asarray(o2, dtype=np.float64)
-    m = np.maximum(l1, l2)
-    dead = ~np.isfinite(m)
-    ms = np.where(dead, 0.0, m)
-    w1 = np.where(np.isfinite(l1), np.exp(l1 - ms), 0.0)
-    w2 = np.where(np.isfinite(l2), np.exp(l2 - ms), 0.0)
-    den = w1 + w2
-    with np.errstate(divide="ignore", invalid="ignore"):
-        o = np.where(dead[..., None], 0.0,
-                     (w1[..., None] * o1 + w2[..., None] * o2) / np.where(dead, 1.0, den)[..., None])
-        lse = np.where(dead, -np.inf, ms + np.log(np.where(dead, 1.0, den)))
-    return o, lse
+    """Exact merge of two partial softmax attentions over disjoint key sets
+    (``or_merge``): M = max(L1, L2); w_k = e^(L_k - M); L = M + ln(w1 + w2);
+    O = (w1 O1 + w2 O2) / (w1 + w2); both -inf gives O = 0, L = -inf.
+    [comfy-kitchen] "Question 2"; [FlyDSL] "Kernel implementation". float64."""
+    a1 = _c(o1, np.float64)
+    a2 = _c(o2, np.float64)
+    b1 = _c(lse1, np.float64)
+    b2 = _c(lse2, np.float64)
+    D = a1.shape[-1]
+    n = b1.size
+    o = np.zeros_like(a1)
+    l = np.zeros_like(b1)
+    _load().or_merge(a1.reshape(n, D), b1.reshape(n), a2.reshape(n, D), b2.reshape(n), n, D,
+                     o.reshape(n, D), l.reshape(n))
+    return o, l
 
 
 def quantize_and_attend(q, k, v, *, granularity="token", center_k=True, kv_valid=None,

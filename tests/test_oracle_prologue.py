@@ -106,3 +106,63 @@ def test_prologue_path_close_to_exact_attention_on_normed_roped_inputs():
 
     oe, le = exact_attention(ref64(q, wq), ref64(k, wk), v)
     assert np.abs(o - oe).mean() < 1e-2
+
+
+def test_rmsnorm_uses_the_exact_sum_of_squares():
+    """The oracle's RMSNorm is the mathematics: the sum of squares exact,
+    rounded once to fp32, then r = 1/sqrt(ss/D + eps) and y = (x r) w in fp32
+    and one rounding to the 16-bit type, here written out with Python's exact
+    rationals for the sum. On thousands of random fp16 rows it must agree bit
+    for bit; a running fp32 sum (the GPU kernels' documented order) gives a
+    different 16-bit row on some of them, so the check tells the two apart."""
+    from fractions import Fraction
+    from kernel_order import prologue_kernel_order
+    D, n = 128, 4000
+    x = rnd16((1, 1, n, D), 17, "fp16", 2.0)
+    w = norm_weight(D, 18)
+    eps = np.float32(1e-6)
+    ss = np.array([np.float32(float(sum(Fraction(float(v)) ** 2 for v in row)))  # one rounding
+                   for row in x.reshape(n, D)], np.float32)
+    ms = (ss / np.float32(D)).astype(np.float32)
+    r = (np.float32(1) / np.sqrt((ms + eps).astype(np.float32))).astype(np.float32)
+    want = round_to_16bit(((x * r.reshape(1, 1, n, 1)).astype(np.float32) * w).astype(np.float32),
+                          "fp16")
+    got = qk_prologue(x, dtype="fp16", norm_weight=w, eps=1e-6)
+    assert np.array_equal(got, want)
+    kern = prologue_kernel_order(x, dtype="fp16", norm_weight=w, eps=1e-6)
+    assert np.any(kern != want)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_final_rounding_is_the_library_rounding(dtype):
+    """With neither norm nor rotation the prologue is its last step alone, the
+    rounding to the 16-bit type: it must equal torch's bf16 / numpy's fp16
+    conversion bit for bit, ties, subnormals and overflow included."""
+    rng = np.random.default_rng(13)
+    x = (rng.standard_normal(4096) * np.exp2(rng.integers(-30, 30, 4096))).astype(np.float32)
+    edge = np.array([0.0, -0.0, 65504.0, 65520.0, 7e4, 1e-8, 6.1e-5, 3e-38, 1e38, 3.4e38,
+                     1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11],
+                    np.float32)
+    x = np.concatenate([x, edge, -edge]).reshape(1, 1, -1, 1)
+    x = np.repeat(x, 2, axis=-1)                               # D = 2: one rotation pair, unused
+    got = qk_prologue(x, dtype=dtype)
+    want = round_to_16bit(x, dtype)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_exact_sum_against_rational_arithmetic():
+    """The exact summation the K mean and the RMSNorm use, against Python's
+    exact rational arithmetic: heavy cancellation, tiny and huge terms."""
+    from fractions import Fraction
+    from oracle import exact_sum
+    rng = np.random.default_rng(7)
+    for trial in range(20):
+        x = rng.standard_normal(300) * np.exp2(rng.integers(-60, 60, 300))
+        x = np.concatenate([x, -x[:150] * (1 + 2.0 ** -40), [2.0 ** -1074, 1e300, -1e300]])
+        want = float(sum((Fraction(float(v)) for v in x), Fraction(0)))  # correctly rounded
+        assert exact_sum(x, 53) == want
+    # binary32: integer sums below 2^53 are exact in float64, then rounded once
+    y = np.array([2.0 ** 24, 1.0, 1.0, 1.0], np.float64)
+    assert exact_sum(y, 24) == float(np.float32(2.0 ** 24 + 3))
+    assert exact_sum(np.array([2.0 ** 24, 1.0]), 24) == 2.0 ** 24     # tie to even
+    assert exact_sum(np.array([2.0 ** 24, 3.0]), 24) == 2.0 ** 24 + 4  # tie to even, upward
