@@ -37,8 +37,7 @@ PAGE_SPLIT_MS = 11.05
 
 # DRAM traffic of attn_fwd_kernel from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum) of the 16-head banded case (Sq 4096, Sk 33600,
-# unmasked), recorded in profiles/attn_fwd_banded_h16.md together with the
-# SHA-256 of the kernel sources it was taken on. A launch's traffic is scaled
+# unmasked), recorded with the SHA-256 of the kernel sources it was taken on. A launch's traffic is scaled
 # from it per head, with the key-proportional part scaled by the keys of the
 # launch. When the kernel sources change, the figure no longer applies.
 ATTN_TRAFFIC = {"source_sha256": "8bf02c4e7352cc98f9e16bc107a4180be5cfe93b121c2fd8e71b6142e102aa7c",
@@ -287,15 +286,19 @@ def run_profile(args):
     from workloads import WORKLOADS, make_inputs
 
     name = args.profile
-    wl = WORKLOADS["sparse" if name == "sparse" else "banded"]
+    wl = WORKLOADS[{"sparse": "sparse", "sdxl": "sdxl"}.get(name, "banded")]
     if args.heads:
         wl = wl.with_(H=args.heads)
     inp = make_inputs(wl, "cuda")
-    q8, qs, k8, ks = ia.quantize_qk(inp.q, inp.k, kv_valid=inp.kv_valid)
+    g = wl.granularity
+    q8, qs, k8, ks = ia.quantize_qk(inp.q, inp.k, kv_valid=inp.kv_valid, granularity=g)
     out, lse = ia.attention(q8, k8, qs, ks, inp.v, block_mask=inp.block_mask,
-                            kv_valid=inp.kv_valid, return_lse=True)
+                            kv_valid=inp.kv_valid, return_lse=True, granularity=g)
     o2, l2 = out.clone(), lse.clone()
     fns = {
+        # the head-dim-64 workload as the benchmark times it (default key split)
+        "sdxl": lambda: ia.attention(q8, k8, qs, ks, inp.v, out=out, lse=lse, return_lse=True,
+                                     granularity=g),
         "attention": lambda: ia.attention(q8, k8, qs, ks, inp.v, out=out, lse=lse, return_lse=True),
         "attention_bias": lambda: ia.attention(q8, k8, qs, ks, inp.v, bias=inp.bias, out=out,
                                                lse=lse, return_lse=True),
@@ -414,7 +417,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip timing the other four workloads")
     ap.add_argument("--profile", default=None,
-                    choices=["attention", "attention_bias", "quantize", "merge", "sparse"],
+                    choices=["attention", "attention_bias", "quantize", "merge", "sparse", "sdxl"],
                     help="run one kernel alone, --steps times after --warmup (for ncu)")
     ap.add_argument("--heads", type=int, default=None, help="heads of the --profile case")
     args = ap.parse_args()

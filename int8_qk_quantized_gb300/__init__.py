@@ -12,7 +12,6 @@ raises; there is no fallback implementation.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 
 import torch
@@ -478,7 +477,3 @@ def merge_lse_n(outs, lses, out=None, lse_out=None, stream=None):
 def device_status(stream=None):
     """Synchronise the stream and raise if a bounded device wait ran out."""
     _check(load_library().ia_device_status(_stream(stream)))
-
-
-def default_sm_scale(D: int) -> float:
-    return 1.0 / math.sqrt(D)

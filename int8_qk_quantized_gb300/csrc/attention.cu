@@ -135,8 +135,10 @@ struct Layout {
   // A CTA pair (PAIR) holds half of each key tile's K rows and half of V's
   // columns per CTA; the 256-row MMA reads the other halves from the peer.
   // One query stage (QS == 1): S is double-buffered in TMEM, so the QK^T of
-  // key tile j+1 runs while the softmax works on tile j; B_OF then counts the
-  // P V of every tile (the softmax waits on it before rescaling O).
+  // key tile j+1 runs while the softmax works on tile j; B_PVT then counts the
+  // P V of every tile (the softmax waits on it before rescaling O). B_OF is
+  // committed once, after the last P V, in every kernel: the epilogue waits
+  // on its single phase.
   static constexpr bool DBS = QS == 1;
   static constexpr int NSB = DBS ? 2 : QS;  // S buffers in TMEM
   static constexpr int KROWS = PAIR ? BN / 2 : BN;  // keys of a K tile held here
@@ -168,8 +170,8 @@ struct Layout {
                        B_KCF = B_KRE + NRS, B_KCE = B_KCF + NKS, B_VF = B_KCE + NKS,
                        B_VE = B_VF + NVS, B_SCF = B_VE + NVS, B_SCE = B_SCF + NSC,
                        B_SF = B_SCE + NSC, B_PF = B_SF + NSB, B_OF = B_PF + NSB,
-                       B_DRAIN = B_OF + QS, B_STALL = B_DRAIN + 1, B_MF = B_STALL + 1,
-                       NBAR = B_MF + NSC;
+                       B_PVT = B_OF + QS, B_DRAIN = B_PVT + 1, B_STALL = B_DRAIN + 1,
+                       B_MF = B_STALL + 1, NBAR = B_MF + NSC;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;       // tmem base, abort, count, pad
   static constexpr int OFF_LIST = OFF_MISC + 16 + 32;       // + warp counts for the list scan
   static constexpr int SMEM_FIXED = OFF_LIST;
@@ -568,6 +570,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       mbar_init(bar(L::B_PF + s), kM + peer_p);
     }
     for (int s = 0; s < QS; ++s) mbar_init(bar(L::B_OF + s), 1);
+    mbar_init(bar(L::B_PVT), 1);
     for (int i = 0; i < L::NSC; ++i) mbar_init(bar(L::B_MF + i), 1);
     mbar_init(bar(L::B_DRAIN), 1);
     mbar_init(bar(L::B_STALL), 1);  // never signalled: the timeout test hook waits on it
@@ -721,6 +724,11 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         ok = wait_bar(bar(L::B_VF + vs), (it / L::NVS) & 1, ctl, kErrMma);
         if (ok) mbar_arrive_remote(lbar(L::B_VF + vs));
       }
+      // The leader's last commit reaches this CTA too, after every earlier
+      // one (and after all of the pair's MMAs, which read this CTA's shared
+      // memory and TMEM): wait for it before this CTA may leave, on the
+      // normal path and after an abort alike.
+      drain_bar(bar(L::B_DRAIN), 0, a.timeout_ns);
     } else if (lane == 0) {
       constexpr int MM = PAIR ? 2 * kM : kM;  // rows of one MMA
       constexpr uint32_t idq = idesc_f16(MM, BN, 0, 0, 0, 0);                  // f16 x f16, K-major
@@ -786,10 +794,11 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
           if (!ok) break;
           tc_fence_after();
           issue_pv(0, vs, it == 0, it & 1);
-          commit(L::B_OF);  // one phase per tile
+          commit(L::B_PVT);  // one phase per tile
           commit(L::B_VE + vs);
           if (it + 2 < n_it) ok = qk_step(it + 2);
         }
+        if (ok && n_it > 0) commit(L::B_OF);  // after the last P V: the epilogue's one phase
       }
       for (int it = 0; it < n_it && ok && !L::DBS; ++it) {
         const int kst = it % L::NKS;
@@ -831,12 +840,11 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
           commit(L::B_OF + s);
         }
       }
-      // every MMA issued above has completed once this arrives (here only)
-      if constexpr (PAIR) mma_commit_pair(bar(L::B_DRAIN), 1);
+      // every MMA issued above has completed once this arrives (in both CTAs
+      // of a pair: the peer waits for it before it exits)
+      if constexpr (PAIR) mma_commit_pair(bar(L::B_DRAIN), 3);
       else mma_commit(bar(L::B_DRAIN));
       drain_bar(bar(L::B_DRAIN), 0, a.timeout_ns);
-      // after an abort, commits to the peer may still be in flight
-      if (PAIR && !ok) __nanosleep(20000);
     }
   } else if (warp >= L::W_CONV) {
     // ---------------------------------------------- int8 -> fp16 converters
@@ -1000,12 +1008,14 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     float m = -INFINITY;  // reference maximum (log2 units) that P is relative to
     float m_pend = -INFINITY;  // one-pass tiles: the reference the next tile takes
     float l = 0.f;
-    // One query stage: this tile's P is stored (and O rescaled) only once the
-    // previous tile's P V has completed. Stores that overlapped it corrupted O
-    // on some rows (128-dim block-sparse parity test), although they target
-    // the other S buffer; with the wait the outputs match exactly. A wait
-    // that runs out (voted across the warp) clears `ok`, which ends the loop
-    // after this tile.
+    // One query stage: O is rescaled only once the previous tile's P V has
+    // completed (B_PVT, one phase per tile). That wait cannot alias: when this
+    // tile's S is ready, the P V two tiles back has completed, so B_PVT is at
+    // most one phase behind the phase waited for. The epilogue instead waits
+    // on B_OF, committed once after the last P V: a parity wait on B_PVT there
+    // could find the barrier two phases behind (the last two P Vs in flight)
+    // and pass before O is complete. A wait that runs out (voted across the
+    // warp) clears `ok`, which ends the loop after this tile.
     for (int it = 0; it < n_it && ok; ++it) {
       const int ss = it % L::NSC;
       if (r == 0) IA_TRACE_POINT(4 * s, it);
@@ -1034,10 +1044,6 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         uint32_t z[BN / 2];
 #pragma unroll
         for (int e = 0; e < BN / 2; ++e) z[e] = 0u;
-        if (L::DBS && it > 0) {
-          if (!__all_sync(0xffffffffu, wait_bar(bar(L::B_OF), (it - 1) & 1, ctl, kErrSoftmax))) ok = false;
-          tc_fence_after();
-        }
         if constexpr (BN == 128) {
           tmem_st64(tS, z);
         } else {
@@ -1190,7 +1196,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         if (__any_sync(0xffffffffu, need)) {
           const float alpha = need ? ex2(m - m_new) : 1.f;
           if (L::DBS && it > 0) {  // the previous tile's P V may still be adding into O
-            ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_OF), (it - 1) & 1, ctl, kErrSoftmax));
+            ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_PVT), (it - 1) & 1, ctl, kErrSoftmax));
             if (!ok) break;
             tc_fence_after();
           }
@@ -1225,10 +1231,6 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         }
         if (OP) m_pend = m;
         }  // ---- two passes
-        if (L::DBS && it > 0) {
-          if (!__all_sync(0xffffffffu, wait_bar(bar(L::B_OF), (it - 1) & 1, ctl, kErrSoftmax))) ok = false;
-          tc_fence_after();
-        }
         if constexpr (BN == 128) {
           tmem_st64(tS, *reinterpret_cast<uint32_t(*)[64]>(sv));
         } else {
@@ -1255,7 +1257,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     }
     // ------------------------------------------------------------ epilogue
     if (ok && n_it > 0)
-      ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_OF + s), L::DBS ? (n_it - 1) & 1 : 0, ctl, kErrSoftmax));
+      ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_OF + s), 0, ctl, kErrSoftmax));
     if (ok) {
       tc_fence_after();
       bool pad = false;
