@@ -76,6 +76,10 @@ typedef enum ia_rope_layout {
  *   quantization then see these values. Padding rows (past kv_valid) stay 0.
  * The fixed order makes the result the same bit for bit in every kernel that
  * applies the prologue (ia_quantize_qk_prologue, ia_attention_fwd_quant_q).
+ * The order is this library's choice, not part of the method: the sum of
+ * squares itself is exact only up to the fp32 roundings of that order, so a
+ * row can come out one 16-bit ulp away from the same steps taken on the exact
+ * sum rounded once (and its codes one or two steps away).
  */
 typedef struct ia_qk_prologue {
   const float* q_norm_weight; /* fp32 [D] RMSNorm weight of Q rows, or NULL (no norm) */
@@ -310,8 +314,12 @@ IA_API size_t ia_attention_workspace_size(const ia_attn_params* p);
  * allocating library routine).
  *
  * Set-up: the first call on each device, with that device current, looks up
- * the array's device address (cudaGetSymbolAddress) and caches it; make that
- * first call before any stream capture.
+ * the array's device address (cudaGetSymbolAddress) and caches it together
+ * with the ID of the current CUDA context; make that first call before any
+ * stream capture. A later call in a different context of the device (after
+ * cudaDeviceReset, or once the primary context was released and made again)
+ * looks the address up again, so the first call in each new context should
+ * also come before any capture.
  *
  * Sharing: every call on a device uses the same array, and the array keeps
  * the last call's contents. Nothing in it needs to start at zero: every entry

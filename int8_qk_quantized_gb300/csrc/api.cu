@@ -1,11 +1,13 @@
 // C ABI of libia.so: argument checking, status codes and dispatch to the
 // kernel launchers. Nothing here allocates device memory or synchronises
 // (except ia_device_status, which exists to synchronise).
-#include <atomic>
+#include <cuda.h>
+
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "launch.h"
 
@@ -68,23 +70,70 @@ bool strides_ok(const int64_t* st, int n, int64_t esize) {
 static __device__ __align__(256) unsigned char g_static_workspace[IA_STATIC_WORKSPACE_BYTES];
 
 constexpr int kMaxDevices = 64;
-std::atomic<void*> g_static_workspace_ptr[kMaxDevices];
 
-// Device address of g_static_workspace on the current device, looked up once
-// per device with that device current.
+// The array's address belongs to a CUDA context: a context made later on the
+// same device (after cudaDeviceReset, or after the primary context was
+// released and created again) maps it elsewhere. The looked-up address is
+// therefore kept per device together with the ID of the context it was
+// looked up in, and looked up again when the current context differs.
+struct StaticWorkspaceSlot {
+  unsigned long long ctx_id;  // 0: none
+  void* ptr;
+};
+std::mutex g_static_workspace_mu;
+StaticWorkspaceSlot g_static_workspace_slot[kMaxDevices];
+
+// ID of the calling thread's current context through the driver's entry
+// points (the library links the runtime statically and not libcuda); false
+// when there is none yet or the entry points are unavailable.
+bool current_context_id(unsigned long long* id) {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+  });
+  if (get_current == nullptr || get_id == nullptr) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS && *id != 0;
+}
+
+// Device address of g_static_workspace in the current context of the current
+// device: looked up with cudaGetSymbolAddress on the first call in a context
+// (which also makes the device's primary context current if nothing had),
+// then taken from the cache while that context stays current.
 ia_status static_workspace(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(IA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices)
     return fail(IA_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev, kMaxDevices);
-  void* ptr = g_static_workspace_ptr[dev].load(std::memory_order_acquire);
-  if (ptr == nullptr) {
-    e = cudaGetSymbolAddress(&ptr, g_static_workspace);
-    if (e != cudaSuccess || ptr == nullptr)
-      return fail(IA_ERR_CUDA, "cudaGetSymbolAddress(static workspace): %s", cudaGetErrorString(e));
-    g_static_workspace_ptr[dev].store(ptr, std::memory_order_release);
+  unsigned long long id = 0;
+  bool have_id = current_context_id(&id);
+  std::lock_guard<std::mutex> lock(g_static_workspace_mu);
+  StaticWorkspaceSlot& slot = g_static_workspace_slot[dev];
+  if (have_id && slot.ctx_id == id && slot.ptr != nullptr) {
+    *out = slot.ptr;
+    return IA_OK;
   }
+  void* ptr = nullptr;
+  e = cudaGetSymbolAddress(&ptr, g_static_workspace);
+  if (e != cudaSuccess || ptr == nullptr)
+    return fail(IA_ERR_CUDA, "cudaGetSymbolAddress(static workspace): %s", cudaGetErrorString(e));
+  if (!have_id) have_id = current_context_id(&id);
+  slot.ctx_id = have_id ? id : 0ull;  // without an ID the next call looks the address up again
+  slot.ptr = ptr;
   *out = ptr;
   return IA_OK;
 }

@@ -84,3 +84,24 @@ def test_rejects_more_than_the_fixed_scratch():
     out = torch.empty_like(tensors[4])
     with pytest.raises(ia.IAError, match="fixed workspace"):
         ia.attention_static_workspace(*tensors, out, kv_splits=8, **args)
+
+
+def test_allocates_no_device_memory():
+    """The property the entry point exists for: a call with a key split takes
+    no device memory. After one warm-up call (which may load the kernels'
+    module), the device's free memory is the same before and after a call,
+    and torch's allocator holds the same bytes."""
+    import int8_qk_quantized_gb300 as ia
+    tensors, args = _prepare("anima4k", dict(H=3, Sq=700, Sk=3000))
+    q8, k8, qs, ks, v = tensors
+    out = torch.empty_like(v[:, :, :700])
+    lse = torch.empty((1, 3, 700), dtype=torch.float32, device="cuda")
+    ia.attention_static_workspace(q8, k8, qs, ks, v, out, lse=lse, kv_splits=4, **args)
+    torch.cuda.synchronize()
+    free0, held0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    for splits in (4, 2, 4):
+        ia.attention_static_workspace(q8, k8, qs, ks, v, out, lse=lse, kv_splits=splits, **args)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_allocated() == held0
+    ia.device_status()
