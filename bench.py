@@ -667,7 +667,28 @@ def main():
 
     hbm, bf16, bf16_sus, peak_kind = peaks()
     achieved = att_ops / (att_ms * 1e-3) / 1e12
-    quant_bytes = B * H * (Sq + Sk) * D * (2 + 1) + B * H * (Sq + Sk) * 4 + B * H * Sk * D * 2
+    # compulsory bytes of the quantize pass: Q and K read once (16-bit), codes
+    # written (int8), one fp32 scale per row and the fp32 K mean; a second read
+    # of K (the codes need the mean first) is not counted
+    quant_bytes = B * H * (Sq + Sk) * D * (2 + 1) + B * H * (Sq + Sk) * 4 + B * H * D * 4
+    # The second bound of the attention launches: the softmax's ALU and MUFU
+    # work, one exp2 per score at the measured 32 ex2/clk/SM, and its issue
+    # slots at 4 warp instructions per clock per SM. Per 8 scores of a 128-key
+    # row the fast path issues 2 shared loads of k scales, 4 f32x2 multiplies,
+    # 4 three-input maxima, 4 f32x2 FMAs, 8 ex2, 4 f32x2 adds (row sum) and 4
+    # packing conversions: 30 instructions, 3.75 per score.
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_mhz = (clocks or {}).get("sm_mhz") or 2070.0
+    scores = att_ops / (4 * D) / args.steps  # one score per 4*D operations
+    per_sec = sm_count * sm_mhz * 1e6
+    alu = {"bound": "alu", "scores_per_step": scores, "ex2_per_clk_per_sm": 32,
+           "issue_per_score": 3.75, "sm_count": sm_count, "sm_mhz": sm_mhz,
+           "mufu_ms": scores / (32 * per_sec) * 1e3,
+           "issue_ms": scores * 3.75 / (128 * per_sec) * 1e3,
+           "tensor_ms": att_ops / args.steps / (bf16 * 1e12) * 1e3,
+           "attention_ms": att_ms / args.steps}
+    alu["frac_mufu"] = alu["mufu_ms"] / alu["attention_ms"]
+    alu["frac_issue"] = alu["issue_ms"] / alu["attention_ms"]
     if rank != 0:
         if pg:
             pg.destroy_process_group()
@@ -706,7 +727,8 @@ def main():
                      "kernel": "attn_fwd_kernel (CTA pairs, QS=2, BN=128, D=128); per launch = mean of "
                                "the step's three attention launches",
                      "peak_source": f"{peak_kind} bf16 dense burst (MEASURED_PEAKS.json)",
-                     "frac_of_sustained": achieved / bf16_sus if bf16_sus else None},
+                     "frac_of_sustained": achieved / bf16_sus if bf16_sus else None,
+                     "second_bound": alu},
         "e2e": {"value": weak_value(ws, ops, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "copies": "pinned host <-> device every step on two copy streams, double-"

@@ -124,7 +124,8 @@ struct Params {
   int qp_pos0;
 };
 
-template <int D, int QS, int BN, bool SPARSE, bool ROWMASK = false, bool PAIR = false>
+template <int D, int QS, int BN, bool SPARSE, bool ROWMASK = false, bool PAIR = false,
+          bool KB = false>
 struct Layout {
   // Block-sparse, D == 128: the int8 K tile lands (by TMA) in the second
   // 64-column block of its fp16 K buffer and is widened in place, which keeps
@@ -143,6 +144,15 @@ struct Layout {
   static constexpr int NSB = DBS ? 2 : QS;  // S buffers in TMEM
   static constexpr int KROWS = PAIR ? BN / 2 : BN;  // keys of a K tile held here
   static constexpr int VCOLS = PAIR ? D / 2 : D;    // V columns held here
+  // Dense head dim 64 with per-row K scales (single CTAs): the P V MMA has
+  // N = D + 16, its last 16 columns reading a block of ones in shared memory,
+  // so that column D of O accumulates the row sum of the 16-bit P the MMA
+  // multiplied (the softmax keeps no running sum). A ones block sits at a fixed
+  // distance (the descriptor's leading byte offset) from each V buffer. With
+  // per-block K scales (KB) the softmax is light and the tensor core sets the
+  // pace, so the extra MMA columns would cost more than the sum they save.
+  static constexpr bool ONES = D == 64 && QS == 2 && !PAIR && !SPARSE && !ROWMASK && !KB;
+  static constexpr int OW = D + (ONES ? 16 : 0);  // O columns per stage in TMEM
   static constexpr int QH = kM * D * 2;      // fp16 Q stage
   static constexpr int KH = KROWS * D * 2;   // fp16 K tile
   static constexpr int VB = BN * VCOLS * 2;  // 16-bit V tile
@@ -161,7 +171,8 @@ struct Layout {
   static constexpr int OFF_KR = OFF_V + NVS * VB;
   static constexpr int OFF_QST = OFF_KR + NRS * KR;
   static constexpr int OFF_QIN = PAIR ? OFF_QST : OFF_V;  // where Q lands before conversion
-  static constexpr int OFF_MK = OFF_QST + QST;
+  static constexpr int OFF_ONES = OFF_QST + QST;  // ONES: NVS blocks of BN x 64 ones
+  static constexpr int OFF_MK = OFF_ONES + (ONES ? NVS * VB : 0);
   static constexpr int OFF_SC = OFF_MK + NSC * MB;
   static constexpr int OFF_VS = OFF_SC + NSC * SC;
   static constexpr int OFF_BAR = (OFF_VS + D * 4 + 7) / 8 * 8;
@@ -175,7 +186,7 @@ struct Layout {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;       // tmem base, abort, count, pad
   static constexpr int OFF_LIST = OFF_MISC + 16 + 32;       // + warp counts for the list scan
   static constexpr int SMEM_FIXED = OFF_LIST;
-  static constexpr int TMEM_NEED = NSB * BN + QS * D;
+  static constexpr int TMEM_NEED = NSB * BN + QS * OW;
   static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64
                                    : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
   static constexpr int NWARPS = 4 * QS + 4;
@@ -184,7 +195,10 @@ struct Layout {
   static_assert(PAIR || QS * QR * 2 <= NVS * VB, "16-bit Q is staged in the V buffers");
   static_assert(TMEM_NEED <= 512, "TMEM budget");
   static_assert(OFF_QH % 1024 == 0 && OFF_KH % 1024 == 0 && OFF_V % 1024 == 0 &&
-                    OFF_MK % 1024 == 0 && OFF_QST % 1024 == 0, "swizzle align");
+                    OFF_MK % 1024 == 0 && OFF_QST % 1024 == 0 && OFF_ONES % 1024 == 0,
+                "swizzle align");
+  static_assert(!ONES || (VB == BN * 128 && (OFF_ONES - OFF_V) / 16 < (1 << 14)),
+                "one 64-column V block per buffer; the ones within the descriptor's reach");
   static_assert(!ROWMASK || (QS == 1 && BN == 64 && !SPARSE), "row-mask shape");
   static_assert(!INPLACE || KR == BN * 128, "the int8 tile fills one 64-column fp16 block");
   // the pair's V half is one 64-column swizzle block; dense tiles only
@@ -512,13 +526,16 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
 // QS x 128 query rows; the pair walks the same key tiles, each CTA loading
 // and widening half of every K tile and half of V's columns, and the
 // even-ranked CTA issues 256-row MMAs over both (cta_group::2).
-template <int D, int QS, int BN, bool SPARSE, bool VBF16, bool QRAW, bool ROWMASK, bool PAIR>
+// KB: per-64-key-block K scales in the dense head-dim-64 kernel, folded into one
+// constant per block and row (see the softmax).
+template <int D, int QS, int BN, bool SPARSE, bool VBF16, bool QRAW, bool ROWMASK, bool PAIR,
+          bool KB = false>
 __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_m, const Params a) {
-  using L = Layout<D, QS, BN, SPARSE, ROWMASK, PAIR>;
+  using L = Layout<D, QS, BN, SPARSE, ROWMASK, PAIR, KB>;
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x;
@@ -532,6 +549,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     if (tid == 0) atomicOr(&g_attn_status, kErrSmemAlign);
     return;
   }
+  if (tid == 0) IA_TRACE_POINT(14, 0);  // events of CTA 0 in slot 14 (profiling build only)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
@@ -588,6 +606,12 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
   }
   float* vsc = reinterpret_cast<float*>(smem + L::OFF_VS);
   for (int i = tid; i < D; i += blockDim.x) vsc[i] = a.v_scale ? __ldg(a.v_scale + h * D + i) : 1.f;
+  if constexpr (L::ONES) {  // the row-sum columns of V: 1.0 in V's type
+    const uint32_t one2 = VBF16 ? 0x3F803F80u : 0x3C003C00u;
+    uint4* ones = reinterpret_cast<uint4*>(smem + L::OFF_ONES);
+    for (int i = tid; i < L::NVS * L::VB / 16; i += blockDim.x) ones[i] = make_uint4(one2, one2, one2, one2);
+    fence_proxy_async_smem();
+  }
 
   // Key tiles this CTA visits: all of them (dense) or the union of the kept
   // tiles of its two 64-row query tiles, in ascending order (block-sparse).
@@ -627,6 +651,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
   if constexpr (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = misc[0];
+  if (tid == 0) IA_TRACE_POINT(14, 1);
 
   const uint32_t sm_qh = smem_u32(smem + L::OFF_QH);
   const uint32_t sm_kh = smem_u32(smem + L::OFF_KH);
@@ -653,6 +678,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       constexpr int QB = QRAW ? 2 : 1;
       const uint32_t sm_qin = smem_u32(smem + L::OFF_QIN);
       mbar_arrive_expect_tx(bar(L::B_QFULL), QS * kM * D * QB);
+      IA_TRACE_POINT(14, 2);
       for (int s = 0; s < QS; ++s)
         tma_load_4d(sm_qin + s * L::QR * QB, &tm_q, bar(L::B_QFULL), 0, q0 + s * kM, h, b);
       bool ok = true;
@@ -732,14 +758,16 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     } else if (lane == 0) {
       constexpr int MM = PAIR ? 2 * kM : kM;  // rows of one MMA
       constexpr uint32_t idq = idesc_f16(MM, BN, 0, 0, 0, 0);                  // f16 x f16, K-major
-      constexpr uint32_t idv = idesc_f16(MM, D, VBF16 ? 1 : 0, VBF16 ? 1 : 0, 0, 1);  // V MN-major
+      constexpr uint32_t idv = idesc_f16(MM, L::OW, VBF16 ? 1 : 0, VBF16 ? 1 : 0, 0, 1);  // V MN-major
       // Descriptors are built once; a k-step or buffer offset is added to the
       // 14-bit start-address field (16-byte units), which cannot overflow for
       // addresses inside the CTA's shared memory. This keeps the issuing
       // thread to a few instructions per MMA.
       const uint64_t qdesc = sdesc_sw128(sm_qh, 16, 1024);
       const uint64_t kdesc = sdesc_sw128(sm_kh, 16, 1024);
-      const uint64_t vdesc = sdesc_sw128(sm_v, BN * 128, 1024);
+      // V's 64-column blocks are BN*128 bytes apart; the ones block sits at the
+      // same distance from every V buffer
+      const uint64_t vdesc = sdesc_sw128(sm_v, L::ONES ? L::OFF_ONES - L::OFF_V : BN * 128, 1024);
       // a barrier that also counts the peer's arrivals
       auto wait_in = [&](int i, uint32_t parity) { return wait_bar(bar(i), parity, ctl, kErrMma); };
       auto commit = [&](int i) {
@@ -762,7 +790,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       // O_s += P V (P from S buffer sb, V from stage vs)
       auto issue_pv = [&](int s, int vs, bool first, int sb) {
         const uint64_t vb = vdesc + static_cast<uint64_t>((vs * L::VB) >> 4);
-        const uint32_t dt = tmem + L::NSB * BN + s * D;
+        const uint32_t dt = tmem + L::NSB * BN + s * L::OW;
         const uint32_t pt = tmem + sb * BN;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
@@ -772,6 +800,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         }
       };
       bool ok = wait_in(L::B_QCONV, 0);
+      IA_TRACE_POINT(14, 5);
       if (ok && a.debug_stall) ok = wait_bar(bar(L::B_STALL), 0, ctl, kErrMma);
       tc_fence_after();
       if constexpr (L::DBS) {
@@ -842,6 +871,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       }
       // every MMA issued above has completed once this arrives (in both CTAs
       // of a pair: the peer waits for it before it exits)
+      IA_TRACE_POINT(14, 7);
       if constexpr (PAIR) mma_commit_pair(bar(L::B_DRAIN), 3);
       else mma_commit(bar(L::B_DRAIN));
       drain_bar(bar(L::B_DRAIN), 0, a.timeout_ns);
@@ -851,11 +881,13 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     const int ct = tid - L::W_CONV * 32;
     bool ok = QRAW ? true : wait_bar(bar(L::B_QFULL), 0, ctl, kErrConverter);
     if constexpr (PAIR) ok = __all_sync(0xffffffffu, ok);
+    if (ct == 0) IA_TRACE_POINT(14, 3);
     if (ok && !QRAW) {
       for (int s = 0; s < QS; ++s)
         widen_tile<D, kM, false>(smem + L::OFF_QIN + s * L::QR, smem + L::OFF_QH + s * L::QH, ct);
       fence_proxy_async_smem();
       mbar_arrive(bar(L::B_QCONV));
+      if (ct == 0) IA_TRACE_POINT(14, 4);
     }
     const uint8_t* mrow0 = nullptr;
     const uint8_t* mrow1 = nullptr;
@@ -963,7 +995,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     const int r = tid & (kM - 1);
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS0 = tmem + s * BN + lane_off;
-    const uint32_t tO = tmem + L::NSB * BN + s * D + lane_off;
+    const uint32_t tO = tmem + L::NSB * BN + s * L::OW + lane_off;
     const int row = q0 + s * kM + r;
     const bool row_ok = row < a.Sq;
     float cq = 0.f;
@@ -1005,6 +1037,34 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       cq = __ldg(a.q_scale + b * a.qs_sb + h * a.qs_sh + (a.gran_block ? (row >> 6) : row)) * a.cq_mult;
     }
     const int half = (r >= 64) ? 1 : 0;
+    // O *= alpha over all of this stage's O columns (with ONES, the row sum too)
+    auto rescale_o = [&](float alpha) {
+#pragma unroll 1
+      for (int c0 = 0; c0 + 32 <= L::OW; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(tO + c0, rr);
+        tmem_wait_ld(rr);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+        tmem_st32(tO + c0, rr);
+      }
+      if constexpr (L::OW % 32 != 0) {
+        uint32_t rr[16];
+        tmem_ld16(tO + (L::OW & ~31), rr);
+        tmem_wait_ld(rr);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+        tmem_st16(tO + (L::OW & ~31), rr);
+      }
+    };
+    // p = 2^t for two logits, packed to the 16-bit type of V. Without ONES the
+    // fp32 p are also added to the row sum `acc`; with ONES the MMA sums the
+    // 16-bit P it multiplies.
+    auto p_pack = [&](float t0, float t1, uint64_t& acc) -> uint32_t {
+      const float p0 = ex2(t0), p1 = ex2(t1);
+      if constexpr (!L::ONES) acc = fadd2(acc, pack2(p0, p1));
+      return VBF16 ? cvt_bf16x2(p0, p1) : cvt_f16x2(p0, p1);
+    };
     float m = -INFINITY;  // reference maximum (log2 units) that P is relative to
     float m_pend = -INFINITY;  // one-pass tiles: the reference the next tile takes
     float l = 0.f;
@@ -1038,6 +1098,14 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       const bool fast = ((flags & 1u) | fw[1] | fw[2]) == 0;
       const bool keep = SPARSE ? ((flags >> (1 + half)) & 1u) != 0 : true;
       const uint64_t cq2 = pack2(cq, cq);
+      // KB: each 64-key half of the tile has one k scale; s * k * cq becomes
+      // s * (k * cq), one constant per half and row, so the logits take one
+      // packed FMA and no per-key scale loads.
+      float cb0 = 0.f, cb1 = 0.f;
+      if constexpr (KB) {
+        cb0 = ksm[0] * cq;
+        cb1 = ksm[64] * cq;
+      }
       if (SPARSE && !keep) {
         // This row's query tile dropped the key tile: P = 0, the row's maximum
         // and sum stay as they are, and S need not be read.
@@ -1076,15 +1144,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         if constexpr (OP) {
           if (__any_sync(0xffffffffu, m_pend > m)) {  // the reference grew on the last tile
             const float alpha = m_pend > m ? ex2(m - m_pend) : 1.f;
-  #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-              uint32_t rr[32];
-              tmem_ld32(tO + c0, rr);
-              tmem_wait_ld(rr);
-  #pragma unroll
-              for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-              tmem_st32(tO + c0, rr);
-            }
+            rescale_o(alpha);
             l *= alpha;
             m = fmaxf(m, m_pend);
           }
@@ -1096,22 +1156,43 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
             if (!fast) {  // t = acc k cq + offset (log2 units; -inf for invalid keys)
   #pragma unroll
               for (int c = 0; c < BN; c += 4) {
-                const float4 k4 = *reinterpret_cast<const float4*>(ksm + c);
                 const float4 b4 = *reinterpret_cast<const float4*>(b2m + c);
                 float t[4];
-                unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(k4.x, k4.y)),
-                              cq2o, pack2(b4.x, b4.y)), t[0], t[1]);
-                unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(k4.z, k4.w)),
-                              cq2o, pack2(b4.z, b4.w)), t[2], t[3]);
+                if constexpr (KB) {
+                  const uint64_t c2 = c < 64 ? pack2(cb0, cb0) : pack2(cb1, cb1);
+                  unpack2(ffma2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), c2,
+                                pack2(b4.x, b4.y)), t[0], t[1]);
+                  unpack2(ffma2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), c2,
+                                pack2(b4.z, b4.w)), t[2], t[3]);
+                } else {
+                  const float4 k4 = *reinterpret_cast<const float4*>(ksm + c);
+                  unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(k4.x, k4.y)),
+                                cq2o, pack2(b4.x, b4.y)), t[0], t[1]);
+                  unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(k4.z, k4.w)),
+                                cq2o, pack2(b4.z, b4.w)), t[2], t[3]);
+                }
                 const int q = (c >> 2) & 3;
                 mo[q] = fmax3(mo[q], fmaxf(t[0], t[1]), fmaxf(t[2], t[3]));
   #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                   float t0, t1;
                   unpack2(fadd2(pack2(t[2 * h2], t[2 * h2 + 1]), nmo), t0, t1);
-                  const float p0 = ex2(t0), p1 = ex2(t1);
-                  lsum[h2] = fadd2(lsum[h2], pack2(p0, p1));
-                  sv[(c >> 1) + h2] = VBF16 ? cvt_bf16x2(p0, p1) : cvt_f16x2(p0, p1);
+                  sv[(c >> 1) + h2] = p_pack(t0, t1, lsum[h2]);
+                }
+              }
+            } else if constexpr (KB) {
+              // raw maxima per 64-key half (mo[0..1] and mo[2..3]), scaled below
+  #pragma unroll
+              for (int c = 0; c < BN; c += 8) {
+                const uint64_t c2 = c < 64 ? pack2(cb0, cb0) : pack2(cb1, cb1);
+  #pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  const float s0 = __uint_as_float(sv[c + 2 * q]), s1 = __uint_as_float(sv[c + 2 * q + 1]);
+                  const int i = (c < 64 ? 0 : 2) + (q & 1);
+                  mo[i] = fmax3(mo[i], s0, s1);
+                  float t0, t1;
+                  unpack2(ffma2(pack2(s0, s1), c2, nmo), t0, t1);
+                  sv[(c >> 1) + q] = p_pack(t0, t1, lsum[q & 1]);
                 }
               }
             } else {
@@ -1129,14 +1210,13 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
                 mo[q] = fmax3(mo[q], u[2 * q], u[2 * q + 1]);
                 float t0, t1;
                 unpack2(ffma2(pack2(u[2 * q], u[2 * q + 1]), cq2o, nmo), t0, t1);
-                const float p0 = ex2(t0), p1 = ex2(t1);
-                lsum[q & 1] = fadd2(lsum[q & 1], pack2(p0, p1));
-                sv[(c >> 1) + q] = VBF16 ? cvt_bf16x2(p0, p1) : cvt_f16x2(p0, p1);
+                sv[(c >> 1) + q] = p_pack(t0, t1, lsum[q & 1]);
               }
             }
             }
             const float rmo = fmaxf(fmaxf(mo[0], mo[1]), fmaxf(mo[2], mo[3]));
-            const float tmx = fast ? cq * rmo : rmo;
+            float tmx = fast ? cq * rmo : rmo;
+            if (KB && fast) tmx = fmaxf(fmaxf(mo[0], mo[1]) * cb0, fmaxf(mo[2], mo[3]) * cb1);
             if (__any_sync(0xffffffffu, tmx > m + kRedo)) {
               one = false;  // redo exactly: S is still in TMEM
               if constexpr (BN == 128) tmem_ld128(tS, sv);
@@ -1152,7 +1232,15 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         // u = acc * k_scale (fast tiles) or t = u * cq + bias*log2e / -inf
         // (masked tiles), in place, and the row maximum.
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (fast) {
+        if (KB && fast) {  // raw S stays; maxima per 64-key half
+  #pragma unroll
+          for (int c = 0; c < BN; c += 8)
+  #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int i = (c < 64 ? 0 : 2) + (q & 1);
+              mx[i] = fmax3(mx[i], __uint_as_float(sv[c + 2 * q]), __uint_as_float(sv[c + 2 * q + 1]));
+            }
+        } else if (fast) {
   #pragma unroll
           for (int c = 0; c < BN; c += 8) {
             const float4 ka = *reinterpret_cast<const float4*>(ksm + c);
@@ -1170,13 +1258,21 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         } else {
   #pragma unroll
           for (int c = 0; c < BN; c += 4) {
-            const float4 k4 = *reinterpret_cast<const float4*>(ksm + c);
             const float4 b4 = *reinterpret_cast<const float4*>(b2m + c);
             float f[4];
-            unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(k4.x, k4.y)),
-                          cq2, pack2(b4.x, b4.y)), f[0], f[1]);
-            unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(k4.z, k4.w)),
-                          cq2, pack2(b4.z, b4.w)), f[2], f[3]);
+            if constexpr (KB) {
+              const uint64_t c2 = c < 64 ? pack2(cb0, cb0) : pack2(cb1, cb1);
+              unpack2(ffma2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), c2,
+                            pack2(b4.x, b4.y)), f[0], f[1]);
+              unpack2(ffma2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), c2,
+                            pack2(b4.z, b4.w)), f[2], f[3]);
+            } else {
+              const float4 k4 = *reinterpret_cast<const float4*>(ksm + c);
+              unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(k4.x, k4.y)),
+                            cq2, pack2(b4.x, b4.y)), f[0], f[1]);
+              unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(k4.z, k4.w)),
+                            cq2, pack2(b4.z, b4.w)), f[2], f[3]);
+            }
             if constexpr (ROWMASK) {
               float mk[4];
               row_mask4(smem + L::OFF_MK + ss * L::MB, r, c, a.rm_dtype, mk);
@@ -1190,7 +1286,8 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
           }
         }
         const float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        const float tmax = fast ? cq * rmax : rmax;
+        float tmax = fast ? cq * rmax : rmax;
+        if (KB && fast) tmax = fmaxf(fmaxf(mx[0], mx[1]) * cb0, fmaxf(mx[2], mx[3]) * cb1);
         const float m_new = fmaxf(m, tmax);
         const bool need = m_new > m + kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
@@ -1200,17 +1297,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
             if (!ok) break;
             tc_fence_after();
           }
-          if (it > 0) {
-  #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-              uint32_t rr[32];
-              tmem_ld32(tO + c0, rr);
-              tmem_wait_ld(rr);
-  #pragma unroll
-              for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-              tmem_st32(tO + c0, rr);
-            }
-          }
+          if (it > 0) rescale_o(alpha);
           l *= alpha;
           if (need) m = m_new;
         }
@@ -1223,11 +1310,11 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         // to the first BN/2 columns of S in one store.
   #pragma unroll
         for (int e = 0; e < BN / 2; ++e) {
+          uint64_t kv2 = k1v;
+          if (KB && fast) kv2 = 2 * e < 64 ? pack2(cb0, cb0) : pack2(cb1, cb1);
           float t0, t1;
-          unpack2(ffma2(pack2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), k1v, nm), t0, t1);
-          const float p0 = ex2(t0), p1 = ex2(t1);
-          lsum[e & 1] = fadd2(lsum[e & 1], pack2(p0, p1));
-          sv[e] = VBF16 ? cvt_bf16x2(p0, p1) : cvt_f16x2(p0, p1);
+          unpack2(ffma2(pack2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), kv2, nm), t0, t1);
+          sv[e] = p_pack(t0, t1, lsum[e & 1]);
         }
         if (OP) m_pend = m;
         }  // ---- two passes
@@ -1260,6 +1347,15 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_OF + s), 0, ctl, kErrSoftmax));
     if (ok) {
       tc_fence_after();
+      if (r == 0 && s == 0) IA_TRACE_POINT(14, 8);
+      if constexpr (L::ONES) {  // the row sum the MMA accumulated in column D
+        if (n_it > 0) {
+          uint32_t lr[16];
+          tmem_ld16(tO + D, lr);
+          tmem_wait_ld(lr);
+          l = __uint_as_float(lr[0]);
+        }
+      }
       bool pad = false;
       if (a.pad_query && row_ok) pad = (row & 63) >= __ldg(a.kv_valid + (row >> 6));
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
@@ -1312,8 +1408,10 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
   }
 
   // ------------------------------------------------------------- teardown
+  if (warp == 0 && lane == 0) IA_TRACE_POINT(14, 9);
   tc_fence_before();
   __syncthreads();
+  if (tid == 0) IA_TRACE_POINT(14, 10);
   // Neither CTA of a pair leaves while the leader's MMAs may still read the
   // peer's shared memory or TMEM, or the peer's arrivals reach the leader.
   if constexpr (PAIR) cluster_sync();
@@ -1360,9 +1458,10 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int esiz
   return r == CUDA_SUCCESS;
 }
 
-template <int D, int QS, int BN, bool SPARSE, bool VBF16, bool QRAW, bool ROWMASK, bool PAIR = false>
+template <int D, int QS, int BN, bool SPARSE, bool VBF16, bool QRAW, bool ROWMASK, bool PAIR = false,
+          bool KB = false>
 ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** msg) {
-  using L = Layout<D, QS, BN, SPARSE, ROWMASK, PAIR>;
+  using L = Layout<D, QS, BN, SPARSE, ROWMASK, PAIR, KB>;
   const ia_attn_params& p = A.p;
   CUtensorMap tq, tk, tv, tm;
   std::memset(&tm, 0, sizeof(tm));
@@ -1453,7 +1552,7 @@ ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** ms
     a.ws_l = a.ws_o + static_cast<int64_t>(nsplit) * rows * D;
   }
   const size_t smem = L::SMEM_FIXED + (SPARSE ? static_cast<size_t>(a.Tk) * 2 : 0);
-  auto kern = attn_fwd_kernel<D, QS, BN, SPARSE, VBF16, QRAW, ROWMASK, PAIR>;
+  auto kern = attn_fwd_kernel<D, QS, BN, SPARSE, VBF16, QRAW, ROWMASK, PAIR, KB>;
   if (smem > 232448) {
     *msg = "key-tile list does not fit in shared memory (too many key tiles)";
     return IA_ERR_UNSUPPORTED;
@@ -1543,6 +1642,9 @@ ia_status dispatch(const AttnLaunch& A, int num_sms, cudaStream_t st, const char
   if (p.D == 128)  // CTA pairs with 256-row MMAs
     return bf ? run<128, 2, 128, false, true, QRAW, false, true>(A, num_sms, st, msg)
               : run<128, 2, 128, false, false, QRAW, false, true>(A, num_sms, st, msg);
+  if (p.granularity == IA_PER_BLOCK64)  // per-block K scales folded into the softmax constants
+    return bf ? run<64, 2, 128, false, true, QRAW, false, false, true>(A, num_sms, st, msg)
+              : run<64, 2, 128, false, false, QRAW, false, false, true>(A, num_sms, st, msg);
   return bf ? run<64, 2, 128, false, true, QRAW, false>(A, num_sms, st, msg)
             : run<64, 2, 128, false, false, QRAW, false>(A, num_sms, st, msg);
 }

@@ -35,6 +35,11 @@ def declared_symbols():
 
 
 def assert_lse_close(got, ref, valid=None):
+    """LSE within LSE_REL relative of the reference, -inf exactly where it is
+    -inf. Reading of "1e-4 relative": the error is divided by max(|LSE|, 1), so
+    it is relative for |LSE| >= 1 and an absolute 1e-4 below (an LSE near 0
+    would otherwise make any bound vanish; LSE is ln of a sum of exponentials,
+    so 1e-4 absolute there is a relative 1e-4 on that sum)."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     if valid is not None:
