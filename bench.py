@@ -40,8 +40,8 @@ PAGE_SPLIT_MS = 11.05
 # unmasked), recorded with the SHA-256 of the kernel sources it was taken on. A launch's traffic is scaled
 # from it per head, with the key-proportional part scaled by the keys of the
 # launch. When the kernel sources change, the figure no longer applies.
-ATTN_TRAFFIC = {"source_sha256": "8bf02c4e7352cc98f9e16bc107a4180be5cfe93b121c2fd8e71b6142e102aa7c",
-                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 246631680.0}
+ATTN_TRAFFIC = {"source_sha256": "275b5f7d2d7062f3dac150f252940781f38c034708176f6ec9751aca688adc8d",
+                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 246638592.0}
 
 
 def attn_source_sha():

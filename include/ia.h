@@ -280,6 +280,16 @@ IA_API ia_status ia_attention_fwd(const int8_t* q_i8, const int8_t* k_i8, const 
  *   others   as ia_attention_fwd; p->granularity sets the layout of both the
  *            in-kernel Q scales and k_scale. Query rows past kv_valid (when
  *            Sq == Sk) are padding: they are excluded from their block's amax.
+ *
+ * When it pays (GB300, whole path of K quantization + attention against
+ * ia_quantize_qk + ia_attention_fwd): dense shapes gain the Q pass (anima 4096
+ * and 9216 rows, sdxl: 2-7% faster). With a block mask it loses (65536 rows,
+ * 80 kept tiles per query tile: about 2% slower): each CTA quantizes its Q rows
+ * before any key tile while the block-sparse CTA has few tiles to hide that
+ * behind. With the RMSNorm + RoPE prologue in the kernel (p->q_prologue) it is
+ * 2-3% slower as well: the prologue's per-row work in the softmax warps costs
+ * more than the separate pass it saves. The two paths give identical results;
+ * choose by shape.
  */
 IA_API ia_status ia_attention_fwd_quant_q(const void* q, const int8_t* k_i8, const float* k_scale,
                                           const void* v, const float* bias_or_null,
