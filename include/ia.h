@@ -137,7 +137,15 @@ typedef enum ia_mask_dtype {
  *   q_i8, k_i8  outputs, int8 contiguous [B,H,Sq,D] / [B,H,Sk,D].
  *   q_scale, k_scale  outputs, fp32 contiguous [B,H,Sq] / [B,H,Sk] per token,
  *               [B,H,ceil(S/64)] per block.
- *   k_mean_out  optional fp32 [B,H,D] output of the mean that was used.
+ *   k_mean_out  optional fp32 [B,H,D] output of the mean that was used. When
+ *               the mean is computed, k_mean_out is given and K holds more
+ *               than 32 MiB, the pass runs as two kernels: the K sum
+ *               (clusters of CTAs per head, writing the mean here), then the
+ *               codes. Otherwise one fused kernel sums and quantises each
+ *               head. The results are the same bits; on a large K the
+ *               two-kernel form is faster (K no longer fits in L2 for the
+ *               fused kernel's second read, and its code pass is not held
+ *               at a cluster barrier).
  * Limits (IA_ERR_UNSUPPORTED): H <= 65535 and B <= 65535.
  */
 IA_API ia_status ia_quantize_qk(const void* q, const void* k, ia_dtype in_dtype, int B, int H,

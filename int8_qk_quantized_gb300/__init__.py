@@ -185,11 +185,15 @@ def _strides3(t):
 
 
 def quantize_qk(q, k, granularity: str = "token", center_k: bool = True, kv_valid=None,
-                k_mean=None, return_mean: bool = False, stream=None, prologue=None):
+                k_mean=None, return_mean: bool = False, stream=None, prologue=None,
+                two_pass: bool = True):
     """Quantise Q (may be None) and K to INT8 with symmetric fp32 scales.
 
     ``prologue`` (from ``make_prologue``) applies RMSNorm + RoPE to each row
-    first, in the same kernel (``ia_quantize_qk_prologue``).
+    first, in the same kernel (``ia_quantize_qk_prologue``). ``two_pass``
+    (default) hands the library a buffer for the K mean, which selects its
+    mean-then-codes kernels; False leaves it out unless ``return_mean``, which
+    selects the single fused kernel (same results).
     Returns ``(q8, q_scale, k8, k_scale)`` (``None`` for a skipped input), plus
     the K mean ``[B,H,D]`` that was used when ``return_mean``.
     """
@@ -214,7 +218,7 @@ def quantize_qk(q, k, granularity: str = "token", center_k: bool = True, kv_vali
         k8 = torch.empty((B, H, Sk, D), dtype=torch.int8, device=dev)
         ks = torch.empty((B, H, nscale(Sk)), dtype=torch.float32, device=dev)
     mu = None
-    if return_mean and k is not None and center_k:
+    if k is not None and center_k and (two_pass or return_mean):
         mu = torch.empty((B, H, D), dtype=torch.float32, device=dev)
     if kv_valid is not None:
         kv_valid = kv_valid.to(device=dev, dtype=torch.int32).contiguous()

@@ -165,14 +165,73 @@ __device__ __forceinline__ void prologue8(float (&v)[8], bool ok, int rr, int tc
   for (int i = 0; i < 8; ++i) v[i] = ok ? round16<DT>(v[i]) : 0.f;
 }
 
+// Per-token codes and scales of rows [r_lo, r_hi) of one head, the mean (if
+// centring) in s_mu (16-byte aligned shared memory), walked from the last
+// row. Four adjacent lanes own a row: lane t of the four loads the row's
+// 16-byte chunks t, t+4, t+8, ... (the four read 64 contiguous bytes per
+// load), so a warp covers 8 rows, the row maximum takes two shuffles and one
+// pair of IEEE divisions serves 8 rows per warp. The raw 16-bit chunks stay
+// in registers; the centred values are formed twice (for the maximum, then
+// for the codes) with the same IEEE subtraction.
+template <int D, int DT, int NT>
+__device__ __forceinline__ void lean_codes(const QuantArgs& a, const char* xb, int8_t* cb, float* sc,
+                                           int r_lo, int r_hi, const float* s_mu, int tid) {
+  constexpr int CPT = D / 32;  // 16-byte chunks per lane
+  constexpr int RPP = NT / 4;  // rows per pass
+  const int g = tid >> 2, tc = tid & 3;
+  // the trip count is uniform over the block: every lane reaches the shuffles
+  for (int base = r_hi - RPP; base > r_lo - RPP; base -= RPP) {
+    const int rr = base + g;
+    const bool in = rr >= r_lo && rr < r_hi;
+    const bool ok = in && row_valid(a.valid, rr);
+    uint4 w[CPT];
+#pragma unroll
+    for (int j = 0; j < CPT; ++j)
+      w[j] = ok ? __ldg(reinterpret_cast<const uint4*>(xb + (static_cast<int64_t>(rr) * a.ss + (tc + 4 * j) * 8) * 2))
+                : make_uint4(0u, 0u, 0u, 0u);
+    auto centred = [&](int j, float (&v)[8]) {
+      unpack8<DT>(w[j], v);
+      if (a.center && ok) {
+        const float4 m0 = *reinterpret_cast<const float4*>(s_mu + (tc + 4 * j) * 8);
+        const float4 m1 = *reinterpret_cast<const float4*>(s_mu + (tc + 4 * j) * 8 + 4);
+        unpack2(fsub2(pack2(v[0], v[1]), pack2(m0.x, m0.y)), v[0], v[1]);
+        unpack2(fsub2(pack2(v[2], v[3]), pack2(m0.z, m0.w)), v[2], v[3]);
+        unpack2(fsub2(pack2(v[4], v[5]), pack2(m1.x, m1.y)), v[4], v[5]);
+        unpack2(fsub2(pack2(v[6], v[7]), pack2(m1.z, m1.w)), v[6], v[7]);
+      }
+    };
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+      float v[8];
+      centred(j, v);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m = fmax3(m, fabsf(v[2 * i]), fabsf(v[2 * i + 1]));
+    }
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    if (!in) continue;
+    const float inv = m > 0.f ? __fdiv_rn(127.f, m) : 0.f;
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+      float v[8];
+      centred(j, v);
+      store_codes(cb + static_cast<int64_t>(rr) * D + (tc + 4 * j) * 8, v, inv);
+    }
+    if (tc == 0) sc[rr] = (ok && m > 0.f) ? __fdiv_rn(m, 127.f) : 0.f;
+  }
+}
+
 // grid: (chunks, H, B). Chunk c holds rows [c*chunk, min(S, (c+1)*chunk)).
-// With CLUSTER_MEAN the chunks of one head are one cluster and compute the mean.
-template <int D, int DT, bool CLUSTER_MEAN, bool PRO>
+// With CLUSTER_MEAN the chunks of one head are one cluster and compute the mean;
+// MEAN_ONLY then stops once the mean is written to a.mean_out (codes_kernel
+// writes the codes in a second pass).
+template <int D, int DT, bool CLUSTER_MEAN, bool PRO, bool MEAN_ONLY = false>
 __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a, int chunk) {
   constexpr int TPR = D / 8;            // threads per row, 8 elements each
   constexpr int RPP = kThreads / TPR;   // rows per pass
   static_assert(RPP * TPR == kThreads, "layout");
-  __shared__ float s_mu[D];
+  __shared__ __align__(16) float s_mu[D];
   __shared__ double s_red[CLUSTER_MEAN ? RPP : 1][CLUSTER_MEAN ? D : 1];
   __shared__ double s_part[CLUSTER_MEAN ? D : 1];
   __shared__ float s_wmax[kThreads / 32];
@@ -250,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a
         if (a.mean_out && cluster.block_rank() == 0) a.mean_out[bh * D + tid] = s_mu[tid];
       }
       cluster.sync();  // no CTA leaves while another still reads its partials
+      if constexpr (MEAN_ONLY) return;
     } else {
       if (tid < D) {
         s_mu[tid] = __ldg(a.mean_in + bh * D + tid);
@@ -264,6 +324,10 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a
 
   int8_t* cb = a.codes + bh * static_cast<int64_t>(a.S) * D;
   // ------------------------------------------------------ per-token codes
+  if (!PRO && !a.gran_block) {
+    lean_codes<D, DT, kThreads>(a, xb, cb, a.scales + bh * a.S, r0, r1, s_mu, tid);
+    return;
+  }
   if (!a.gran_block) {
     float* sc = a.scales + bh * a.S;
     // The loop bound is uniform across the CTA: every lane reaches the shuffles.
@@ -351,6 +415,48 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a
   }
 }
 
+// Per-token codes without the prologue, the mean (if any) read from
+// a.mean_in. grid: (ceil(S / rows), H, B); block x covers rows
+// [S - (x+1) rows, S - x rows) clamped at 0, so the first blocks take the
+// head's last rows.
+constexpr int kCodeThreads = 256;
+constexpr int kCodeRows = 512;  // rows per block: 8 passes of 64
+template <int D, int DT>
+__global__ void __launch_bounds__(kCodeThreads) codes_kernel(const QuantArgs a) {
+  __shared__ __align__(16) float s_mu[D];
+  const int tid = threadIdx.x;
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int r_hi = a.S - blockIdx.x * kCodeRows;
+  const int r_lo = max(0, r_hi - kCodeRows);
+  const int64_t bh = static_cast<int64_t>(b) * a.H + h;
+  const char* xb = static_cast<const char*>(a.x) + (static_cast<int64_t>(b) * a.sb +
+                                                    static_cast<int64_t>(h) * a.sh) * 2;
+  if (tid < D) s_mu[tid] = a.center ? __ldg(a.mean_in + bh * D + tid) : 0.f;
+  __syncthreads();
+  lean_codes<D, DT, kCodeThreads>(a, xb, a.codes + bh * static_cast<int64_t>(a.S) * D, a.scales + bh * a.S,
+                                  r_lo, r_hi, s_mu, tid);
+}
+
+// Codes and scales with the mean (if any) already known (a.mean_in).
+template <int D, int DT, bool PRO>
+cudaError_t launch_codes(const QuantArgs& a, cudaStream_t st) {
+  if (!PRO && !a.gran_block) {
+    if (a.center && a.mean_out != nullptr && a.mean_out != a.mean_in) {  // the mean that was used
+      const cudaError_t e = cudaMemcpyAsync(a.mean_out, a.mean_in, static_cast<size_t>(a.B) * a.H * D * sizeof(float),
+                                            cudaMemcpyDeviceToDevice, st);
+      if (e != cudaSuccess) return e;
+    }
+    dim3 grid((a.S + kCodeRows - 1) / kCodeRows, a.H, a.B);
+    codes_kernel<D, DT><<<grid, kCodeThreads, 0, st>>>(a);
+    return cudaGetLastError();
+  }
+  // Rows split into chunks of 256 (a multiple of 64); no cluster.
+  const int chunk = 256;
+  dim3 grid((a.S + chunk - 1) / chunk, a.H, a.B);
+  quantize_kernel<D, DT, false, PRO><<<grid, kThreads, 0, st>>>(a, chunk);
+  return cudaGetLastError();
+}
+
 template <int D, int DT, bool PRO>
 cudaError_t launch_typed(const QuantArgs& a, int num_sms, cudaStream_t st) {
   const int BH = a.B * a.H;
@@ -358,11 +464,21 @@ cudaError_t launch_typed(const QuantArgs& a, int num_sms, cudaStream_t st) {
     // One cluster per head, sized so that the grid fills two CTAs per SM in
     // one wave where the heads allow (up to the largest cluster the device
     // can place; 16 needs the non-portable cluster size attribute).
-    auto kern = quantize_kernel<D, DT, true, PRO>;
-    static int max_cl = 0;
+    // A K larger than ~1/4 of L2 is not there any more when the fused pass
+    // reads it the second time: then, with somewhere to put the mean, two
+    // passes (the clusters only sum K and write the mean, the code kernel
+    // reads it), which keeps the code pass off the cluster barrier. A
+    // smaller K stays in L2 and one fused pass saves a launch.
+    const bool two_pass = a.mean_out != nullptr &&
+                          static_cast<int64_t>(BH) * a.S * D * 2 > (int64_t{32} << 20);
+    auto fused = quantize_kernel<D, DT, true, PRO, false>;
+    auto mean_only = quantize_kernel<D, DT, true, PRO, true>;
+    auto kern = two_pass ? mean_only : fused;
+    static int max_cl = 0;  // the two kernels have the same resources
     if (max_cl == 0) {
       max_cl = 8;
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+      if (cudaFuncSetAttribute(fused, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+          cudaFuncSetAttribute(mean_only, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
         cudaLaunchConfig_t q = {};
         q.gridDim = dim3(16, 1, 1);
         q.blockDim = dim3(kThreads);
@@ -391,13 +507,14 @@ cudaError_t launch_typed(const QuantArgs& a, int num_sms, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a, chunk);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, chunk);
+    if (e != cudaSuccess || !two_pass) return e;
+    QuantArgs c = a;
+    c.mean_in = a.mean_out;
+    c.mean_out = nullptr;
+    return launch_codes<D, DT, PRO>(c, st);
   }
-  // Rows split into chunks of 256 (a multiple of 64); no cluster.
-  const int chunk = 256;
-  dim3 grid((a.S + chunk - 1) / chunk, a.H, a.B);
-  quantize_kernel<D, DT, false, PRO><<<grid, kThreads, 0, st>>>(a, chunk);
-  return cudaGetLastError();
+  return launch_codes<D, DT, PRO>(a, st);
 }
 
 }  // namespace

@@ -86,8 +86,15 @@ QUANT_CASES = [
 ]
 
 
-@pytest.mark.parametrize("name,kw", QUANT_CASES)
-def test_quantize_outputs_stay_in_bounds(name, kw):
+@pytest.mark.parametrize("with_mean", [True, False], ids=["mean_out", "no_mean_out"])
+@pytest.mark.parametrize("name,kw", QUANT_CASES + [
+    # K above 32 MiB: with a mean output, the mean kernel and the code kernel
+    ("banded", dict(H=2, Sq=200, Sk=66001, skirt_width=600)),
+    ("sparse", dict(H=1, Sq=135168, Sk=135168, band_tiles=4, random_tiles=2, granularity="block64")),
+])
+def test_quantize_outputs_stay_in_bounds(name, kw, with_mean):
+    """A K above 32 MiB with a mean output runs the mean and code kernels;
+    otherwise the fused kernel."""
     import int8_qk_quantized_gb300 as ia
     wl = WORKLOADS[name].with_(**kw)
     inp = make_inputs(wl, "cuda")
@@ -105,10 +112,12 @@ def test_quantize_outputs_stay_in_bounds(name, kw):
     st = L.ia_quantize_qk(inp.q.data_ptr(), inp.k.data_ptr(), ia._dtype_code(inp.q.dtype), B, H,
                           wl.Sq, wl.Sk, D, qst, kst, ia._gran_code(wl.granularity), 1,
                           None if kvv is None else kvv.data_ptr(), None,
-                          *[t.data_ptr() for _, t in (outs[0], outs[2], outs[1], outs[3], outs[4])],
+                          *[t.data_ptr() for _, t in (outs[0], outs[2], outs[1], outs[3])],
+                          outs[4][1].data_ptr() if with_mean else None,
                           torch.cuda.current_stream().cuda_stream)
     assert st == 0, ia.load_library().ia_last_error_message()
-    for (g, t), r, n in zip(outs, ref, ("q codes", "q scales", "k codes", "k scales", "k mean")):
+    n_out = 5 if with_mean else 4
+    for (g, t), r, n in zip(outs[:n_out], ref, ("q codes", "q scales", "k codes", "k scales", "k mean")):
         g.check(n)
         assert torch.equal(t, r), n
 

@@ -1,6 +1,8 @@
 """GPU quantiser against the oracle: codes, scales and the K mean bit for bit.
 
-Covers per-token and per-64-row-block scales, bf16 and fp16, D 64 and 128,
+Covers the fused kernel and, for a K above 32 MiB, the two-kernel path (mean
+pass, then codes), per-token and per-64-row-block scales, bf16 and fp16, D 64
+and 128,
 ragged tails, the validity vector, strided (BSHD-backed) inputs, an external
 mean, no centring, and the full-size K of the banded and block-sparse
 workloads."""
@@ -20,10 +22,13 @@ def _lib():
     ensure_built()
 
 
-def gpu_quant(q, k, gran, kv_valid=None, center=True, k_mean=None):
+def gpu_quant(q, k, gran, kv_valid=None, center=True, k_mean=None, two_pass=True):
+    """two_pass: the library's mean-then-codes kernels (it is given a buffer for
+    the mean, which is returned); False: the fused kernel (no mean buffer, so
+    only codes and scales come back)."""
     import int8_qk_quantized_gb300 as ia
     res = ia.quantize_qk(q, k, granularity=gran, center_k=center, kv_valid=kv_valid,
-                         k_mean=k_mean, return_mean=center)
+                         k_mean=k_mean, return_mean=center and two_pass, two_pass=two_pass)
     torch.cuda.synchronize()
     return [None if t is None else to_np(t) for t in res]
 
@@ -66,6 +71,26 @@ def test_quantize_bit_exact(name, kw):
     wl = WORKLOADS[name].with_(**kw)
     inp = make_inputs(wl, "cuda")
     got = gpu_quant(inp.q, inp.k, wl.granularity, inp.kv_valid)
+    ref = oracle_quant(inp.q, inp.k, wl.granularity, inp.kv_valid)
+    assert_same(got, ref)
+
+
+# K above 32 MiB: with a mean buffer the library runs the mean kernel and the
+# code kernel, without one the fused kernel; both against the oracle (ragged
+# tail, validity vector, per-token and per-block scales)
+LARGE = [
+    ("banded", dict(H=2, Sq=300, Sk=70001, skirt_width=600)),
+    ("sparse", dict(H=1, Sq=140032, Sk=140032, band_tiles=8, random_tiles=4, granularity="block64")),
+]
+
+
+@pytest.mark.parametrize("two_pass", [True, False], ids=["two_pass", "fused"])
+@pytest.mark.parametrize("name,kw", LARGE)
+def test_quantize_large_k_both_paths(name, kw, two_pass):
+    wl = WORKLOADS[name].with_(**kw)
+    assert wl.B * wl.H * wl.Sk * wl.D * 2 > 32 << 20
+    inp = make_inputs(wl, "cuda")
+    got = gpu_quant(inp.q, inp.k, wl.granularity, inp.kv_valid, two_pass=two_pass)
     ref = oracle_quant(inp.q, inp.k, wl.granularity, inp.kv_valid)
     assert_same(got, ref)
 
