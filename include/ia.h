@@ -194,7 +194,12 @@ typedef struct ia_attn_params {
                                    kept-tile list with a block mask); each range is attended
                                    separately into an fp32 partial (O, LSE) in `workspace`,
                                    and the partials are merged exactly, as ia_merge_lse does,
-                                   into out and lse. Helps grids that cover the GPU poorly. */
+                                   into out and lse. Helps grids that cover the GPU poorly.
+                                   Head dim 64, int8 Q, no mask, n == 2 and at least one
+                                   256-row query tile per SM: one CTA per SM takes an equal
+                                   share of all (query tile, key tile) pairs, so a query
+                                   tile's two ranges meet where a CTA's share ends (unequal,
+                                   or one range empty); the merge is the same. */
   void* workspace;              /* device scratch of ia_attention_workspace_size(p) bytes,
                                    used only when kv_splits >= 2; owned by the caller */
   size_t workspace_bytes;       /* its size, checked */
@@ -360,7 +365,10 @@ IA_API ia_status ia_attention_fwd_static_workspace(
  * partial written and read back by the merge. A split is suggested only when
  * the model expects it to save at least 5%, which happens when the grid
  * covers the SMs poorly (short queries against long keys); with a block mask
- * only when the grid is under one wave. Returns 1..16.
+ * only when the grid is under one wave. For head dim 64 without a block mask
+ * and with at least one 256-row query tile per SM, two ranges are costed as
+ * the balanced schedule ia_attention_fwd then runs (see kv_splits). Returns
+ * 1..16.
  * block_mask: nonzero if a block mask will be passed.
  */
 IA_API int ia_attention_default_splits(const ia_attn_params* p, int block_mask);

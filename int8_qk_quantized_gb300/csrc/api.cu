@@ -514,6 +514,13 @@ IA_API int ia_attention_default_splits(const ia_attn_params* p, int block_mask) 
       best_cost = cost;
     }
   }
+  // Dense head dim 64 with at least one query tile per SM: two ranges run as
+  // balanced segments (one CTA per SM takes an equal share of the (query
+  // tile, key tile) units, in up to three segments, each with its fixed cost).
+  if (!block_mask && p->D == 64 && ctas >= slots) {
+    const double seg = static_cast<double>(ctas) * tiles / slots + 2.0 * kFixed + merge_per_split * 2.0;
+    if (seg < best_cost) best = 2;
+  }
   const int64_t n = best;
   return n < 2 ? 1 : static_cast<int>(n);
 }

@@ -112,6 +112,8 @@ struct Params {
   int tps;           // dense: key tiles per range
   float* ws_o;       // nsplit >= 2: fp32 partial O [nsplit][B][H][Sq][D]
   float* ws_l;       //              fp32 partial LSE [nsplit][B][H][Sq]
+  int64_t seg_units;  // > 0 (nsplit == 2): balanced segments over B*H*seg_nqt*n_tiles units
+  int seg_nqt;        // query tiles of kM*QS rows per (b, h)
   int B;
   // QRAW kernels: RMSNorm + RoPE of the Q rows before the in-kernel quantization
   int q_pro;          // 1: apply the fields below
@@ -141,6 +143,10 @@ struct Layout {
   // committed once, after the last P V, in every kernel: the epilogue waits
   // on its single phase.
   static constexpr bool DBS = QS == 1;
+  // dense single-CTA head-dim-64 kernels can take a balanced share of the
+  // (query tile, key tile) units in segments (Params::seg_units; not with the
+  // in-kernel Q quantization, whose registers the segment loop would spill)
+  static constexpr bool SEGOK = D == 64 && QS == 2 && !PAIR && !SPARSE && !ROWMASK;
   static constexpr int NSB = DBS ? 2 : QS;  // S buffers in TMEM
   static constexpr int KROWS = PAIR ? BN / 2 : BN;  // keys of a K tile held here
   static constexpr int VCOLS = PAIR ? D / 2 : D;    // V columns held here
@@ -528,22 +534,22 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
 // even-ranked CTA issues 256-row MMAs over both (cta_group::2).
 // KB: per-64-key-block K scales in the dense head-dim-64 kernel, folded into one
 // constant per block and row (see the softmax).
+// SEGM: the balanced-segment form (Params::seg_units), a separate
+// instantiation so that the one-range form keeps its own register allocation.
 template <int D, int QS, int BN, bool SPARSE, bool VBF16, bool QRAW, bool ROWMASK, bool PAIR,
-          bool KB = false>
+          bool KB = false, bool SEGM = false>
 __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_m, const Params a) {
   using L = Layout<D, QS, BN, SPARSE, ROWMASK, PAIR, KB>;
+  constexpr bool SEG = SEGM;
+  static_assert(!SEGM || (L::SEGOK && !QRAW), "segments: dense single-CTA head-dim-64, int8 Q");
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.y;
-  const int b = blockIdx.z / a.nsplit;
-  const int split = blockIdx.z % a.nsplit;
-  const int q0 = blockIdx.x * (kM * QS);
 
   if ((smem_u32(smem) & 1023u) != 0) {  // swizzled operands need 1024-byte alignment
     if (tid == 0) atomicOr(&g_attn_status, kErrSmemAlign);
@@ -566,846 +572,903 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
   const uint32_t peer_p = (PAIR && leader) ? 4u : 0u;
   const uint32_t peer_f = (PAIR && leader) ? 1u : 0u;
 
-  if (tid == 0) {
-    mbar_init(bar(L::B_QFULL), 1);
-    mbar_init(bar(L::B_QCONV), (QRAW ? QS * kM : 64) + peer_f);
-    for (int i = 0; i < L::NKS; ++i) {
-      mbar_init(bar(L::B_KRF + i), 1);
-      mbar_init(bar(L::B_KCF + i), 64 + peer_k);
-      mbar_init(bar(L::B_KCE + i), 1);
+  // Work of this CTA: one query tile and key range, or (a.seg_units > 0, dense
+  // single-CTA head-dim-64 kernels) an equal share of all (query tile, key
+  // tile) units: the contiguous run [x U / C, (x+1) U / C) of the units ordered
+  // by query tile, then key tile, cut into segments at query-tile boundaries.
+  // A segment that starts a query tile's keys writes partial 0, one that ends
+  // them partial 1 (a share of at least n_tiles units meets each query tile
+  // at most twice); one that covers all of them writes partial 0 and marks
+  // partial 1 empty. The body below runs once per segment; TMEM stays
+  // allocated, the barriers are initialised again.
+  // (a trip count of one for the kernels without segments: no loop is left there)
+  for (int seg = 0; seg < (SEG ? INT_MAX : 1); ++seg) {
+    // segment seg: key tiles [seg_k0, seg_k1) of one query tile
+    int seg_b = 0, seg_h = 0, seg_q0 = 0, seg_k0 = 0, seg_k1 = 0;
+    if constexpr (SEG) {
+      if (a.seg_units > 0) {
+        // it starts at this CTA's first unit, then at each following query
+        // tile's first key tile (recomputed, not carried across segments)
+        const int64_t u0 = static_cast<int64_t>(blockIdx.x) * a.seg_units / gridDim.x;
+        const int64_t u1 = static_cast<int64_t>(blockIdx.x + 1) * a.seg_units / gridDim.x;
+        const int64_t us = seg == 0 ? u0 : (u0 / a.n_tiles + seg) * a.n_tiles;
+        if (us >= u1) break;
+        const int64_t qt = us / a.n_tiles;
+        seg_k0 = static_cast<int>(us - qt * a.n_tiles);
+        seg_k1 = static_cast<int>(min(static_cast<int64_t>(a.n_tiles), seg_k0 + (u1 - us)));
+        const int bh = static_cast<int>(qt / a.seg_nqt);
+        seg_q0 = static_cast<int>(qt % a.seg_nqt) * (kM * QS);
+        seg_h = bh % a.H;
+        seg_b = bh / a.H;
+      } else if (seg > 0) {
+        break;
+      }
     }
-    for (int i = 0; i < L::NRS; ++i) mbar_init(bar(L::B_KRE + i), 64);
-    for (int i = 0; i < L::NVS; ++i) {
-      mbar_init(bar(L::B_VF + i), 1 + peer_f);
-      mbar_init(bar(L::B_VE + i), 1);
+    const bool segd = SEG && a.seg_units > 0;
+    const int h = segd ? seg_h : static_cast<int>(blockIdx.y);
+    const int b = segd ? seg_b : static_cast<int>(blockIdx.z) / a.nsplit;
+    const int split = segd ? (seg_k0 == 0 ? 0 : 1) : static_cast<int>(blockIdx.z) % a.nsplit;
+    const int q0 = segd ? seg_q0 : static_cast<int>(blockIdx.x) * (kM * QS);
+    const bool seg_full = segd && seg_k0 == 0 && seg_k1 == a.n_tiles;
+    if (seg > 0) {
+      // every role has finished the last segment: its copies landed, its
+      // MMAs completed (the issuer's drain), its barriers have no waiter
+      tc_fence_before();
+      __syncthreads();
+      if (*abort_flag) break;
+      if (tid == 0)
+        for (int i = 0; i < L::NBAR; ++i) mbar_inval(bar(i));
     }
-    for (int i = 0; i < L::NSC; ++i) {
-      mbar_init(bar(L::B_SCF + i), 64);
-      mbar_init(bar(L::B_SCE + i), 4 * QS);
+    if (tid == 0) {
+      mbar_init(bar(L::B_QFULL), 1);
+      mbar_init(bar(L::B_QCONV), (QRAW ? QS * kM : 64) + peer_f);
+      for (int i = 0; i < L::NKS; ++i) {
+        mbar_init(bar(L::B_KRF + i), 1);
+        mbar_init(bar(L::B_KCF + i), 64 + peer_k);
+        mbar_init(bar(L::B_KCE + i), 1);
+      }
+      for (int i = 0; i < L::NRS; ++i) mbar_init(bar(L::B_KRE + i), 64);
+      for (int i = 0; i < L::NVS; ++i) {
+        mbar_init(bar(L::B_VF + i), 1 + peer_f);
+        mbar_init(bar(L::B_VE + i), 1);
+      }
+      for (int i = 0; i < L::NSC; ++i) {
+        mbar_init(bar(L::B_SCF + i), 64);
+        mbar_init(bar(L::B_SCE + i), 4 * QS);
+      }
+      for (int s = 0; s < L::NSB; ++s) {
+        mbar_init(bar(L::B_SF + s), 1);
+        mbar_init(bar(L::B_PF + s), kM + peer_p);
+      }
+      for (int s = 0; s < QS; ++s) mbar_init(bar(L::B_OF + s), 1);
+      mbar_init(bar(L::B_PVT), 1);
+      for (int i = 0; i < L::NSC; ++i) mbar_init(bar(L::B_MF + i), 1);
+      mbar_init(bar(L::B_DRAIN), 1);
+      mbar_init(bar(L::B_STALL), 1);  // never signalled: the timeout test hook waits on it
+      misc[1] = 0;
+      fence_mbar_init();
     }
-    for (int s = 0; s < L::NSB; ++s) {
-      mbar_init(bar(L::B_SF + s), 1);
-      mbar_init(bar(L::B_PF + s), kM + peer_p);
+    if (seg == 0 && warp == L::W_MMA) {  // TMEM stays allocated for every segment
+      if constexpr (PAIR) {
+        tmem_alloc_pair(smem_u32(misc), L::TMEM_COLS);
+        tmem_relinquish_pair();
+      } else {
+        tmem_alloc(smem_u32(misc), L::TMEM_COLS);
+        tmem_relinquish();
+      }
     }
-    for (int s = 0; s < QS; ++s) mbar_init(bar(L::B_OF + s), 1);
-    mbar_init(bar(L::B_PVT), 1);
-    for (int i = 0; i < L::NSC; ++i) mbar_init(bar(L::B_MF + i), 1);
-    mbar_init(bar(L::B_DRAIN), 1);
-    mbar_init(bar(L::B_STALL), 1);  // never signalled: the timeout test hook waits on it
-    misc[1] = 0;
-    fence_mbar_init();
-  }
-  if (warp == L::W_MMA) {
-    if constexpr (PAIR) {
-      tmem_alloc_pair(smem_u32(misc), L::TMEM_COLS);
-      tmem_relinquish_pair();
+    float* vsc = reinterpret_cast<float*>(smem + L::OFF_VS);
+    for (int i = tid; i < D; i += blockDim.x) vsc[i] = a.v_scale ? __ldg(a.v_scale + h * D + i) : 1.f;
+    if constexpr (L::ONES) {  // the row-sum columns of V: 1.0 in V's type
+      const uint32_t one2 = VBF16 ? 0x3F803F80u : 0x3C003C00u;
+      uint4* ones = reinterpret_cast<uint4*>(smem + L::OFF_ONES);
+      for (int i = tid; i < L::NVS * L::VB / 16; i += blockDim.x) ones[i] = make_uint4(one2, one2, one2, one2);
+      fence_proxy_async_smem();
+    }
+
+    // Key tiles this CTA visits: all of them (dense) or the union of the kept
+    // tiles of its two 64-row query tiles, in ascending order (block-sparse).
+    uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::OFF_LIST);
+    int n_it, it0;
+    const int qt0 = q0 / 64;
+    const int qt1 = qt0 + 1;
+    if constexpr (SPARSE) {
+      const uint8_t* m0 = a.mask + (static_cast<int64_t>(b * a.H + h) * a.Tq + qt0) * a.Tk;
+      const uint8_t* m1 = qt1 < a.Tq ? m0 + a.Tk : nullptr;
+      int* wcnt = reinterpret_cast<int*>(smem + L::OFF_MISC + 16);
+      int total = 0;
+      const int nw = blockDim.x >> 5;
+      for (int base = 0; base < a.Tk; base += blockDim.x) {
+        const int t = base + tid;
+        const bool keep = t < a.Tk && (m0[t] != 0 || (m1 != nullptr && m1[t] != 0));
+        const unsigned bal = __ballot_sync(0xffffffffu, keep);
+        if (lane == 0) wcnt[warp] = __popc(bal);
+        __syncthreads();
+        int before = total;
+        for (int w = 0; w < warp; ++w) before += wcnt[w];
+        if (keep) list[before + __popc(bal & ((1u << lane) - 1u))] = static_cast<uint16_t>(t);
+        for (int w = 0; w < nw; ++w) total += wcnt[w];
+        __syncthreads();
+      }
+      // this CTA's share of the kept-tile list
+      const int per = (total + a.nsplit - 1) / a.nsplit;
+      it0 = split * per;
+      n_it = max(0, min(total - it0, per));
+    } else if (SEG && a.seg_units > 0) {
+      it0 = seg_k0;
+      n_it = seg_k1 - seg_k0;
     } else {
-      tmem_alloc(smem_u32(misc), L::TMEM_COLS);
-      tmem_relinquish();
+      it0 = split * a.tps;
+      n_it = max(0, min(a.n_tiles - it0, a.tps));
     }
-  }
-  float* vsc = reinterpret_cast<float*>(smem + L::OFF_VS);
-  for (int i = tid; i < D; i += blockDim.x) vsc[i] = a.v_scale ? __ldg(a.v_scale + h * D + i) : 1.f;
-  if constexpr (L::ONES) {  // the row-sum columns of V: 1.0 in V's type
-    const uint32_t one2 = VBF16 ? 0x3F803F80u : 0x3C003C00u;
-    uint4* ones = reinterpret_cast<uint4*>(smem + L::OFF_ONES);
-    for (int i = tid; i < L::NVS * L::VB / 16; i += blockDim.x) ones[i] = make_uint4(one2, one2, one2, one2);
-    fence_proxy_async_smem();
-  }
+    tc_fence_before();
+    __syncthreads();
+    // a pair's barriers take arrivals from both CTAs: both are initialised first
+    if constexpr (PAIR) cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    if (tid == 0) IA_TRACE_POINT(14, 1);
 
-  // Key tiles this CTA visits: all of them (dense) or the union of the kept
-  // tiles of its two 64-row query tiles, in ascending order (block-sparse).
-  uint16_t* list = reinterpret_cast<uint16_t*>(smem + L::OFF_LIST);
-  int n_it, it0;
-  const int qt0 = q0 / 64;
-  const int qt1 = qt0 + 1;
-  if constexpr (SPARSE) {
-    const uint8_t* m0 = a.mask + (static_cast<int64_t>(b * a.H + h) * a.Tq + qt0) * a.Tk;
-    const uint8_t* m1 = qt1 < a.Tq ? m0 + a.Tk : nullptr;
-    int* wcnt = reinterpret_cast<int*>(smem + L::OFF_MISC + 16);
-    int total = 0;
-    const int nw = blockDim.x >> 5;
-    for (int base = 0; base < a.Tk; base += blockDim.x) {
-      const int t = base + tid;
-      const bool keep = t < a.Tk && (m0[t] != 0 || (m1 != nullptr && m1[t] != 0));
-      const unsigned bal = __ballot_sync(0xffffffffu, keep);
-      if (lane == 0) wcnt[warp] = __popc(bal);
-      __syncthreads();
-      int before = total;
-      for (int w = 0; w < warp; ++w) before += wcnt[w];
-      if (keep) list[before + __popc(bal & ((1u << lane) - 1u))] = static_cast<uint16_t>(t);
-      for (int w = 0; w < nw; ++w) total += wcnt[w];
-      __syncthreads();
-    }
-    // this CTA's share of the kept-tile list
-    const int per = (total + a.nsplit - 1) / a.nsplit;
-    it0 = split * per;
-    n_it = max(0, min(total - it0, per));
-  } else {
-    it0 = split * a.tps;
-    n_it = max(0, min(a.n_tiles - it0, a.tps));
-  }
-  tc_fence_before();
-  __syncthreads();
-  // a pair's barriers take arrivals from both CTAs: both are initialised first
-  if constexpr (PAIR) cluster_sync();
-  tc_fence_after();
-  const uint32_t tmem = misc[0];
-  if (tid == 0) IA_TRACE_POINT(14, 1);
+    const uint32_t sm_qh = smem_u32(smem + L::OFF_QH);
+    const uint32_t sm_kh = smem_u32(smem + L::OFF_KH);
+    const uint32_t sm_v = smem_u32(smem + L::OFF_V);
+    const uint32_t sm_kr = smem_u32(smem + L::OFF_KR);
 
-  const uint32_t sm_qh = smem_u32(smem + L::OFF_QH);
-  const uint32_t sm_kh = smem_u32(smem + L::OFF_KH);
-  const uint32_t sm_v = smem_u32(smem + L::OFF_V);
-  const uint32_t sm_kr = smem_u32(smem + L::OFF_KR);
-
-  if (warp == L::W_PROD) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      if (ROWMASK) prefetch_tmap(&tm_m);
-      int kr_last[L::NKS], v_last[L::NVS], m_last[L::NSC];
-      for (int i = 0; i < L::NKS; ++i) kr_last[i] = -1;
-      for (int i = 0; i < L::NVS; ++i) v_last[i] = -1;
-      for (int i = 0; i < L::NSC; ++i) m_last[i] = -1;
-      // per-row mask boxes: 128-byte rows of 32 fp32, 64 16-bit or 128 bool keys
-      const int m_kpb = a.rm_dtype == IA_MASK_F32 ? 32 : a.rm_dtype == IA_MASK_BOOL ? 128 : 64;
-      const int m_nbox = a.rm_dtype == IA_MASK_F32 ? 2 : 1;
-      const int m_h = a.rm_h ? h : 0, m_b = a.rm_b ? b : 0;
-      // int8 Q codes, or 16-bit Q rows that the softmax warps quantize; either
-      // way they are staged in the V buffers until converted
-      constexpr int QB = QRAW ? 2 : 1;
-      const uint32_t sm_qin = smem_u32(smem + L::OFF_QIN);
-      mbar_arrive_expect_tx(bar(L::B_QFULL), QS * kM * D * QB);
-      IA_TRACE_POINT(14, 2);
-      for (int s = 0; s < QS; ++s)
-        tma_load_4d(sm_qin + s * L::QR * QB, &tm_q, bar(L::B_QFULL), 0, q0 + s * kM, h, b);
-      bool ok = true;
-      for (int it = 0; it < n_it; ++it) {
-        const int kt = SPARSE ? static_cast<int>(list[it0 + it]) : it0 + it;
-        // int8 K tile: into its fp16 buffer (in place) or a staging buffer
-        const int ks = it % L::NKS;
-        uint32_t kdst;
-        if constexpr (L::INPLACE) {
-          if (it >= L::NKS) ok = wait_bar(bar(L::B_KCE + ks), ((it / L::NKS) - 1) & 1, ctl, kErrProducer);
-          kdst = sm_kh + ks * L::KH + BN * 128;
-        } else {
-          const int rs = it % L::NRS;
-          if (it >= L::NRS) ok = wait_bar(bar(L::B_KRE + rs), ((it / L::NRS) - 1) & 1, ctl, kErrProducer);
-          kdst = sm_kr + rs * L::KR;
-        }
-        if (!ok) break;
-        mbar_arrive_expect_tx(bar(L::B_KRF + ks), L::KROWS * D);
-        tma_load_4d(kdst, &tm_k, bar(L::B_KRF + ks), 0, kt * BN + static_cast<int>(crank) * L::KROWS, h, b);
-        kr_last[ks] = it;
-        const int vs = it % L::NVS;
-        if (!PAIR && (it == 0 || (QRAW && it < L::NVS)))  // raw Q sits in V buffer 0 (all of them)
-          ok = wait_bar(bar(L::B_QCONV), 0, ctl, kErrProducer);
-        else if (it >= L::NVS)
-          ok = wait_bar(bar(L::B_VE + vs), ((it / L::NVS) - 1) & 1, ctl, kErrProducer);
-        if (!ok) break;
-        mbar_arrive_expect_tx(bar(L::B_VF + vs), BN * L::VCOLS * 2);
-#pragma unroll
-        for (int c = 0; c < L::VCOLS / 64; ++c)
-          tma_load_4d(sm_v + vs * L::VB + c * BN * 128, &tm_v, bar(L::B_VF + vs),
-                      static_cast<int>(crank) * L::VCOLS + c * 64, kt * BN, h, b);
-        v_last[vs] = it;
-        if constexpr (ROWMASK) {  // the tile's mask rows, released with the tile's k scales
-          const int ms = it % L::NSC;
-          if (it >= L::NSC) ok = wait_bar(bar(L::B_SCE + ms), ((it / L::NSC) - 1) & 1, ctl, kErrProducer);
+    if (warp == L::W_PROD) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        if (ROWMASK) prefetch_tmap(&tm_m);
+        int kr_last[L::NKS], v_last[L::NVS], m_last[L::NSC];
+        for (int i = 0; i < L::NKS; ++i) kr_last[i] = -1;
+        for (int i = 0; i < L::NVS; ++i) v_last[i] = -1;
+        for (int i = 0; i < L::NSC; ++i) m_last[i] = -1;
+        // per-row mask boxes: 128-byte rows of 32 fp32, 64 16-bit or 128 bool keys
+        const int m_kpb = a.rm_dtype == IA_MASK_F32 ? 32 : a.rm_dtype == IA_MASK_BOOL ? 128 : 64;
+        const int m_nbox = a.rm_dtype == IA_MASK_F32 ? 2 : 1;
+        const int m_h = a.rm_h ? h : 0, m_b = a.rm_b ? b : 0;
+        // int8 Q codes, or 16-bit Q rows that the softmax warps quantize; either
+        // way they are staged in the V buffers until converted
+        constexpr int QB = QRAW ? 2 : 1;
+        const uint32_t sm_qin = smem_u32(smem + L::OFF_QIN);
+        mbar_arrive_expect_tx(bar(L::B_QFULL), QS * kM * D * QB);
+        IA_TRACE_POINT(14, 2);
+        for (int s = 0; s < QS; ++s)
+          tma_load_4d(sm_qin + s * L::QR * QB, &tm_q, bar(L::B_QFULL), 0, q0 + s * kM, h, b);
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+          const int kt = SPARSE ? static_cast<int>(list[it0 + it]) : it0 + it;
+          // int8 K tile: into its fp16 buffer (in place) or a staging buffer
+          const int ks = it % L::NKS;
+          uint32_t kdst;
+          if constexpr (L::INPLACE) {
+            if (it >= L::NKS) ok = wait_bar(bar(L::B_KCE + ks), ((it / L::NKS) - 1) & 1, ctl, kErrProducer);
+            kdst = sm_kh + ks * L::KH + BN * 128;
+          } else {
+            const int rs = it % L::NRS;
+            if (it >= L::NRS) ok = wait_bar(bar(L::B_KRE + rs), ((it / L::NRS) - 1) & 1, ctl, kErrProducer);
+            kdst = sm_kr + rs * L::KR;
+          }
           if (!ok) break;
-          mbar_arrive_expect_tx(bar(L::B_MF + ms), m_nbox * kM * 128);
-          for (int x = 0; x < m_nbox; ++x)
-            tma_load_4d(smem_u32(smem + L::OFF_MK + ms * L::MB + x * kM * 128), &tm_m,
-                        bar(L::B_MF + ms), kt * BN + x * m_kpb, q0, m_h, m_b);
-          m_last[ms] = it;
+          mbar_arrive_expect_tx(bar(L::B_KRF + ks), L::KROWS * D);
+          tma_load_4d(kdst, &tm_k, bar(L::B_KRF + ks), 0, kt * BN + static_cast<int>(crank) * L::KROWS, h, b);
+          kr_last[ks] = it;
+          const int vs = it % L::NVS;
+          if (!PAIR && (it == 0 || (QRAW && it < L::NVS)))  // raw Q sits in V buffer 0 (all of them)
+            ok = wait_bar(bar(L::B_QCONV), 0, ctl, kErrProducer);
+          else if (it >= L::NVS)
+            ok = wait_bar(bar(L::B_VE + vs), ((it / L::NVS) - 1) & 1, ctl, kErrProducer);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar(L::B_VF + vs), BN * L::VCOLS * 2);
+  #pragma unroll
+          for (int c = 0; c < L::VCOLS / 64; ++c)
+            tma_load_4d(sm_v + vs * L::VB + c * BN * 128, &tm_v, bar(L::B_VF + vs),
+                        static_cast<int>(crank) * L::VCOLS + c * 64, kt * BN, h, b);
+          v_last[vs] = it;
+          if constexpr (ROWMASK) {  // the tile's mask rows, released with the tile's k scales
+            const int ms = it % L::NSC;
+            if (it >= L::NSC) ok = wait_bar(bar(L::B_SCE + ms), ((it / L::NSC) - 1) & 1, ctl, kErrProducer);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar(L::B_MF + ms), m_nbox * kM * 128);
+            for (int x = 0; x < m_nbox; ++x)
+              tma_load_4d(smem_u32(smem + L::OFF_MK + ms * L::MB + x * kM * 128), &tm_m,
+                          bar(L::B_MF + ms), kt * BN + x * m_kpb, q0, m_h, m_b);
+            m_last[ms] = it;
+          }
+        }
+        if (((PAIR && !leader) || SEG) && ok) {
+          // The last V-empty commits (in a pair, the leader's, which arrive here
+          // too) have no other waiter: take them before this CTA may exit or
+          // its barriers are initialised for the next segment.
+          for (int t = max(0, n_it - L::NVS); t < n_it - 1; ++t)
+            drain_bar(bar(L::B_VE + t % L::NVS), (t / L::NVS) & 1, a.timeout_ns);
+        }
+        if (!ok) {  // let issued copies land before the CTA's shared memory goes away
+          drain_bar(bar(L::B_QFULL), 0, a.timeout_ns);
+          for (int i = 0; i < L::NKS; ++i)
+            if (kr_last[i] >= 0) drain_bar(bar(L::B_KRF + i), (kr_last[i] / L::NKS) & 1, a.timeout_ns);
+          for (int i = 0; i < L::NVS; ++i)
+            if (v_last[i] >= 0) drain_bar(bar(L::B_VF + i), (v_last[i] / L::NVS) & 1, a.timeout_ns);
+          for (int i = 0; i < L::NSC; ++i)
+            if (m_last[i] >= 0) drain_bar(bar(L::B_MF + i), (m_last[i] / L::NSC) & 1, a.timeout_ns);
         }
       }
-      if (PAIR && !leader && ok) {
-        // The leader's last V-empty commits arrive here too and nothing else
-        // waits for them: take them before this CTA may exit.
-        for (int t = max(0, n_it - L::NVS); t < n_it - 1; ++t)
-          drain_bar(bar(L::B_VE + t % L::NVS), (t / L::NVS) & 1, a.timeout_ns);
-      }
-      if (!ok) {  // let issued copies land before the CTA's shared memory goes away
-        drain_bar(bar(L::B_QFULL), 0, a.timeout_ns);
-        for (int i = 0; i < L::NKS; ++i)
-          if (kr_last[i] >= 0) drain_bar(bar(L::B_KRF + i), (kr_last[i] / L::NKS) & 1, a.timeout_ns);
-        for (int i = 0; i < L::NVS; ++i)
-          if (v_last[i] >= 0) drain_bar(bar(L::B_VF + i), (v_last[i] / L::NVS) & 1, a.timeout_ns);
-        for (int i = 0; i < L::NSC; ++i)
-          if (m_last[i] >= 0) drain_bar(bar(L::B_MF + i), (m_last[i] / L::NSC) & 1, a.timeout_ns);
-      }
-    }
-  } else if (warp == L::W_MMA) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0 && PAIR && !leader) {
-      // The peer issues no MMA: its lane forwards the completion of its Q
-      // conversion and of each V tile's copy to the leader's barriers.
-      bool ok = wait_bar(bar(L::B_QCONV), 0, ctl, kErrMma);
-      if (ok) mbar_arrive_remote(lbar(L::B_QCONV));
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int vs = it % L::NVS;
-        ok = wait_bar(bar(L::B_VF + vs), (it / L::NVS) & 1, ctl, kErrMma);
-        if (ok) mbar_arrive_remote(lbar(L::B_VF + vs));
-      }
-      // The leader's last commit reaches this CTA too, after every earlier
-      // one (and after all of the pair's MMAs, which read this CTA's shared
-      // memory and TMEM): wait for it before this CTA may leave, on the
-      // normal path and after an abort alike.
-      drain_bar(bar(L::B_DRAIN), 0, a.timeout_ns);
-    } else if (lane == 0) {
-      constexpr int MM = PAIR ? 2 * kM : kM;  // rows of one MMA
-      constexpr uint32_t idq = idesc_f16(MM, BN, 0, 0, 0, 0);                  // f16 x f16, K-major
-      constexpr uint32_t idv = idesc_f16(MM, L::OW, VBF16 ? 1 : 0, VBF16 ? 1 : 0, 0, 1);  // V MN-major
-      // Descriptors are built once; a k-step or buffer offset is added to the
-      // 14-bit start-address field (16-byte units), which cannot overflow for
-      // addresses inside the CTA's shared memory. This keeps the issuing
-      // thread to a few instructions per MMA.
-      const uint64_t qdesc = sdesc_sw128(sm_qh, 16, 1024);
-      const uint64_t kdesc = sdesc_sw128(sm_kh, 16, 1024);
-      // V's 64-column blocks are BN*128 bytes apart; the ones block sits at the
-      // same distance from every V buffer
-      const uint64_t vdesc = sdesc_sw128(sm_v, L::ONES ? L::OFF_ONES - L::OFF_V : BN * 128, 1024);
-      // a barrier that also counts the peer's arrivals
-      auto wait_in = [&](int i, uint32_t parity) { return wait_bar(bar(i), parity, ctl, kErrMma); };
-      auto commit = [&](int i) {
-        if constexpr (PAIR) mma_commit_pair(bar(i), 3);
-        else mma_commit(bar(i));
-      };
-      // S buffer sb <- Q_s K^T (K from stage kst)
-      auto issue_qk = [&](int s, int kst, int sb) {
-        const uint64_t qa = qdesc + static_cast<uint64_t>((s * L::QH) >> 4);
-        const uint64_t kb = kdesc + static_cast<uint64_t>((kst * L::KH) >> 4);
-        const uint32_t dt = tmem + sb * BN;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = qa + static_cast<uint64_t>(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
-          const uint64_t bd = kb + static_cast<uint64_t>(((kk >> 2) * (L::KROWS * 128) + (kk & 3) * 32) >> 4);
-          if constexpr (PAIR) mma_ss_pair(dt, ad, bd, idq, kk > 0 ? 1u : 0u);
-          else mma_ss(dt, ad, bd, idq, kk > 0 ? 1u : 0u);
-        }
-      };
-      // O_s += P V (P from S buffer sb, V from stage vs)
-      auto issue_pv = [&](int s, int vs, bool first, int sb) {
-        const uint64_t vb = vdesc + static_cast<uint64_t>((vs * L::VB) >> 4);
-        const uint32_t dt = tmem + L::NSB * BN + s * L::OW;
-        const uint32_t pt = tmem + sb * BN;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bd = vb + static_cast<uint64_t>((kk * 16 * 128) >> 4);
-          if constexpr (PAIR) mma_ts_pair(dt, pt + kk * 8, bd, idv, (first && kk == 0) ? 0u : 1u);
-          else mma_ts(dt, pt + kk * 8, bd, idv, (first && kk == 0) ? 0u : 1u);
-        }
-      };
-      bool ok = wait_in(L::B_QCONV, 0);
-      IA_TRACE_POINT(14, 5);
-      if (ok && a.debug_stall) ok = wait_bar(bar(L::B_STALL), 0, ctl, kErrMma);
-      tc_fence_after();
-      if constexpr (L::DBS) {
-        // QK^T of tiles 0 and 1, then per tile j: P_j V_j, and the QK^T of
-        // tile j+2 into the S buffer that P_j V_j has just read
-        auto qk_step = [&](int j) -> bool {
-          const int kst = j % L::NKS;
-          if (!wait_in(L::B_KCF + kst, (j / L::NKS) & 1)) return false;
-          tc_fence_after();
-          issue_qk(0, kst, j & 1);
-          commit(L::B_SF + (j & 1));
-          commit(L::B_KCE + kst);
-          return true;
-        };
-        for (int j = 0; j < 2 && j < n_it && ok; ++j) ok = qk_step(j);
+    } else if (warp == L::W_MMA) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0 && PAIR && !leader) {
+        // The peer issues no MMA: its lane forwards the completion of its Q
+        // conversion and of each V tile's copy to the leader's barriers.
+        bool ok = wait_bar(bar(L::B_QCONV), 0, ctl, kErrMma);
+        if (ok) mbar_arrive_remote(lbar(L::B_QCONV));
         for (int it = 0; it < n_it && ok; ++it) {
           const int vs = it % L::NVS;
-          ok = wait_in(L::B_VF + vs, (it / L::NVS) & 1);
-          if (ok) ok = wait_bar(bar(L::B_PF + (it & 1)), (it >> 1) & 1, ctl, kErrMma);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(0, vs, it == 0, it & 1);
-          commit(L::B_PVT);  // one phase per tile
-          commit(L::B_VE + vs);
-          if (it + 2 < n_it) ok = qk_step(it + 2);
+          ok = wait_bar(bar(L::B_VF + vs), (it / L::NVS) & 1, ctl, kErrMma);
+          if (ok) mbar_arrive_remote(lbar(L::B_VF + vs));
         }
-        if (ok && n_it > 0) commit(L::B_OF);  // after the last P V: the epilogue's one phase
-      }
-      for (int it = 0; it < n_it && ok && !L::DBS; ++it) {
-        const int kst = it % L::NKS;
-        IA_TRACE_POINT(8, it);
-        ok = wait_in(L::B_KCF + kst, (it / L::NKS) & 1);
-        if (!ok) break;
-        IA_TRACE_POINT(9, it);
+        // The leader's last commit reaches this CTA too, after every earlier
+        // one (and after all of the pair's MMAs, which read this CTA's shared
+        // memory and TMEM): wait for it before this CTA may leave, on the
+        // normal path and after an abort alike.
+        drain_bar(bar(L::B_DRAIN), 0, a.timeout_ns);
+      } else if (lane == 0) {
+        constexpr int MM = PAIR ? 2 * kM : kM;  // rows of one MMA
+        constexpr uint32_t idq = idesc_f16(MM, BN, 0, 0, 0, 0);                  // f16 x f16, K-major
+        constexpr uint32_t idv = idesc_f16(MM, L::OW, VBF16 ? 1 : 0, VBF16 ? 1 : 0, 0, 1);  // V MN-major
+        // Descriptors are built once; a k-step or buffer offset is added to the
+        // 14-bit start-address field (16-byte units), which cannot overflow for
+        // addresses inside the CTA's shared memory. This keeps the issuing
+        // thread to a few instructions per MMA.
+        const uint64_t qdesc = sdesc_sw128(sm_qh, 16, 1024);
+        const uint64_t kdesc = sdesc_sw128(sm_kh, 16, 1024);
+        // V's 64-column blocks are BN*128 bytes apart; the ones block sits at the
+        // same distance from every V buffer
+        const uint64_t vdesc = sdesc_sw128(sm_v, L::ONES ? L::OFF_ONES - L::OFF_V : BN * 128, 1024);
+        // a barrier that also counts the peer's arrivals
+        auto wait_in = [&](int i, uint32_t parity) { return wait_bar(bar(i), parity, ctl, kErrMma); };
+        auto commit = [&](int i) {
+          if constexpr (PAIR) mma_commit_pair(bar(i), 3);
+          else mma_commit(bar(i));
+        };
+        // S buffer sb <- Q_s K^T (K from stage kst)
+        auto issue_qk = [&](int s, int kst, int sb) {
+          const uint64_t qa = qdesc + static_cast<uint64_t>((s * L::QH) >> 4);
+          const uint64_t kb = kdesc + static_cast<uint64_t>((kst * L::KH) >> 4);
+          const uint32_t dt = tmem + sb * BN;
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t ad = qa + static_cast<uint64_t>(((kk >> 2) * (kM * 128) + (kk & 3) * 32) >> 4);
+            const uint64_t bd = kb + static_cast<uint64_t>(((kk >> 2) * (L::KROWS * 128) + (kk & 3) * 32) >> 4);
+            if constexpr (PAIR) mma_ss_pair(dt, ad, bd, idq, kk > 0 ? 1u : 0u);
+            else mma_ss(dt, ad, bd, idq, kk > 0 ? 1u : 0u);
+          }
+        };
+        // O_s += P V (P from S buffer sb, V from stage vs)
+        auto issue_pv = [&](int s, int vs, bool first, int sb) {
+          const uint64_t vb = vdesc + static_cast<uint64_t>((vs * L::VB) >> 4);
+          const uint32_t dt = tmem + L::NSB * BN + s * L::OW;
+          const uint32_t pt = tmem + sb * BN;
+  #pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t bd = vb + static_cast<uint64_t>((kk * 16 * 128) >> 4);
+            if constexpr (PAIR) mma_ts_pair(dt, pt + kk * 8, bd, idv, (first && kk == 0) ? 0u : 1u);
+            else mma_ts(dt, pt + kk * 8, bd, idv, (first && kk == 0) ? 0u : 1u);
+          }
+        };
+        bool ok = wait_in(L::B_QCONV, 0);
+        IA_TRACE_POINT(14, 5);
+        if (ok && a.debug_stall) ok = wait_bar(bar(L::B_STALL), 0, ctl, kErrMma);
         tc_fence_after();
-        const int pvs = (it + L::NVS - 1) % L::NVS;
-        if (it > 0) {
-          ok = wait_in(L::B_VF + pvs, ((it - 1) / L::NVS) & 1);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        for (int s = 0; s < QS && ok; ++s) {
-          if (it > 0) {
-            ok = wait_bar(bar(L::B_PF + s), (it - 1) & 1, ctl, kErrMma);
+        if constexpr (L::DBS) {
+          // QK^T of tiles 0 and 1, then per tile j: P_j V_j, and the QK^T of
+          // tile j+2 into the S buffer that P_j V_j has just read
+          auto qk_step = [&](int j) -> bool {
+            const int kst = j % L::NKS;
+            if (!wait_in(L::B_KCF + kst, (j / L::NKS) & 1)) return false;
+            tc_fence_after();
+            issue_qk(0, kst, j & 1);
+            commit(L::B_SF + (j & 1));
+            commit(L::B_KCE + kst);
+            return true;
+          };
+          for (int j = 0; j < 2 && j < n_it && ok; ++j) ok = qk_step(j);
+          for (int it = 0; it < n_it && ok; ++it) {
+            const int vs = it % L::NVS;
+            ok = wait_in(L::B_VF + vs, (it / L::NVS) & 1);
+            if (ok) ok = wait_bar(bar(L::B_PF + (it & 1)), (it >> 1) & 1, ctl, kErrMma);
             if (!ok) break;
             tc_fence_after();
-            issue_pv(s, pvs, it == 1, s);
+            issue_pv(0, vs, it == 0, it & 1);
+            commit(L::B_PVT);  // one phase per tile
+            commit(L::B_VE + vs);
+            if (it + 2 < n_it) ok = qk_step(it + 2);
           }
-          issue_qk(s, kst, s);
-          commit(L::B_SF + s);
-          IA_TRACE_POINT(10 + s, it);
+          if (ok && n_it > 0) commit(L::B_OF);  // after the last P V: the epilogue's one phase
         }
-        if (!ok) break;
-        commit(L::B_KCE + kst);
-        if (it > 0) commit(L::B_VE + pvs);
-      }
-      if (ok && n_it > 0 && !L::DBS) {
-        const int pvs = (n_it - 1) % L::NVS;
-        ok = wait_in(L::B_VF + pvs, ((n_it - 1) / L::NVS) & 1);
-        if (ok) tc_fence_after();
-        for (int s = 0; s < QS && ok; ++s) {
-          ok = wait_bar(bar(L::B_PF + s), (n_it - 1) & 1, ctl, kErrMma);
+        for (int it = 0; it < n_it && ok && !L::DBS; ++it) {
+          const int kst = it % L::NKS;
+          IA_TRACE_POINT(8, it);
+          ok = wait_in(L::B_KCF + kst, (it / L::NKS) & 1);
           if (!ok) break;
+          IA_TRACE_POINT(9, it);
           tc_fence_after();
-          issue_pv(s, pvs, n_it == 1, s);
-          commit(L::B_OF + s);
+          const int pvs = (it + L::NVS - 1) % L::NVS;
+          if (it > 0) {
+            ok = wait_in(L::B_VF + pvs, ((it - 1) / L::NVS) & 1);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          for (int s = 0; s < QS && ok; ++s) {
+            if (it > 0) {
+              ok = wait_bar(bar(L::B_PF + s), (it - 1) & 1, ctl, kErrMma);
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(s, pvs, it == 1, s);
+            }
+            issue_qk(s, kst, s);
+            commit(L::B_SF + s);
+            IA_TRACE_POINT(10 + s, it);
+          }
+          if (!ok) break;
+          commit(L::B_KCE + kst);
+          if (it > 0) commit(L::B_VE + pvs);
         }
+        if (ok && n_it > 0 && !L::DBS) {
+          const int pvs = (n_it - 1) % L::NVS;
+          ok = wait_in(L::B_VF + pvs, ((n_it - 1) / L::NVS) & 1);
+          if (ok) tc_fence_after();
+          for (int s = 0; s < QS && ok; ++s) {
+            ok = wait_bar(bar(L::B_PF + s), (n_it - 1) & 1, ctl, kErrMma);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(s, pvs, n_it == 1, s);
+            commit(L::B_OF + s);
+          }
+        }
+        // every MMA issued above has completed once this arrives (in both CTAs
+        // of a pair: the peer waits for it before it exits)
+        IA_TRACE_POINT(14, 7);
+        if constexpr (PAIR) mma_commit_pair(bar(L::B_DRAIN), 3);
+        else mma_commit(bar(L::B_DRAIN));
+        drain_bar(bar(L::B_DRAIN), 0, a.timeout_ns);
       }
-      // every MMA issued above has completed once this arrives (in both CTAs
-      // of a pair: the peer waits for it before it exits)
-      IA_TRACE_POINT(14, 7);
-      if constexpr (PAIR) mma_commit_pair(bar(L::B_DRAIN), 3);
-      else mma_commit(bar(L::B_DRAIN));
-      drain_bar(bar(L::B_DRAIN), 0, a.timeout_ns);
-    }
-  } else if (warp >= L::W_CONV) {
-    // ---------------------------------------------- int8 -> fp16 converters
-    const int ct = tid - L::W_CONV * 32;
-    bool ok = QRAW ? true : wait_bar(bar(L::B_QFULL), 0, ctl, kErrConverter);
-    if constexpr (PAIR) ok = __all_sync(0xffffffffu, ok);
-    if (ct == 0) IA_TRACE_POINT(14, 3);
-    if (ok && !QRAW) {
-      for (int s = 0; s < QS; ++s)
-        widen_tile<D, kM, false>(smem + L::OFF_QIN + s * L::QR, smem + L::OFF_QH + s * L::QH, ct);
-      fence_proxy_async_smem();
-      mbar_arrive(bar(L::B_QCONV));
-      if (ct == 0) IA_TRACE_POINT(14, 4);
-    }
-    const uint8_t* mrow0 = nullptr;
-    const uint8_t* mrow1 = nullptr;
-    if (SPARSE) {
-      mrow0 = a.mask + (static_cast<int64_t>(b * a.H + h) * a.Tq + qt0) * a.Tk;
-      mrow1 = qt1 < a.Tq ? mrow0 + a.Tk : nullptr;
-    }
-    const float* ksb = a.k_scale + b * a.ks_sb + h * a.ks_sh;
-    const void* brow = nullptr;  // this (b, h)'s row of per-key offsets
-    if (a.bias != nullptr) {
-      const int es = a.bias_dtype == IA_MASK_F32 ? 4 : a.bias_dtype == IA_MASK_BOOL ? 1 : 2;
-      brow = static_cast<const char*>(a.bias) + (b * a.bias_sb + h * a.bias_sh) * es;
-    }
-    for (int it = 0; it < n_it && ok; ++it) {
-      const int kt = SPARSE ? static_cast<int>(list[it0 + it]) : it0 + it;
-      // Per-key constants of this tile: the global loads are issued first and
-      // land while the K tile is widened.
-      constexpr int KPT = (BN + 63) / 64;  // keys per converter thread
-      float kv[KPT];
-      uint32_t braw[KPT];
-      bool kval[KPT];
-#pragma unroll
-      for (int e = 0; e < KPT; ++e) {
-        const int key = kt * BN + ct + 64 * e;
-        kval[e] = key < a.Sk && (a.kv_valid == nullptr || (key & 63) < __ldg(a.kv_valid + (key >> 6)));
-        kv[e] = kval[e] ? __ldg(ksb + (a.gran_block ? (key >> 6) : key)) : 0.f;
-        braw[e] = (kval[e] && brow != nullptr) ? key_bias_bits(brow, key, a.bias_dtype) : 0u;
-      }
-      // K tile: int8 -> fp16 codes in the swizzled layout the MMA reads
-      const int kst = it % L::NKS;
-      ok = wait_bar(bar(L::B_KRF + kst), (it / L::NKS) & 1, ctl, kErrConverter);
-      if constexpr (PAIR) ok = __all_sync(0xffffffffu, ok);  // warps stay converged
-      if (!ok) break;
-      if (ct == 0) IA_TRACE_POINT(12, it);
-      if constexpr (L::INPLACE) {
-        uint8_t* kh = smem + L::OFF_KH + kst * L::KH;
-        widen_tile<D, BN, true>(kh + BN * 128, kh, ct);
-      } else {
-        const int rs = it % L::NRS;
-        if (it >= L::NKS) ok = wait_bar(bar(L::B_KCE + kst), ((it / L::NKS) - 1) & 1, ctl, kErrConverter);
-        if constexpr (PAIR) ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        widen_tile<D, L::KROWS, false>(smem + L::OFF_KR + rs * L::KR, smem + L::OFF_KH + kst * L::KH, ct);
-        mbar_arrive(bar(L::B_KRE + rs));
-      }
-      if (ct == 0) IA_TRACE_POINT(13, it);
-      fence_proxy_async_smem();
-      if (PAIR && !leader) {  // the leader's MMA reads this half: one arrival per warp
-        __syncwarp();
-        if ((ct & 31) == 0) mbar_arrive_remote(lbar(L::B_KCF + kst));
-      } else {
-        mbar_arrive(bar(L::B_KCF + kst));
-      }
-      // k scales, bias * log2(e) (-inf past the valid keys) and tile flags
-      const int ss = it % L::NSC;
-      if (it >= L::NSC) ok = wait_bar(bar(L::B_SCE + ss), ((it / L::NSC) - 1) & 1, ctl, kErrConverter);
+    } else if (warp >= L::W_CONV) {
+      // ---------------------------------------------- int8 -> fp16 converters
+      const int ct = tid - L::W_CONV * 32;
+      bool ok = QRAW ? true : wait_bar(bar(L::B_QFULL), 0, ctl, kErrConverter);
       if constexpr (PAIR) ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      float* ksm = reinterpret_cast<float*>(smem + L::OFF_SC + ss * L::SC);
-      float* b2m = ksm + BN;
-      uint32_t* flg = reinterpret_cast<uint32_t*>(b2m + BN);
-      bool nonzero = false;  // a valid key of this thread has a nonzero offset
-#pragma unroll
-      for (int e = 0; e < KPT; ++e) {
-        if (ct + 64 * e < BN) {
-          const float off =
-              kval[e] ? (brow ? key_bias_value(braw[e], a.bias_dtype) * kLog2e : 0.f) : -INFINITY;
-          ksm[ct + 64 * e] = kv[e];
-          b2m[ct + 64 * e] = off;
-          nonzero |= kval[e] && off != 0.f;
-        }
-      }
-      // Each converter warp records whether its keys carry any offset: a tile
-      // whose offsets are all zero (e.g. the core of a window's bias) keeps the
-      // softmax's fast path. Separate words, so the warps need no barrier.
-      {
-        const bool any_nz = __any_sync(__activemask(), nonzero);
-        if ((ct & 31) == 0) flg[1 + (ct >> 5)] = any_nz ? 1u : 0u;
-      }
-      if (ct == 0) {
-        bool partial = kt * BN + BN > a.Sk;
-        if (a.kv_valid)
-          for (int t = (kt * BN) >> 6; t < ((kt + 1) * BN) >> 6 && t * 64 < a.Sk; ++t)
-            partial |= __ldg(a.kv_valid + t) < 64;
-        uint32_t f = (ROWMASK || partial) ? 1u : 0u;
-        if (SPARSE) {
-          const uint32_t k0 = mrow0[kt] ? 1u : 0u;
-          const uint32_t k1 = (mrow1 != nullptr && mrow1[kt]) ? 1u : 0u;
-          f |= (k0 << 1) | (k1 << 2);
-        } else {
-          f |= 6u;
-        }
-        *flg = f;
-      }
-      mbar_arrive(bar(L::B_SCF + ss));
-    }
-    if (PAIR && !leader && ok) {
-      // the leader's last K-empty commits arrive here too; take them before exit
-      for (int t = max(0, n_it - L::NKS); t < n_it; ++t)
-        drain_bar(bar(L::B_KCE + t % L::NKS), (t / L::NKS) & 1, a.timeout_ns);
-    }
-  } else {
-    // ------------------------------------------------------------- softmax
-    const int s = warp >> 2;
-    const int r = tid & (kM - 1);
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS0 = tmem + s * BN + lane_off;
-    const uint32_t tO = tmem + L::NSB * BN + s * L::OW + lane_off;
-    const int row = q0 + s * kM + r;
-    const bool row_ok = row < a.Sq;
-    float cq = 0.f;
-    bool ok = true;
-    if constexpr (QRAW) {
-      // This thread quantizes its own row (per 64-row block: each of the
-      // block's two warps also scans the other warp's rows; without the
-      // prologue those rows are not modified, so no barrier is needed).
-      ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_QFULL), 0, ctl, kErrSoftmax));
-      uint8_t* raw = smem + L::OFF_QIN + static_cast<size_t>(s * kM) * D * 2;
-      auto quantized = [&](int rr) {  // row rr of this stage: real and not padding
-        const int gr = q0 + s * kM + rr;
-        return gr < a.Sq && !(a.pad_query && (gr & 63) >= __ldg(a.kv_valid + (gr >> 6)));
-      };
-      if (a.q_pro) {  // RMSNorm + RoPE of the thread's own row, in place
-        if (ok && quantized(r))
-          q_prologue_row<D, VBF16>(raw + r * D * 2, r, static_cast<int64_t>(a.qp_pos0) + q0 + s * kM + r, a);
-        // a 64-row block's two warps read each other's rows below: both warps
-        // always reach this barrier (its condition is uniform over the CTA)
-        if (a.gran_block) named_bar_sync(1 + (warp >> 1), 64);
-      }
-      if (ok) {
-        const bool keep = quantized(r);
-        uint32_t am = keep ? row_amax_bits<D>(raw + r * D * 2, r) : 0u;
-        if (a.gran_block) {
-          const int rp = r ^ 32;
-          if (quantized(rp)) am = max(am, row_amax_bits<D>(raw + rp * D * 2, r));
-          am = __reduce_max_sync(0xffffffffu, am);
-        }
-        const float amax = half_bits_to_float<VBF16>(am);
-        const float scale = __fdiv_rn(amax, 127.0f);
-        const float inv = (keep && amax > 0.f) ? __fdiv_rn(127.0f, amax) : 0.f;
-        write_q_codes<D, VBF16>(raw + r * D * 2, smem + L::OFF_QH + s * L::QH, r, inv);
-        cq = scale * a.cq_mult;
+      if (ct == 0) IA_TRACE_POINT(14, 3);
+      if (ok && !QRAW) {
+        for (int s = 0; s < QS; ++s)
+          widen_tile<D, kM, false>(smem + L::OFF_QIN + s * L::QR, smem + L::OFF_QH + s * L::QH, ct);
         fence_proxy_async_smem();
         mbar_arrive(bar(L::B_QCONV));
+        if (ct == 0) IA_TRACE_POINT(14, 4);
       }
-    } else if (row_ok) {
-      cq = __ldg(a.q_scale + b * a.qs_sb + h * a.qs_sh + (a.gran_block ? (row >> 6) : row)) * a.cq_mult;
-    }
-    const int half = (r >= 64) ? 1 : 0;
-    // O *= alpha over all of this stage's O columns (with ONES, the row sum too)
-    auto rescale_o = [&](float alpha) {
-#pragma unroll 1
-      for (int c0 = 0; c0 + 32 <= L::OW; c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(tO + c0, rr);
-        tmem_wait_ld(rr);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-        tmem_st32(tO + c0, rr);
+      const uint8_t* mrow0 = nullptr;
+      const uint8_t* mrow1 = nullptr;
+      if (SPARSE) {
+        mrow0 = a.mask + (static_cast<int64_t>(b * a.H + h) * a.Tq + qt0) * a.Tk;
+        mrow1 = qt1 < a.Tq ? mrow0 + a.Tk : nullptr;
       }
-      if constexpr (L::OW % 32 != 0) {
-        uint32_t rr[16];
-        tmem_ld16(tO + (L::OW & ~31), rr);
-        tmem_wait_ld(rr);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-        tmem_st16(tO + (L::OW & ~31), rr);
+      const float* ksb = a.k_scale + b * a.ks_sb + h * a.ks_sh;
+      const void* brow = nullptr;  // this (b, h)'s row of per-key offsets
+      if (a.bias != nullptr) {
+        const int es = a.bias_dtype == IA_MASK_F32 ? 4 : a.bias_dtype == IA_MASK_BOOL ? 1 : 2;
+        brow = static_cast<const char*>(a.bias) + (b * a.bias_sb + h * a.bias_sh) * es;
       }
-    };
-    // p = 2^t for two logits, packed to the 16-bit type of V. Without ONES the
-    // fp32 p are also added to the row sum `acc`; with ONES the MMA sums the
-    // 16-bit P it multiplies.
-    auto p_pack = [&](float t0, float t1, uint64_t& acc) -> uint32_t {
-      const float p0 = ex2(t0), p1 = ex2(t1);
-      if constexpr (!L::ONES) acc = fadd2(acc, pack2(p0, p1));
-      return VBF16 ? cvt_bf16x2(p0, p1) : cvt_f16x2(p0, p1);
-    };
-    float m = -INFINITY;  // reference maximum (log2 units) that P is relative to
-    float m_pend = -INFINITY;  // one-pass tiles: the reference the next tile takes
-    float l = 0.f;
-    // One query stage: O is rescaled only once the previous tile's P V has
-    // completed (B_PVT, one phase per tile). That wait cannot alias: when this
-    // tile's S is ready, the P V two tiles back has completed, so B_PVT is at
-    // most one phase behind the phase waited for. The epilogue instead waits
-    // on B_OF, committed once after the last P V: a parity wait on B_PVT there
-    // could find the barrier two phases behind (the last two P Vs in flight)
-    // and pass before O is complete. A wait that runs out (voted across the
-    // warp) clears `ok`, which ends the loop after this tile.
-    for (int it = 0; it < n_it && ok; ++it) {
-      const int ss = it % L::NSC;
-      if (r == 0) IA_TRACE_POINT(4 * s, it);
-      // this tile's S buffer (alternating with one query stage)
-      const int sb = L::DBS ? (it & 1) : s;
-      const uint32_t tS = L::DBS ? tS0 + sb * BN : tS0;
-      bool w = wait_bar(bar(L::B_SF + sb), L::DBS ? (it >> 1) & 1 : it & 1, ctl, kErrSoftmax);
-      w = w && wait_bar(bar(L::B_SCF + ss), (it / L::NSC) & 1, ctl, kErrSoftmax);
-      if (ROWMASK) w = w && wait_bar(bar(L::B_MF + ss), (it / L::NSC) & 1, ctl, kErrSoftmax);
-      ok = __all_sync(0xffffffffu, w);
-      if (!ok) break;
-      tc_fence_after();
-      if (r == 0) IA_TRACE_POINT(1 + 4 * s, it);
-      const float* ksm = reinterpret_cast<const float*>(smem + L::OFF_SC + ss * L::SC);
-      const float* b2m = ksm + BN;
-      const volatile uint32_t* fw = reinterpret_cast<const volatile uint32_t*>(b2m + BN);
-      const uint32_t flags = fw[0];
-      // the masked path is needed for a partial tile, a per-row mask or a
-      // nonzero per-key offset in either converter warp's keys
-      const bool fast = ((flags & 1u) | fw[1] | fw[2]) == 0;
-      const bool keep = SPARSE ? ((flags >> (1 + half)) & 1u) != 0 : true;
-      const uint64_t cq2 = pack2(cq, cq);
-      // KB: each 64-key half of the tile has one k scale; s * k * cq becomes
-      // s * (k * cq), one constant per half and row, so the logits take one
-      // packed FMA and no per-key scale loads.
-      float cb0 = 0.f, cb1 = 0.f;
-      if constexpr (KB) {
-        cb0 = ksm[0] * cq;
-        cb1 = ksm[64] * cq;
-      }
-      if (SPARSE && !keep) {
-        // This row's query tile dropped the key tile: P = 0, the row's maximum
-        // and sum stay as they are, and S need not be read.
-        uint32_t z[BN / 2];
-#pragma unroll
-        for (int e = 0; e < BN / 2; ++e) z[e] = 0u;
-        if constexpr (BN == 128) {
-          tmem_st64(tS, z);
-        } else {
-          tmem_st32(tS, z);
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int kt = SPARSE ? static_cast<int>(list[it0 + it]) : it0 + it;
+        // Per-key constants of this tile: the global loads are issued first and
+        // land while the K tile is widened.
+        constexpr int KPT = (BN + 63) / 64;  // keys per converter thread
+        float kv[KPT];
+        uint32_t braw[KPT];
+        bool kval[KPT];
+  #pragma unroll
+        for (int e = 0; e < KPT; ++e) {
+          const int key = kt * BN + ct + 64 * e;
+          kval[e] = key < a.Sk && (a.kv_valid == nullptr || (key & 63) < __ldg(a.kv_valid + (key >> 6)));
+          kv[e] = kval[e] ? __ldg(ksb + (a.gran_block ? (key >> 6) : key)) : 0.f;
+          braw[e] = (kval[e] && brow != nullptr) ? key_bias_bits(brow, key, a.bias_dtype) : 0u;
         }
-      } else {
-        // The whole S row of this thread in one TMEM round trip.
-        uint32_t sv[BN];
-        if constexpr (BN == 128) {
-          tmem_ld128(tS, sv);
+        // K tile: int8 -> fp16 codes in the swizzled layout the MMA reads
+        const int kst = it % L::NKS;
+        ok = wait_bar(bar(L::B_KRF + kst), (it / L::NKS) & 1, ctl, kErrConverter);
+        if constexpr (PAIR) ok = __all_sync(0xffffffffu, ok);  // warps stay converged
+        if (!ok) break;
+        if (ct == 0) IA_TRACE_POINT(12, it);
+        if constexpr (L::INPLACE) {
+          uint8_t* kh = smem + L::OFF_KH + kst * L::KH;
+          widen_tile<D, BN, true>(kh + BN * 128, kh, ct);
         } else {
-          tmem_ld64(tS, sv);
+          const int rs = it % L::NRS;
+          if (it >= L::NKS) ok = wait_bar(bar(L::B_KCE + kst), ((it / L::NKS) - 1) & 1, ctl, kErrConverter);
+          if constexpr (PAIR) ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          widen_tile<D, L::KROWS, false>(smem + L::OFF_KR + rs * L::KR, smem + L::OFF_KH + kst * L::KH, ct);
+          mbar_arrive(bar(L::B_KRE + rs));
         }
-        tmem_wait_ld(sv);
-        if (r == 0) IA_TRACE_POINT(2 + 4 * s, it);
-        uint64_t lsum[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
-        // One pass (two query stages, a reference already set): P is taken
-        // relative to the reference the previous tiles set (P may exceed 1: up to
-        // 2^64 in bf16, 2^15 in fp16), the tile's maximum is taken in the same
-        // pass, and a reference that grew by more than 2^8 is applied at the
-        // start of the next tile (O and l rescaled there, before this stage's
-        // next P V; that stage's previous P V has completed by then). This
-        // saves the separate pass over the row for its maximum. A row whose
-        // maximum exceeds the reference by more than that bound redoes the tile
-        // in two passes from S, still in TMEM.
-        constexpr bool OP = !L::DBS;
-        // fp16 P holds values below 2^16, bf16 P those below 2^128
-        constexpr float kRedo = VBF16 ? 64.f : 15.f;
-        bool one = false;
-        if constexpr (OP) {
-          if (__any_sync(0xffffffffu, m_pend > m)) {  // the reference grew on the last tile
-            const float alpha = m_pend > m ? ex2(m - m_pend) : 1.f;
-            rescale_o(alpha);
-            l *= alpha;
-            m = fmaxf(m, m_pend);
+        if (ct == 0) IA_TRACE_POINT(13, it);
+        fence_proxy_async_smem();
+        if (PAIR && !leader) {  // the leader's MMA reads this half: one arrival per warp
+          __syncwarp();
+          if ((ct & 31) == 0) mbar_arrive_remote(lbar(L::B_KCF + kst));
+        } else {
+          mbar_arrive(bar(L::B_KCF + kst));
+        }
+        // k scales, bias * log2(e) (-inf past the valid keys) and tile flags
+        const int ss = it % L::NSC;
+        if (it >= L::NSC) ok = wait_bar(bar(L::B_SCE + ss), ((it / L::NSC) - 1) & 1, ctl, kErrConverter);
+        if constexpr (PAIR) ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        float* ksm = reinterpret_cast<float*>(smem + L::OFF_SC + ss * L::SC);
+        float* b2m = ksm + BN;
+        uint32_t* flg = reinterpret_cast<uint32_t*>(b2m + BN);
+        bool nonzero = false;  // a valid key of this thread has a nonzero offset
+  #pragma unroll
+        for (int e = 0; e < KPT; ++e) {
+          if (ct + 64 * e < BN) {
+            const float off =
+                kval[e] ? (brow ? key_bias_value(braw[e], a.bias_dtype) * kLog2e : 0.f) : -INFINITY;
+            ksm[ct + 64 * e] = kv[e];
+            b2m[ct + 64 * e] = off;
+            nonzero |= kval[e] && off != 0.f;
           }
-          one = __all_sync(0xffffffffu, m > -INFINITY);
-          if (one) {
-            const uint64_t cq2o = pack2(cq, cq);
-            const uint64_t nmo = pack2(-m, -m);
-            float mo[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            if (!fast) {  // t = acc k cq + offset (log2 units; -inf for invalid keys)
+        }
+        // Each converter warp records whether its keys carry any offset: a tile
+        // whose offsets are all zero (e.g. the core of a window's bias) keeps the
+        // softmax's fast path. Separate words, so the warps need no barrier.
+        {
+          const bool any_nz = __any_sync(__activemask(), nonzero);
+          if ((ct & 31) == 0) flg[1 + (ct >> 5)] = any_nz ? 1u : 0u;
+        }
+        if (ct == 0) {
+          bool partial = kt * BN + BN > a.Sk;
+          if (a.kv_valid)
+            for (int t = (kt * BN) >> 6; t < ((kt + 1) * BN) >> 6 && t * 64 < a.Sk; ++t)
+              partial |= __ldg(a.kv_valid + t) < 64;
+          uint32_t f = (ROWMASK || partial) ? 1u : 0u;
+          if (SPARSE) {
+            const uint32_t k0 = mrow0[kt] ? 1u : 0u;
+            const uint32_t k1 = (mrow1 != nullptr && mrow1[kt]) ? 1u : 0u;
+            f |= (k0 << 1) | (k1 << 2);
+          } else {
+            f |= 6u;
+          }
+          *flg = f;
+        }
+        mbar_arrive(bar(L::B_SCF + ss));
+      }
+      if (((PAIR && !leader) || SEG) && ok) {
+        // the last K-empty commits (in a pair, the leader's) have no other
+        // waiter: take them before exit or the next segment's initialisation
+        for (int t = max(0, n_it - L::NKS); t < n_it; ++t)
+          drain_bar(bar(L::B_KCE + t % L::NKS), (t / L::NKS) & 1, a.timeout_ns);
+      }
+    } else {
+      // ------------------------------------------------------------- softmax
+      const int s = warp >> 2;
+      const int r = tid & (kM - 1);
+      const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      const uint32_t tS0 = tmem + s * BN + lane_off;
+      const uint32_t tO = tmem + L::NSB * BN + s * L::OW + lane_off;
+      const int row = q0 + s * kM + r;
+      const bool row_ok = row < a.Sq;
+      float cq = 0.f;
+      bool ok = true;
+      if constexpr (QRAW) {
+        // This thread quantizes its own row (per 64-row block: each of the
+        // block's two warps also scans the other warp's rows; without the
+        // prologue those rows are not modified, so no barrier is needed).
+        ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_QFULL), 0, ctl, kErrSoftmax));
+        uint8_t* raw = smem + L::OFF_QIN + static_cast<size_t>(s * kM) * D * 2;
+        auto quantized = [&](int rr) {  // row rr of this stage: real and not padding
+          const int gr = q0 + s * kM + rr;
+          return gr < a.Sq && !(a.pad_query && (gr & 63) >= __ldg(a.kv_valid + (gr >> 6)));
+        };
+        if (a.q_pro) {  // RMSNorm + RoPE of the thread's own row, in place
+          if (ok && quantized(r))
+            q_prologue_row<D, VBF16>(raw + r * D * 2, r, static_cast<int64_t>(a.qp_pos0) + q0 + s * kM + r, a);
+          // a 64-row block's two warps read each other's rows below: both warps
+          // always reach this barrier (its condition is uniform over the CTA)
+          if (a.gran_block) named_bar_sync(1 + (warp >> 1), 64);
+        }
+        if (ok) {
+          const bool keep = quantized(r);
+          uint32_t am = keep ? row_amax_bits<D>(raw + r * D * 2, r) : 0u;
+          if (a.gran_block) {
+            const int rp = r ^ 32;
+            if (quantized(rp)) am = max(am, row_amax_bits<D>(raw + rp * D * 2, r));
+            am = __reduce_max_sync(0xffffffffu, am);
+          }
+          const float amax = half_bits_to_float<VBF16>(am);
+          const float scale = __fdiv_rn(amax, 127.0f);
+          const float inv = (keep && amax > 0.f) ? __fdiv_rn(127.0f, amax) : 0.f;
+          write_q_codes<D, VBF16>(raw + r * D * 2, smem + L::OFF_QH + s * L::QH, r, inv);
+          cq = scale * a.cq_mult;
+          fence_proxy_async_smem();
+          mbar_arrive(bar(L::B_QCONV));
+        }
+      } else if (row_ok) {
+        cq = __ldg(a.q_scale + b * a.qs_sb + h * a.qs_sh + (a.gran_block ? (row >> 6) : row)) * a.cq_mult;
+      }
+      const int half = (r >= 64) ? 1 : 0;
+      // O *= alpha over all of this stage's O columns (with ONES, the row sum too)
+      auto rescale_o = [&](float alpha) {
+  #pragma unroll 1
+        for (int c0 = 0; c0 + 32 <= L::OW; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(tO + c0, rr);
+          tmem_wait_ld(rr);
   #pragma unroll
-              for (int c = 0; c < BN; c += 4) {
-                const float4 b4 = *reinterpret_cast<const float4*>(b2m + c);
-                float t[4];
-                if constexpr (KB) {
+          for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+          tmem_st32(tO + c0, rr);
+        }
+        if constexpr (L::OW % 32 != 0) {
+          uint32_t rr[16];
+          tmem_ld16(tO + (L::OW & ~31), rr);
+          tmem_wait_ld(rr);
+  #pragma unroll
+          for (int e = 0; e < 16; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+          tmem_st16(tO + (L::OW & ~31), rr);
+        }
+      };
+      // p = 2^t for two logits, packed to the 16-bit type of V. Without ONES the
+      // fp32 p are also added to the row sum `acc`; with ONES the MMA sums the
+      // 16-bit P it multiplies.
+      auto p_pack = [&](float t0, float t1, uint64_t& acc) -> uint32_t {
+        const float p0 = ex2(t0), p1 = ex2(t1);
+        if constexpr (!L::ONES) acc = fadd2(acc, pack2(p0, p1));
+        return VBF16 ? cvt_bf16x2(p0, p1) : cvt_f16x2(p0, p1);
+      };
+      float m = -INFINITY;  // reference maximum (log2 units) that P is relative to
+      float m_pend = -INFINITY;  // one-pass tiles: the reference the next tile takes
+      float l = 0.f;
+      // One query stage: O is rescaled only once the previous tile's P V has
+      // completed (B_PVT, one phase per tile). That wait cannot alias: when this
+      // tile's S is ready, the P V two tiles back has completed, so B_PVT is at
+      // most one phase behind the phase waited for. The epilogue instead waits
+      // on B_OF, committed once after the last P V: a parity wait on B_PVT there
+      // could find the barrier two phases behind (the last two P Vs in flight)
+      // and pass before O is complete. A wait that runs out (voted across the
+      // warp) clears `ok`, which ends the loop after this tile.
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int ss = it % L::NSC;
+        if (r == 0) IA_TRACE_POINT(4 * s, it);
+        // this tile's S buffer (alternating with one query stage)
+        const int sb = L::DBS ? (it & 1) : s;
+        const uint32_t tS = L::DBS ? tS0 + sb * BN : tS0;
+        bool w = wait_bar(bar(L::B_SF + sb), L::DBS ? (it >> 1) & 1 : it & 1, ctl, kErrSoftmax);
+        w = w && wait_bar(bar(L::B_SCF + ss), (it / L::NSC) & 1, ctl, kErrSoftmax);
+        if (ROWMASK) w = w && wait_bar(bar(L::B_MF + ss), (it / L::NSC) & 1, ctl, kErrSoftmax);
+        ok = __all_sync(0xffffffffu, w);
+        if (!ok) break;
+        tc_fence_after();
+        if (r == 0) IA_TRACE_POINT(1 + 4 * s, it);
+        const float* ksm = reinterpret_cast<const float*>(smem + L::OFF_SC + ss * L::SC);
+        const float* b2m = ksm + BN;
+        const volatile uint32_t* fw = reinterpret_cast<const volatile uint32_t*>(b2m + BN);
+        const uint32_t flags = fw[0];
+        // the masked path is needed for a partial tile, a per-row mask or a
+        // nonzero per-key offset in either converter warp's keys
+        const bool fast = ((flags & 1u) | fw[1] | fw[2]) == 0;
+        const bool keep = SPARSE ? ((flags >> (1 + half)) & 1u) != 0 : true;
+        const uint64_t cq2 = pack2(cq, cq);
+        // KB: each 64-key half of the tile has one k scale; s * k * cq becomes
+        // s * (k * cq), one constant per half and row, so the logits take one
+        // packed FMA and no per-key scale loads.
+        float cb0 = 0.f, cb1 = 0.f;
+        if constexpr (KB) {
+          cb0 = ksm[0] * cq;
+          cb1 = ksm[64] * cq;
+        }
+        if (SPARSE && !keep) {
+          // This row's query tile dropped the key tile: P = 0, the row's maximum
+          // and sum stay as they are, and S need not be read.
+          uint32_t z[BN / 2];
+  #pragma unroll
+          for (int e = 0; e < BN / 2; ++e) z[e] = 0u;
+          if constexpr (BN == 128) {
+            tmem_st64(tS, z);
+          } else {
+            tmem_st32(tS, z);
+          }
+        } else {
+          // The whole S row of this thread in one TMEM round trip.
+          uint32_t sv[BN];
+          if constexpr (BN == 128) {
+            tmem_ld128(tS, sv);
+          } else {
+            tmem_ld64(tS, sv);
+          }
+          tmem_wait_ld(sv);
+          if (r == 0) IA_TRACE_POINT(2 + 4 * s, it);
+          uint64_t lsum[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
+          // One pass (two query stages, a reference already set): P is taken
+          // relative to the reference the previous tiles set (P may exceed 1: up to
+          // 2^64 in bf16, 2^15 in fp16), the tile's maximum is taken in the same
+          // pass, and a reference that grew by more than 2^8 is applied at the
+          // start of the next tile (O and l rescaled there, before this stage's
+          // next P V; that stage's previous P V has completed by then). This
+          // saves the separate pass over the row for its maximum. A row whose
+          // maximum exceeds the reference by more than that bound redoes the tile
+          // in two passes from S, still in TMEM.
+          constexpr bool OP = !L::DBS;
+          // fp16 P holds values below 2^16, bf16 P those below 2^128
+          constexpr float kRedo = VBF16 ? 64.f : 15.f;
+          bool one = false;
+          if constexpr (OP) {
+            if (__any_sync(0xffffffffu, m_pend > m)) {  // the reference grew on the last tile
+              const float alpha = m_pend > m ? ex2(m - m_pend) : 1.f;
+              rescale_o(alpha);
+              l *= alpha;
+              m = fmaxf(m, m_pend);
+            }
+            one = __all_sync(0xffffffffu, m > -INFINITY);
+            if (one) {
+              const uint64_t cq2o = pack2(cq, cq);
+              const uint64_t nmo = pack2(-m, -m);
+              float mo[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+              if (!fast) {  // t = acc k cq + offset (log2 units; -inf for invalid keys)
+    #pragma unroll
+                for (int c = 0; c < BN; c += 4) {
+                  const float4 b4 = *reinterpret_cast<const float4*>(b2m + c);
+                  float t[4];
+                  if constexpr (KB) {
+                    const uint64_t c2 = c < 64 ? pack2(cb0, cb0) : pack2(cb1, cb1);
+                    unpack2(ffma2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), c2,
+                                  pack2(b4.x, b4.y)), t[0], t[1]);
+                    unpack2(ffma2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), c2,
+                                  pack2(b4.z, b4.w)), t[2], t[3]);
+                  } else {
+                    const float4 k4 = *reinterpret_cast<const float4*>(ksm + c);
+                    unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(k4.x, k4.y)),
+                                  cq2o, pack2(b4.x, b4.y)), t[0], t[1]);
+                    unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(k4.z, k4.w)),
+                                  cq2o, pack2(b4.z, b4.w)), t[2], t[3]);
+                  }
+                  const int q = (c >> 2) & 3;
+                  mo[q] = fmax3(mo[q], fmaxf(t[0], t[1]), fmaxf(t[2], t[3]));
+    #pragma unroll
+                  for (int h2 = 0; h2 < 2; ++h2) {
+                    float t0, t1;
+                    unpack2(fadd2(pack2(t[2 * h2], t[2 * h2 + 1]), nmo), t0, t1);
+                    sv[(c >> 1) + h2] = p_pack(t0, t1, lsum[h2]);
+                  }
+                }
+              } else if constexpr (KB) {
+                // raw maxima per 64-key half (mo[0..1] and mo[2..3]), scaled below
+    #pragma unroll
+                for (int c = 0; c < BN; c += 8) {
                   const uint64_t c2 = c < 64 ? pack2(cb0, cb0) : pack2(cb1, cb1);
-                  unpack2(ffma2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), c2,
-                                pack2(b4.x, b4.y)), t[0], t[1]);
-                  unpack2(ffma2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), c2,
-                                pack2(b4.z, b4.w)), t[2], t[3]);
-                } else {
-                  const float4 k4 = *reinterpret_cast<const float4*>(ksm + c);
-                  unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(k4.x, k4.y)),
-                                cq2o, pack2(b4.x, b4.y)), t[0], t[1]);
-                  unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(k4.z, k4.w)),
-                                cq2o, pack2(b4.z, b4.w)), t[2], t[3]);
+    #pragma unroll
+                  for (int q = 0; q < 4; ++q) {
+                    const float s0 = __uint_as_float(sv[c + 2 * q]), s1 = __uint_as_float(sv[c + 2 * q + 1]);
+                    const int i = (c < 64 ? 0 : 2) + (q & 1);
+                    mo[i] = fmax3(mo[i], s0, s1);
+                    float t0, t1;
+                    unpack2(ffma2(pack2(s0, s1), c2, nmo), t0, t1);
+                    sv[(c >> 1) + q] = p_pack(t0, t1, lsum[q & 1]);
+                  }
                 }
-                const int q = (c >> 2) & 3;
-                mo[q] = fmax3(mo[q], fmaxf(t[0], t[1]), fmaxf(t[2], t[3]));
-  #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                  float t0, t1;
-                  unpack2(fadd2(pack2(t[2 * h2], t[2 * h2 + 1]), nmo), t0, t1);
-                  sv[(c >> 1) + h2] = p_pack(t0, t1, lsum[h2]);
-                }
-              }
-            } else if constexpr (KB) {
-              // raw maxima per 64-key half (mo[0..1] and mo[2..3]), scaled below
-  #pragma unroll
+              } else {
+    #pragma unroll
               for (int c = 0; c < BN; c += 8) {
-                const uint64_t c2 = c < 64 ? pack2(cb0, cb0) : pack2(cb1, cb1);
-  #pragma unroll
+                const float4 ka = *reinterpret_cast<const float4*>(ksm + c);
+                const float4 kb = *reinterpret_cast<const float4*>(ksm + c + 4);
+                float u[8];
+                unpack2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(ka.x, ka.y)), u[0], u[1]);
+                unpack2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(ka.z, ka.w)), u[2], u[3]);
+                unpack2(fmul2(pack2(__uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5])), pack2(kb.x, kb.y)), u[4], u[5]);
+                unpack2(fmul2(pack2(__uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7])), pack2(kb.z, kb.w)), u[6], u[7]);
+    #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                  const float s0 = __uint_as_float(sv[c + 2 * q]), s1 = __uint_as_float(sv[c + 2 * q + 1]);
-                  const int i = (c < 64 ? 0 : 2) + (q & 1);
-                  mo[i] = fmax3(mo[i], s0, s1);
+                  mo[q] = fmax3(mo[q], u[2 * q], u[2 * q + 1]);
                   float t0, t1;
-                  unpack2(ffma2(pack2(s0, s1), c2, nmo), t0, t1);
+                  unpack2(ffma2(pack2(u[2 * q], u[2 * q + 1]), cq2o, nmo), t0, t1);
                   sv[(c >> 1) + q] = p_pack(t0, t1, lsum[q & 1]);
                 }
               }
-            } else {
-  #pragma unroll
+              }
+              const float rmo = fmaxf(fmaxf(mo[0], mo[1]), fmaxf(mo[2], mo[3]));
+              float tmx = fast ? cq * rmo : rmo;
+              if (KB && fast) tmx = fmaxf(fmaxf(mo[0], mo[1]) * cb0, fmaxf(mo[2], mo[3]) * cb1);
+              if (__any_sync(0xffffffffu, tmx > m + kRedo)) {
+                one = false;  // redo exactly: S is still in TMEM
+                if constexpr (BN == 128) tmem_ld128(tS, sv);
+                else tmem_ld64(tS, sv);
+                tmem_wait_ld(sv);
+                lsum[0] = lsum[1] = pack2(0.f, 0.f);
+              } else {
+                m_pend = tmx > m + kRescaleLog2 ? tmx : m;
+              }
+            }
+          }
+          if (!one) {  // ---- two passes: the row maximum, then P
+          // u = acc * k_scale (fast tiles) or t = u * cq + bias*log2e / -inf
+          // (masked tiles), in place, and the row maximum.
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          if (KB && fast) {  // raw S stays; maxima per 64-key half
+    #pragma unroll
+            for (int c = 0; c < BN; c += 8)
+    #pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int i = (c < 64 ? 0 : 2) + (q & 1);
+                mx[i] = fmax3(mx[i], __uint_as_float(sv[c + 2 * q]), __uint_as_float(sv[c + 2 * q + 1]));
+              }
+          } else if (fast) {
+    #pragma unroll
             for (int c = 0; c < BN; c += 8) {
               const float4 ka = *reinterpret_cast<const float4*>(ksm + c);
               const float4 kb = *reinterpret_cast<const float4*>(ksm + c + 4);
-              float u[8];
-              unpack2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(ka.x, ka.y)), u[0], u[1]);
-              unpack2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(ka.z, ka.w)), u[2], u[3]);
-              unpack2(fmul2(pack2(__uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5])), pack2(kb.x, kb.y)), u[4], u[5]);
-              unpack2(fmul2(pack2(__uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7])), pack2(kb.z, kb.w)), u[6], u[7]);
-  #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                mo[q] = fmax3(mo[q], u[2 * q], u[2 * q + 1]);
-                float t0, t1;
-                unpack2(ffma2(pack2(u[2 * q], u[2 * q + 1]), cq2o, nmo), t0, t1);
-                sv[(c >> 1) + q] = p_pack(t0, t1, lsum[q & 1]);
+              float f[8];
+              unpack2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(ka.x, ka.y)), f[0], f[1]);
+              unpack2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(ka.z, ka.w)), f[2], f[3]);
+              unpack2(fmul2(pack2(__uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5])), pack2(kb.x, kb.y)), f[4], f[5]);
+              unpack2(fmul2(pack2(__uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7])), pack2(kb.z, kb.w)), f[6], f[7]);
+    #pragma unroll
+              for (int q = 0; q < 4; ++q) mx[q] = fmax3(mx[q], f[2 * q], f[2 * q + 1]);
+    #pragma unroll
+              for (int q = 0; q < 8; ++q) sv[c + q] = __float_as_uint(f[q]);
+            }
+          } else {
+    #pragma unroll
+            for (int c = 0; c < BN; c += 4) {
+              const float4 b4 = *reinterpret_cast<const float4*>(b2m + c);
+              float f[4];
+              if constexpr (KB) {
+                const uint64_t c2 = c < 64 ? pack2(cb0, cb0) : pack2(cb1, cb1);
+                unpack2(ffma2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), c2,
+                              pack2(b4.x, b4.y)), f[0], f[1]);
+                unpack2(ffma2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), c2,
+                              pack2(b4.z, b4.w)), f[2], f[3]);
+              } else {
+                const float4 k4 = *reinterpret_cast<const float4*>(ksm + c);
+                unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(k4.x, k4.y)),
+                              cq2, pack2(b4.x, b4.y)), f[0], f[1]);
+                unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(k4.z, k4.w)),
+                              cq2, pack2(b4.z, b4.w)), f[2], f[3]);
               }
-            }
-            }
-            const float rmo = fmaxf(fmaxf(mo[0], mo[1]), fmaxf(mo[2], mo[3]));
-            float tmx = fast ? cq * rmo : rmo;
-            if (KB && fast) tmx = fmaxf(fmaxf(mo[0], mo[1]) * cb0, fmaxf(mo[2], mo[3]) * cb1);
-            if (__any_sync(0xffffffffu, tmx > m + kRedo)) {
-              one = false;  // redo exactly: S is still in TMEM
-              if constexpr (BN == 128) tmem_ld128(tS, sv);
-              else tmem_ld64(tS, sv);
-              tmem_wait_ld(sv);
-              lsum[0] = lsum[1] = pack2(0.f, 0.f);
-            } else {
-              m_pend = tmx > m + kRescaleLog2 ? tmx : m;
+              if constexpr (ROWMASK) {
+                float mk[4];
+                row_mask4(smem + L::OFF_MK + ss * L::MB, r, c, a.rm_dtype, mk);
+    #pragma unroll
+                for (int e = 0; e < 4; ++e) f[e] = fmaf(mk[e], kLog2e, f[e]);
+              }
+              const int q = (c >> 2) & 3;
+              mx[q] = fmax3(mx[q], fmaxf(f[0], f[1]), fmaxf(f[2], f[3]));
+    #pragma unroll
+              for (int e = 0; e < 4; ++e) sv[c + e] = __float_as_uint(f[e]);
             }
           }
+          const float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+          float tmax = fast ? cq * rmax : rmax;
+          if (KB && fast) tmax = fmaxf(fmaxf(mx[0], mx[1]) * cb0, fmaxf(mx[2], mx[3]) * cb1);
+          const float m_new = fmaxf(m, tmax);
+          const bool need = m_new > m + kRescaleLog2;
+          if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? ex2(m - m_new) : 1.f;
+            if (L::DBS && it > 0) {  // the previous tile's P V may still be adding into O
+              ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_PVT), (it - 1) & 1, ctl, kErrSoftmax));
+              if (!ok) break;
+              tc_fence_after();
+            }
+            if (it > 0) rescale_o(alpha);
+            l *= alpha;
+            if (need) m = m_new;
+          }
+          const float mref = (m == -INFINITY) ? 0.f : m;
+          const float k1 = fast ? cq : 1.f;
+          const uint64_t k1v = pack2(k1, k1);
+          const uint64_t nm = pack2(-mref, -mref);
+          // p = 2^(t - m) with the row sum in fp32; P packed to 16 bits in place
+          // (pair i lands in word i, whose value is already consumed) and written
+          // to the first BN/2 columns of S in one store.
+    #pragma unroll
+          for (int e = 0; e < BN / 2; ++e) {
+            uint64_t kv2 = k1v;
+            if (KB && fast) kv2 = 2 * e < 64 ? pack2(cb0, cb0) : pack2(cb1, cb1);
+            float t0, t1;
+            unpack2(ffma2(pack2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), kv2, nm), t0, t1);
+            sv[e] = p_pack(t0, t1, lsum[e & 1]);
+          }
+          if (OP) m_pend = m;
+          }  // ---- two passes
+          if constexpr (BN == 128) {
+            tmem_st64(tS, *reinterpret_cast<uint32_t(*)[64]>(sv));
+          } else {
+            tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(sv));
+          }
+          float la, lb, lc, ld;
+          unpack2(lsum[0], la, lb);
+          unpack2(lsum[1], lc, ld);
+          l += (la + lb) + (lc + ld);
         }
-        if (!one) {  // ---- two passes: the row maximum, then P
-        // u = acc * k_scale (fast tiles) or t = u * cq + bias*log2e / -inf
-        // (masked tiles), in place, and the row maximum.
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (KB && fast) {  // raw S stays; maxima per 64-key half
-  #pragma unroll
-          for (int c = 0; c < BN; c += 8)
-  #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int i = (c < 64 ? 0 : 2) + (q & 1);
-              mx[i] = fmax3(mx[i], __uint_as_float(sv[c + 2 * q]), __uint_as_float(sv[c + 2 * q + 1]));
-            }
-        } else if (fast) {
-  #pragma unroll
-          for (int c = 0; c < BN; c += 8) {
-            const float4 ka = *reinterpret_cast<const float4*>(ksm + c);
-            const float4 kb = *reinterpret_cast<const float4*>(ksm + c + 4);
-            float f[8];
-            unpack2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(ka.x, ka.y)), f[0], f[1]);
-            unpack2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(ka.z, ka.w)), f[2], f[3]);
-            unpack2(fmul2(pack2(__uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5])), pack2(kb.x, kb.y)), f[4], f[5]);
-            unpack2(fmul2(pack2(__uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7])), pack2(kb.z, kb.w)), f[6], f[7]);
-  #pragma unroll
-            for (int q = 0; q < 4; ++q) mx[q] = fmax3(mx[q], f[2 * q], f[2 * q + 1]);
-  #pragma unroll
-            for (int q = 0; q < 8; ++q) sv[c + q] = __float_as_uint(f[q]);
-          }
+        tmem_wait_st();
+        tc_fence_before();
+        if (PAIR && !leader) {
+          // The leader's MMA reads this P from this CTA's TMEM: one arrival per
+          // warp, ordered by the tcgen05 wait and fence above.
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(lbar(L::B_PF + sb));
         } else {
-  #pragma unroll
-          for (int c = 0; c < BN; c += 4) {
-            const float4 b4 = *reinterpret_cast<const float4*>(b2m + c);
-            float f[4];
-            if constexpr (KB) {
-              const uint64_t c2 = c < 64 ? pack2(cb0, cb0) : pack2(cb1, cb1);
-              unpack2(ffma2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), c2,
-                            pack2(b4.x, b4.y)), f[0], f[1]);
-              unpack2(ffma2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), c2,
-                            pack2(b4.z, b4.w)), f[2], f[3]);
-            } else {
-              const float4 k4 = *reinterpret_cast<const float4*>(ksm + c);
-              unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), pack2(k4.x, k4.y)),
-                            cq2, pack2(b4.x, b4.y)), f[0], f[1]);
-              unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(k4.z, k4.w)),
-                            cq2, pack2(b4.z, b4.w)), f[2], f[3]);
-            }
-            if constexpr (ROWMASK) {
-              float mk[4];
-              row_mask4(smem + L::OFF_MK + ss * L::MB, r, c, a.rm_dtype, mk);
-  #pragma unroll
-              for (int e = 0; e < 4; ++e) f[e] = fmaf(mk[e], kLog2e, f[e]);
-            }
-            const int q = (c >> 2) & 3;
-            mx[q] = fmax3(mx[q], fmaxf(f[0], f[1]), fmaxf(f[2], f[3]));
-  #pragma unroll
-            for (int e = 0; e < 4; ++e) sv[c + e] = __float_as_uint(f[e]);
-          }
+          mbar_arrive(bar(L::B_PF + sb));
         }
-        const float rmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        float tmax = fast ? cq * rmax : rmax;
-        if (KB && fast) tmax = fmaxf(fmaxf(mx[0], mx[1]) * cb0, fmaxf(mx[2], mx[3]) * cb1);
-        const float m_new = fmaxf(m, tmax);
-        const bool need = m_new > m + kRescaleLog2;
-        if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? ex2(m - m_new) : 1.f;
-          if (L::DBS && it > 0) {  // the previous tile's P V may still be adding into O
-            ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_PVT), (it - 1) & 1, ctl, kErrSoftmax));
-            if (!ok) break;
-            tc_fence_after();
-          }
-          if (it > 0) rescale_o(alpha);
-          l *= alpha;
-          if (need) m = m_new;
-        }
-        const float mref = (m == -INFINITY) ? 0.f : m;
-        const float k1 = fast ? cq : 1.f;
-        const uint64_t k1v = pack2(k1, k1);
-        const uint64_t nm = pack2(-mref, -mref);
-        // p = 2^(t - m) with the row sum in fp32; P packed to 16 bits in place
-        // (pair i lands in word i, whose value is already consumed) and written
-        // to the first BN/2 columns of S in one store.
-  #pragma unroll
-        for (int e = 0; e < BN / 2; ++e) {
-          uint64_t kv2 = k1v;
-          if (KB && fast) kv2 = 2 * e < 64 ? pack2(cb0, cb0) : pack2(cb1, cb1);
-          float t0, t1;
-          unpack2(ffma2(pack2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), kv2, nm), t0, t1);
-          sv[e] = p_pack(t0, t1, lsum[e & 1]);
-        }
-        if (OP) m_pend = m;
-        }  // ---- two passes
-        if constexpr (BN == 128) {
-          tmem_st64(tS, *reinterpret_cast<uint32_t(*)[64]>(sv));
-        } else {
-          tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(sv));
-        }
-        float la, lb, lc, ld;
-        unpack2(lsum[0], la, lb);
-        unpack2(lsum[1], lc, ld);
-        l += (la + lb) + (lc + ld);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      if (PAIR && !leader) {
-        // The leader's MMA reads this P from this CTA's TMEM: one arrival per
-        // warp, ordered by the tcgen05 wait and fence above.
+        if (r == 0) IA_TRACE_POINT(3 + 4 * s, it);
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(lbar(L::B_PF + sb));
-      } else {
-        mbar_arrive(bar(L::B_PF + sb));
+        if (lane == 0) mbar_arrive(bar(L::B_SCE + ss));
       }
-      if (r == 0) IA_TRACE_POINT(3 + 4 * s, it);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::B_SCE + ss));
-    }
-    // ------------------------------------------------------------ epilogue
-    if (ok && n_it > 0)
-      ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_OF + s), 0, ctl, kErrSoftmax));
-    if (ok) {
-      tc_fence_after();
-      if (r == 0 && s == 0) IA_TRACE_POINT(14, 8);
-      if constexpr (L::ONES) {  // the row sum the MMA accumulated in column D
-        if (n_it > 0) {
-          uint32_t lr[16];
-          tmem_ld16(tO + D, lr);
-          tmem_wait_ld(lr);
-          l = __uint_as_float(lr[0]);
-        }
-      }
-      bool pad = false;
-      if (a.pad_query && row_ok) pad = (row & 63) >= __ldg(a.kv_valid + (row >> 6));
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      char* orow = static_cast<char*>(a.out) +
-                   (b * a.o_sb + h * a.o_sh + static_cast<int64_t>(row) * a.o_ss) * 2;
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t rr[32];
-        if (n_it > 0) {
-          tmem_ld32(tO + c0, rr);
-          tmem_wait_ld(rr);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) rr[i] = 0u;
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float o0 = __uint_as_float(rr[2 * i]) * inv_l * vsc[c0 + 2 * i];
-          float o1 = __uint_as_float(rr[2 * i + 1]) * inv_l * vsc[c0 + 2 * i + 1];
-          if (pad) o0 = o1 = 0.f;
-          pk[i] = VBF16 ? cvt_bf16x2(o0, o1) : cvt_f16x2(o0, o1);
-        }
-        if (row_ok && a.ws_o != nullptr) {  // fp32 partial of this key range
-          float4* dst = reinterpret_cast<float4*>(
-              a.ws_o + ((static_cast<int64_t>(split * a.B + b) * a.H + h) * a.Sq + row) * D + c0);
-#pragma unroll
-          for (int v4 = 0; v4 < 8; ++v4) {
-            float f[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              f[e] = pad ? 0.f : __uint_as_float(rr[4 * v4 + e]) * inv_l * vsc[c0 + 4 * v4 + e];
-            dst[v4] = make_float4(f[0], f[1], f[2], f[3]);
+      // ------------------------------------------------------------ epilogue
+      if (ok && n_it > 0)
+        ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_OF + s), 0, ctl, kErrSoftmax));
+      if (ok) {
+        tc_fence_after();
+        if (r == 0 && s == 0) IA_TRACE_POINT(14, 8);
+        if constexpr (L::ONES) {  // the row sum the MMA accumulated in column D
+          if (n_it > 0) {
+            uint32_t lr[16];
+            tmem_ld16(tO + D, lr);
+            tmem_wait_ld(lr);
+            l = __uint_as_float(lr[0]);
           }
-        } else if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c0 * 2);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+        bool pad = false;
+        if (a.pad_query && row_ok) pad = (row & 63) >= __ldg(a.kv_valid + (row >> 6));
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        char* orow = static_cast<char*>(a.out) +
+                     (b * a.o_sb + h * a.o_sh + static_cast<int64_t>(row) * a.o_ss) * 2;
+  #pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t rr[32];
+          if (n_it > 0) {
+            tmem_ld32(tO + c0, rr);
+            tmem_wait_ld(rr);
+          } else {
+  #pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = 0u;
+          }
+          uint32_t pk[16];
+  #pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float o0 = __uint_as_float(rr[2 * i]) * inv_l * vsc[c0 + 2 * i];
+            float o1 = __uint_as_float(rr[2 * i + 1]) * inv_l * vsc[c0 + 2 * i + 1];
+            if (pad) o0 = o1 = 0.f;
+            pk[i] = VBF16 ? cvt_bf16x2(o0, o1) : cvt_f16x2(o0, o1);
+          }
+          if (row_ok && a.ws_o != nullptr) {  // fp32 partial of this key range
+            float4* dst = reinterpret_cast<float4*>(
+                a.ws_o + ((static_cast<int64_t>(split * a.B + b) * a.H + h) * a.Sq + row) * D + c0);
+  #pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4) {
+              float f[4];
+  #pragma unroll
+              for (int e = 0; e < 4; ++e)
+                f[e] = pad ? 0.f : __uint_as_float(rr[4 * v4 + e]) * inv_l * vsc[c0 + 4 * v4 + e];
+              dst[v4] = make_float4(f[0], f[1], f[2], f[3]);
+            }
+          } else if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c0 * 2);
+  #pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
+        }
+        if (row_ok && (a.lse != nullptr || a.ws_l != nullptr)) {
+          const float lse = (pad || !(l > 0.f)) ? -INFINITY : (m + log2f(l)) * kLn2;
+          if (a.ws_l != nullptr) {
+            a.ws_l[(static_cast<int64_t>(split * a.B + b) * a.H + h) * a.Sq + row] = lse;
+            if (seg_full)  // the query tile's second partial is empty (its O is not read)
+              a.ws_l[(static_cast<int64_t>(a.B + b) * a.H + h) * a.Sq + row] = -INFINITY;
+          } else {
+            a.lse[b * a.l_sb + h * a.l_sh + row] = lse;
+          }
         }
       }
-      if (row_ok && (a.lse != nullptr || a.ws_l != nullptr)) {
-        const float lse = (pad || !(l > 0.f)) ? -INFINITY : (m + log2f(l)) * kLn2;
-        if (a.ws_l != nullptr)
-          a.ws_l[(static_cast<int64_t>(split * a.B + b) * a.H + h) * a.Sq + row] = lse;
-        else
-          a.lse[b * a.l_sb + h * a.l_sh + row] = lse;
-      }
     }
-  }
+
+  }  // segments
 
   // ------------------------------------------------------------- teardown
   if (warp == 0 && lane == 0) IA_TRACE_POINT(14, 9);
@@ -1417,6 +1480,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
   if constexpr (PAIR) cluster_sync();
   if (warp == L::W_MMA) {
     tc_fence_after();
+    const uint32_t tmem = misc[0];
     if constexpr (PAIR) tmem_dealloc_pair(tmem, L::TMEM_COLS);
     else tmem_dealloc(tmem, L::TMEM_COLS);
   }
@@ -1552,7 +1616,23 @@ ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** ms
     a.ws_l = a.ws_o + static_cast<int64_t>(nsplit) * rows * D;
   }
   const size_t smem = L::SMEM_FIXED + (SPARSE ? static_cast<size_t>(a.Tk) * 2 : 0);
+  // Two key ranges on the dense head-dim-64 kernel with at least one query tile
+  // per SM: one CTA per SM, each taking an equal share of the (query tile, key
+  // tile) units, instead of a grid whose last round runs part-empty.
+  int gx = (p.Sq + kM * QS - 1) / (kM * QS);
+  if (PAIR) gx = (gx + 1) & ~1;  // whole pairs; a surplus CTA's rows are all past Sq
+  dim3 grid(gx, p.H, p.B * nsplit);
+  a.seg_units = 0;
+  a.seg_nqt = gx;
   auto kern = attn_fwd_kernel<D, QS, BN, SPARSE, VBF16, QRAW, ROWMASK, PAIR, KB>;
+  if constexpr (L::SEGOK && !QRAW) {
+    const int64_t n_qt = static_cast<int64_t>(p.B) * p.H * gx;
+    if (nsplit == 2 && n_qt >= num_sms && n_qt * a.n_tiles < (int64_t{1} << 40)) {
+      a.seg_units = n_qt * a.n_tiles;
+      grid = dim3(num_sms, 1, 1);
+      kern = attn_fwd_kernel<D, QS, BN, SPARSE, VBF16, QRAW, ROWMASK, PAIR, KB, true>;
+    }
+  }
   if (smem > 232448) {
     *msg = "key-tile list does not fit in shared memory (too many key tiles)";
     return IA_ERR_UNSUPPORTED;
@@ -1563,9 +1643,7 @@ ia_status run(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** ms
     *msg = cudaGetErrorString(e);
     return IA_ERR_CUDA;
   }
-  int gx = (p.Sq + kM * QS - 1) / (kM * QS);
-  if (PAIR) gx = (gx + 1) & ~1;  // whole pairs; a surplus CTA's rows are all past Sq
-  dim3 grid(gx, p.H, p.B * nsplit);
+
   if constexpr (PAIR) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;

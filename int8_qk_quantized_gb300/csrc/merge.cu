@@ -141,7 +141,8 @@ __global__ void __launch_bounds__(kThreads) merge_n_kernel(const MergeNArgs a) {
     if (m != -INFINITY) {
       float den = 0.f;
       for (int k = 0; k < a.n; ++k) {
-        const float w = expf(a.l[k][r] - m);  // 0 for an empty partial
+        const float w = expf(a.l[k][r] - m);
+        if (!(w > 0.f)) continue;  // an empty partial: its O is not read
         den += w;
         float x[8];
         if (IN_F32) {

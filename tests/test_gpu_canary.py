@@ -130,6 +130,8 @@ ATTN_CASES = [
     ("banded", dict(H=2, Sq=300, Sk=2500, skirt_width=500), dict(bias=True)),
     ("anima4k", dict(H=2, Sq=200, Sk=3000, v_scale=False), dict(kv_splits=3)),
     ("sdxl", dict(H=2, Sq=100, Sk=2048), dict(kv_splits=4)),
+    # two key ranges over >= one 256-row query tile per SM: balanced segments
+    ("sdxl", dict(H=60, Sq=700, Sk=1000), dict(kv_splits=2, segments=True)),
     ("sparse", dict(H=2, Sq=1024, Sk=1024, band_tiles=4, random_tiles=2), {}),
     ("sparse", dict(H=1, Sq=1024, Sk=1024, band_tiles=4, random_tiles=2, D=64,
                     granularity="block64"), dict(kv_splits=2)),
@@ -180,7 +182,14 @@ def test_attention_outputs_and_workspace_stay_in_bounds(name, kw, extra):
         ia.device_status()
         go.check("fused-Q out")
         gl.check("fused-Q lse")
-        assert torch.equal(o2, ro) and torch.equal(l2, rl)
+        if extra.get("segments"):
+            # the int8-Q call split the keys in balanced segments, the fused-Q
+            # call (no segments) in two equal ranges: equal up to the merge's
+            # rounding
+            assert (o2.float() - ro.float()).abs().max().item() < 2e-3
+            assert (l2 - rl).abs().max().item() < 1e-4
+        else:
+            assert torch.equal(o2, ro) and torch.equal(l2, rl)
 
 
 def test_key_subrange_views_and_bshd_outputs_stay_in_bounds():

@@ -92,3 +92,37 @@ def test_merge_n_of_key_ranges_equals_oracle():
     ro, rl = oracle_full(inp, wl)
     assert_out_close(to_np(mo), ro)
     assert_lse_close(to_np(ml), rl)
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("name,gran,Sq,Sk", [
+    ("sdxl", "block64", 1000, 1000),   # per-block K scales (fp16), ragged keys
+    ("sdxl", "token", 1100, 777),      # per-token scales, ragged rows and keys
+    ("tiny", "token", 600, 3000),      # bf16, many key tiles per CTA
+])
+def test_two_way_split_in_balanced_segments(name, gran, Sq, Sk):
+    """Two key ranges on the dense head-dim-64 kernel with at least one 256-row
+    query tile per SM: one CTA per SM takes an equal share of the (query tile,
+    key tile) units, so a query tile's two ranges meet wherever a CTA's share
+    ends (or one CTA covers all its keys). The result meets the same bar as
+    one pass over all keys."""
+    import int8_qk_quantized_gb300 as ia
+    nqt = (Sq + 255) // 256
+    H = -(-_sms() // nqt) + 1  # enough query tiles for the balanced schedule
+    wl = WORKLOADS[name].with_(H=H, Sq=Sq, Sk=Sk, granularity=gran)
+    inp = make_inputs(wl, "cuda")
+    q8, qs, k8, ks = ia.quantize_qk(inp.q, inp.k, granularity=gran, kv_valid=inp.kv_valid)
+    args = dict(v_scale=inp.v_scale, granularity=gran, return_lse=True)
+    o1, l1 = ia.attention(q8, k8, qs, ks, inp.v, kv_splits=1, **args)
+    o2, l2 = ia.attention(q8, k8, qs, ks, inp.v, kv_splits=2, **args)
+    o3, l3 = ia.attention(q8, k8, qs, ks, inp.v, kv_splits=2, **args)
+    ia.device_status()
+    assert torch.equal(o2, o3) and torch.equal(l2, l3)  # a fixed schedule: run to run equal
+    d = (o2.float() - o1.float()).abs()
+    assert d.max().item() < 2e-2 and d.mean().item() < 1e-3
+    ro, rl = oracle_full(inp, wl)
+    assert_out_close(to_np(o2), ro)
+    assert_lse_close(to_np(l2), rl)

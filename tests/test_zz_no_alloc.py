@@ -6,6 +6,8 @@ array inside the library. Each check makes two calls in a row, so the second
 one finds the first one's partials in the shared scratch; both must match the
 allocating entry point within the parity tolerance.
 """
+import gc
+
 import pytest
 import torch
 
@@ -98,10 +100,13 @@ def test_allocates_no_device_memory():
     lse = torch.empty((1, 3, 700), dtype=torch.float32, device="cuda")
     ia.attention_static_workspace(q8, k8, qs, ks, v, out, lse=lse, kv_splits=4, **args)
     torch.cuda.synchronize()
+    gc.collect()  # tensors of earlier tests are not freed during the measurement
     free0, held0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
     for splits in (4, 2, 4):
         ia.attention_static_workspace(q8, k8, qs, ks, v, out, lse=lse, kv_splits=splits, **args)
     torch.cuda.synchronize()
     assert torch.cuda.mem_get_info()[0] == free0
-    assert torch.cuda.memory_allocated() == held0
+    # torch's allocator gave the calls nothing (a collection may still free
+    # unrelated tensors, never add any)
+    assert torch.cuda.memory_allocated() <= held0
     ia.device_status()
