@@ -126,3 +126,47 @@ def test_two_way_split_in_balanced_segments(name, gran, Sq, Sk):
     ro, rl = oracle_full(inp, wl)
     assert_out_close(to_np(o2), ro)
     assert_lse_close(to_np(l2), rl)
+
+
+def test_balanced_segments_with_validity_vector_and_batches():
+    """Balanced segments (head dim 64, two key ranges, >= one query tile per SM)
+    with B = 2, a per-tile validity vector (padded keys and padded query rows)
+    and ragged sequence lengths, against the oracle."""
+    import int8_qk_quantized_gb300 as ia
+    Sq = Sk = 1088  # 17 tiles of 64, the last one 37 rows valid
+    H = -(-_sms() // (2 * 5)) + 1  # B * H * 5 query tiles >= SMs
+    wl = WORKLOADS["sparse"].with_(B=2, H=H, Sq=Sq, Sk=Sk, D=64, granularity="token")
+    inp = make_inputs(wl, "cuda")
+    assert inp.kv_valid is not None
+    q8, qs, k8, ks = ia.quantize_qk(inp.q, inp.k, kv_valid=inp.kv_valid)
+    args = dict(kv_valid=inp.kv_valid, return_lse=True)
+    o1, l1 = ia.attention(q8, k8, qs, ks, inp.v, kv_splits=1, **args)
+    o2, l2 = ia.attention(q8, k8, qs, ks, inp.v, kv_splits=2, **args)
+    ia.device_status()
+    valid = oracle.row_validity(wl.Sq, inp.kv_valid.cpu().numpy())
+    d = (o2.float() - o1.float()).abs()[:, :, torch.from_numpy(valid).cuda()]
+    assert d.max().item() < 2e-2 and d.mean().item() < 1e-3
+    vbs = inp.kv_valid.cpu().numpy()
+    ro, rl, _ = oracle.quantize_and_attend(to_np(inp.q), to_np(inp.k), to_np(inp.v),
+                                           granularity="token", kv_valid=vbs)
+    assert_out_close(to_np(o2), ro, valid=valid)
+    assert_lse_close(to_np(l2)[:, :, valid], rl[:, :, valid])
+
+
+def test_balanced_segments_into_bshd_outputs():
+    """Balanced segments writing into head-interleaved (BSHD) output views."""
+    import int8_qk_quantized_gb300 as ia
+    Sq, Sk = 700, 1000
+    H = -(-_sms() // 3) + 1
+    wl = WORKLOADS["sdxl"].with_(H=H, Sq=Sq, Sk=Sk)
+    inp = make_inputs(wl, "cuda")
+    q8, qs, k8, ks = ia.quantize_qk(inp.q, inp.k, granularity=wl.granularity)
+    ref, rl = ia.attention(q8, k8, qs, ks, inp.v, granularity=wl.granularity, kv_splits=2,
+                           return_lse=True)
+    parent = torch.full((1, Sq, H, 64), 7.0, dtype=ref.dtype, device="cuda")
+    out = parent.permute(0, 2, 1, 3)
+    o, l = ia.attention(q8, k8, qs, ks, inp.v, granularity=wl.granularity, kv_splits=2,
+                        return_lse=True, out=out)
+    ia.device_status()
+    assert torch.equal(o, ref) and torch.equal(l, rl)
+    assert torch.equal(parent.permute(0, 2, 1, 3), ref)

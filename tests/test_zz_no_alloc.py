@@ -110,3 +110,20 @@ def test_allocates_no_device_memory():
     # unrelated tensors, never add any)
     assert torch.cuda.memory_allocated() <= held0
     ia.device_status()
+
+
+def test_balanced_segments_through_the_fixed_workspace():
+    """Head dim 64 with two key ranges and at least one query tile per SM runs
+    the balanced segments; through the allocation-free entry point the partials
+    live in the fixed workspace, and the result equals the allocating call."""
+    import int8_qk_quantized_gb300 as ia
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H = -(-sms // 3) + 1  # 3 query tiles of 256 rows per head
+    tensors, args = _prepare("sdxl", dict(H=H, Sq=700, Sk=1000))
+    q8, k8, qs, ks, v = tensors
+    ref, rl = ia.attention(q8, k8, qs, ks, v, kv_splits=2, return_lse=True, **args)
+    out = torch.empty_like(ref)
+    lse = torch.empty_like(rl)
+    o, l = ia.attention_static_workspace(q8, k8, qs, ks, v, out, lse=lse, kv_splits=2, **args)
+    ia.device_status()
+    assert torch.equal(o, ref) and torch.equal(l, rl)
