@@ -379,6 +379,29 @@ __device__ __forceinline__ void write_q_codes(const uint8_t* row, uint8_t* qh, i
   }
 }
 
+// One thread's int8 row of D codes (row r of a kM-row stage) -> fp16 codes in
+// the 128-byte-swizzled K-major layout widen_tile writes (64-column blocks
+// kM*128 bytes apart). Thread r starts at chunk r so that a warp's rows spread
+// over the shared-memory banks.
+template <int D>
+__device__ __forceinline__ void widen_row(const uint8_t* row, uint8_t* qh, int r) {
+  constexpr int CPR = D / 16;  // 16-byte int8 chunks in the row
+#pragma unroll
+  for (int c = 0; c < CPR; ++c) {
+    const int cc = (c + r) & (CPR - 1);
+    const uint4 w = *reinterpret_cast<const uint4*>(row + cc * 16);
+    uint32_t hv[8];
+    i8x4_to_f16x4(w.x, hv[0], hv[1]);
+    i8x4_to_f16x4(w.y, hv[2], hv[3]);
+    i8x4_to_f16x4(w.z, hv[4], hv[5]);
+    i8x4_to_f16x4(w.w, hv[6], hv[7]);
+    const int blk = cc >> 2, k0 = (cc & 3) * 2;  // 64-column block, first 16-byte chunk
+    uint8_t* rowp = qh + blk * (kM * 128) + r * 128;
+    *reinterpret_cast<uint4*>(rowp + ((k0 ^ (r & 7)) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    *reinterpret_cast<uint4*>(rowp + (((k0 + 1) ^ (r & 7)) << 4)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+  }
+}
+
 // One per-key offset of a key row of a general mask, in two steps so that the
 // load can be issued early and converted later: the raw bits of element
 // `key`, then their value in logit units (float dtypes as they are, bool as
@@ -545,6 +568,11 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
                     const __grid_constant__ CUtensorMap tm_m, const Params a) {
   using L = Layout<D, QS, BN, SPARSE, ROWMASK, PAIR, KB>;
   constexpr bool SEG = SEGM;
+  // dense single-CTA head-dim-64 kernels with int8 Q and per-token K scales: the
+  // softmax threads widen their own Q rows (each a row), so the converters start
+  // on K at once (with per-block scales the softmax is the lighter side and this
+  // measured slower)
+  constexpr bool QSOFT = L::SEGOK && !QRAW && !KB;
   static_assert(!SEGM || (L::SEGOK && !QRAW), "segments: dense single-CTA head-dim-64, int8 Q");
   extern __shared__ __align__(1024) uint8_t smem[];
 
@@ -616,38 +644,46 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       tc_fence_before();
       __syncthreads();
       if (*abort_flag) break;
-      if (tid == 0)
-        for (int i = 0; i < L::NBAR; ++i) mbar_inval(bar(i));
     }
+    // The barriers are (invalidated after a segment, then) initialised by five
+    // threads in five warps, side by side.
+    auto binit = [&](int i, uint32_t n) {
+      if (seg > 0) mbar_inval(bar(i));
+      mbar_init(bar(i), n);
+    };
     if (tid == 0) {
-      mbar_init(bar(L::B_QFULL), 1);
-      mbar_init(bar(L::B_QCONV), (QRAW ? QS * kM : 64) + peer_f);
-      for (int i = 0; i < L::NKS; ++i) {
-        mbar_init(bar(L::B_KRF + i), 1);
-        mbar_init(bar(L::B_KCF + i), 64 + peer_k);
-        mbar_init(bar(L::B_KCE + i), 1);
-      }
-      for (int i = 0; i < L::NRS; ++i) mbar_init(bar(L::B_KRE + i), 64);
-      for (int i = 0; i < L::NVS; ++i) {
-        mbar_init(bar(L::B_VF + i), 1 + peer_f);
-        mbar_init(bar(L::B_VE + i), 1);
-      }
-      for (int i = 0; i < L::NSC; ++i) {
-        mbar_init(bar(L::B_SCF + i), 64);
-        mbar_init(bar(L::B_SCE + i), 4 * QS);
-      }
-      for (int s = 0; s < L::NSB; ++s) {
-        mbar_init(bar(L::B_SF + s), 1);
-        mbar_init(bar(L::B_PF + s), kM + peer_p);
-      }
-      for (int s = 0; s < QS; ++s) mbar_init(bar(L::B_OF + s), 1);
-      mbar_init(bar(L::B_PVT), 1);
-      for (int i = 0; i < L::NSC; ++i) mbar_init(bar(L::B_MF + i), 1);
-      mbar_init(bar(L::B_DRAIN), 1);
-      mbar_init(bar(L::B_STALL), 1);  // never signalled: the timeout test hook waits on it
+      binit(L::B_QFULL, 1);
+      binit(L::B_QCONV, ((QRAW || QSOFT) ? QS * kM : 64) + peer_f);
+      binit(L::B_PVT, 1);
+      binit(L::B_DRAIN, 1);
+      binit(L::B_STALL, 1);  // never signalled: the timeout test hook waits on it
       misc[1] = 0;
-      fence_mbar_init();
+    } else if (tid == 32) {
+      for (int i = 0; i < L::NKS; ++i) {
+        binit(L::B_KRF + i, 1);
+        binit(L::B_KCF + i, 64 + peer_k);
+        binit(L::B_KCE + i, 1);
+      }
+      for (int i = 0; i < L::NRS; ++i) binit(L::B_KRE + i, 64);
+    } else if (tid == 64) {
+      for (int i = 0; i < L::NVS; ++i) {
+        binit(L::B_VF + i, 1 + peer_f);
+        binit(L::B_VE + i, 1);
+      }
+      for (int i = 0; i < L::NSC; ++i) binit(L::B_MF + i, 1);
+    } else if (tid == 96) {
+      for (int i = 0; i < L::NSC; ++i) {
+        binit(L::B_SCF + i, 64);
+        binit(L::B_SCE + i, 4 * QS);
+      }
+    } else if (tid == 128) {
+      for (int s = 0; s < L::NSB; ++s) {
+        binit(L::B_SF + s, 1);
+        binit(L::B_PF + s, kM + peer_p);
+      }
+      for (int s = 0; s < QS; ++s) binit(L::B_OF + s, 1);
     }
+    if ((tid & 31) == 0 && tid <= 128) fence_mbar_init();
     if (seg == 0 && warp == L::W_MMA) {  // TMEM stays allocated for every segment
       if constexpr (PAIR) {
         tmem_alloc_pair(smem_u32(misc), L::TMEM_COLS);
@@ -936,10 +972,10 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
     } else if (warp >= L::W_CONV) {
       // ---------------------------------------------- int8 -> fp16 converters
       const int ct = tid - L::W_CONV * 32;
-      bool ok = QRAW ? true : wait_bar(bar(L::B_QFULL), 0, ctl, kErrConverter);
+      bool ok = (QRAW || QSOFT) ? true : wait_bar(bar(L::B_QFULL), 0, ctl, kErrConverter);
       if constexpr (PAIR) ok = __all_sync(0xffffffffu, ok);
       if (ct == 0) IA_TRACE_POINT(14, 3);
-      if (ok && !QRAW) {
+      if (ok && !QRAW && !QSOFT) {
         for (int s = 0; s < QS; ++s)
           widen_tile<D, kM, false>(smem + L::OFF_QIN + s * L::QR, smem + L::OFF_QH + s * L::QH, ct);
         fence_proxy_async_smem();
@@ -1091,8 +1127,17 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
           fence_proxy_async_smem();
           mbar_arrive(bar(L::B_QCONV));
         }
-      } else if (row_ok) {
-        cq = __ldg(a.q_scale + b * a.qs_sb + h * a.qs_sh + (a.gran_block ? (row >> 6) : row)) * a.cq_mult;
+      } else {
+        if constexpr (QSOFT) {  // this thread widens its own Q row
+          ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_QFULL), 0, ctl, kErrSoftmax));
+          if (ok) {
+            widen_row<D>(smem + L::OFF_QIN + s * L::QR + r * D, smem + L::OFF_QH + s * L::QH, r);
+            fence_proxy_async_smem();
+            mbar_arrive(bar(L::B_QCONV));
+          }
+        }
+        if (row_ok)
+          cq = __ldg(a.q_scale + b * a.qs_sb + h * a.qs_sh + (a.gran_block ? (row >> 6) : row)) * a.cq_mult;
       }
       const int half = (r >= 64) ? 1 : 0;
       // O *= alpha over all of this stage's O columns (with ONES, the row sum too)
@@ -1419,6 +1464,15 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
         char* orow = static_cast<char*>(a.out) +
                      (b * a.o_sb + h * a.o_sh + static_cast<int64_t>(row) * a.o_ss) * 2;
+        // Head dim 64: an fp32 partial goes out through shared memory (the K
+        // buffers for stage 0, the V buffers for stage 1, idle once this
+        // stage's last P V has completed), each warp storing its 32 rows as 512
+        // contiguous bytes per instruction instead of 32 scattered 16-byte
+        // pieces. 16-byte chunk j of lane l's row sits at slot j ^ (l & 15).
+        constexpr bool STAGE = L::SEGOK;
+        const bool staged = STAGE && a.ws_o != nullptr;
+        uint8_t* stg = smem + (s == 0 ? L::OFF_KH : L::OFF_V) + (warp & 3) * (32 * D * 4);
+        if (staged) fence_proxy_async_smem();
   #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t rr[32];
@@ -1437,7 +1491,18 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
             if (pad) o0 = o1 = 0.f;
             pk[i] = VBF16 ? cvt_bf16x2(o0, o1) : cvt_f16x2(o0, o1);
           }
-          if (row_ok && a.ws_o != nullptr) {  // fp32 partial of this key range
+          if (staged) {
+  #pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4) {
+              float f[4];
+  #pragma unroll
+              for (int e = 0; e < 4; ++e)
+                f[e] = pad ? 0.f : __uint_as_float(rr[4 * v4 + e]) * inv_l * vsc[c0 + 4 * v4 + e];
+              const int j = c0 / 4 + v4;
+              *reinterpret_cast<float4*>(stg + lane * (D * 4) + ((j ^ (lane & 15)) << 4)) =
+                  make_float4(f[0], f[1], f[2], f[3]);
+            }
+          } else if (row_ok && a.ws_o != nullptr) {  // fp32 partial of this key range
             float4* dst = reinterpret_cast<float4*>(
                 a.ws_o + ((static_cast<int64_t>(split * a.B + b) * a.H + h) * a.Sq + row) * D + c0);
   #pragma unroll
@@ -1453,6 +1518,23 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
   #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4)
               dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
+        }
+        if constexpr (STAGE) {
+          if (staged) {
+            static_assert(D == 64 && L::NKS * L::KH >= 4 * 32 * D * 4 && L::NVS * L::VB >= 4 * 32 * D * 4,
+                          "staging: 256-byte rows, 32 KB per stage");
+            __syncwarp();
+            float* wsb = a.ws_o + (static_cast<int64_t>(split * a.B + b) * a.H + h) * a.Sq * D;
+            const int rbase = q0 + s * kM + (warp & 3) * 32;
+  #pragma unroll 4
+            for (int i = 0; i < 16; ++i) {  // rows 2i and 2i+1, one per half-warp
+              const int rw = 2 * i + (lane >> 4), j = lane & 15;
+              const float4 v = *reinterpret_cast<const float4*>(stg + rw * (D * 4) + ((j ^ (rw & 15)) << 4));
+              if (rbase + rw < a.Sq)
+                *reinterpret_cast<float4*>(wsb + static_cast<int64_t>(rbase + rw) * D + j * 4) = v;
+            }
+            fence_proxy_async_smem();  // before the next segment's copies into these buffers
           }
         }
         if (row_ok && (a.lse != nullptr || a.ws_l != nullptr)) {
