@@ -40,8 +40,8 @@ PAGE_SPLIT_MS = 11.05
 # unmasked), recorded with the SHA-256 of the kernel sources it was taken on. A launch's traffic is scaled
 # from it per head, with the key-proportional part scaled by the keys of the
 # launch. When the kernel sources change, the figure no longer applies.
-ATTN_TRAFFIC = {"source_sha256": "39e8c4b528a9e67152960c9219da4f4185d893bc5574c372388165eafa7d74d2",
-                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 245694208.0}
+ATTN_TRAFFIC = {"source_sha256": "58c55929a7a8b488a5f4e72a68f31c4ff92d85c56b4e4c66943f7e596c64e6e1",
+                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 244957440.0}
 
 
 def attn_source_sha():
