@@ -170,3 +170,27 @@ def test_balanced_segments_into_bshd_outputs():
     ia.device_status()
     assert torch.equal(o, ref) and torch.equal(l, rl)
     assert torch.equal(parent.permute(0, 2, 1, 3), ref)
+
+
+@pytest.mark.parametrize("name,kw", [
+    # per-key bias (skirts) and a per-channel V scale
+    ("banded", dict(D=64, Sq=700, Sk=2000, skirt_width=400, v_scale=True)),
+    # one key tile: every segment covers its query tile's keys whole (the
+    # second partial is marked empty)
+    ("sdxl", dict(Sq=700, Sk=100)),
+])
+def test_balanced_segments_with_bias_vscale_and_single_key_tile(name, kw):
+    import int8_qk_quantized_gb300 as ia
+    H = -(-_sms() // 3) + 1
+    wl = WORKLOADS[name].with_(H=H, **kw)
+    inp = make_inputs(wl, "cuda")
+    q8, qs, k8, ks = ia.quantize_qk(inp.q, inp.k, granularity=wl.granularity)
+    args = dict(bias=inp.bias, v_scale=inp.v_scale, granularity=wl.granularity, return_lse=True)
+    o1, l1 = ia.attention(q8, k8, qs, ks, inp.v, kv_splits=1, **args)
+    o2, l2 = ia.attention(q8, k8, qs, ks, inp.v, kv_splits=2, **args)
+    ia.device_status()
+    d = (o2.float() - o1.float()).abs()
+    assert d.max().item() < 2e-2 and d.mean().item() < 1e-3
+    ro, rl = oracle_full(inp, wl)
+    assert_out_close(to_np(o2), ro)
+    assert_lse_close(to_np(l2), rl)
