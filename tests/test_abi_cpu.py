@@ -159,6 +159,17 @@ def test_static_workspace_limit_checked_before_any_work(lib):
                                                  None, None, None) == 1
 
 
+def test_workspace_holds_the_partials(lib):
+    """Key-split scratch: the fp32 O and LSE of every key range."""
+    for B, H, Sq, D, n in [(1, 2, 256, 128, 2), (2, 3, 1000, 64, 2), (1, 1, 33, 64, 5),
+                           (3, 5, 4097, 64, 3), (1, 1, 1, 64, 2)]:
+        p = _params(lib, D=D, Sq=Sq)
+        p.B, p.H, p.kv_splits = B, H, n
+        assert lib.ia_attention_workspace_size(ctypes.byref(p)) == n * B * H * Sq * (D + 1) * 4
+    p.kv_splits = 1
+    assert lib.ia_attention_workspace_size(ctypes.byref(p)) == 0
+
+
 def test_mask_argument_errors(lib):
     fake = ctypes.c_void_p(0x1000)
     p = _params(lib)

@@ -175,8 +175,8 @@ def test_balanced_segments_into_bshd_outputs():
 @pytest.mark.parametrize("name,kw", [
     # per-key bias (skirts) and a per-channel V scale
     ("banded", dict(D=64, Sq=700, Sk=2000, skirt_width=400, v_scale=True)),
-    # one key tile: every segment covers its query tile's keys whole (the
-    # second partial is marked empty)
+    # one key tile: every segment covers its query tile's keys whole and
+    # writes the output directly (no partial, no merge)
     ("sdxl", dict(Sq=700, Sk=100)),
 ])
 def test_balanced_segments_with_bias_vscale_and_single_key_tile(name, kw):
@@ -194,3 +194,84 @@ def test_balanced_segments_with_bias_vscale_and_single_key_tile(name, kw):
     ro, rl = oracle_full(inp, wl)
     assert_out_close(to_np(o2), ro)
     assert_lse_close(to_np(l2), rl)
+
+
+def _workspace_bytes(wl, splits):
+    import ctypes
+    import int8_qk_quantized_gb300 as ia
+    p = ia.AttnParams()
+    ia.load_library().ia_attn_params_init(ctypes.byref(p), wl.B, wl.H, wl.Sq, wl.Sk, wl.D, 0, 0)
+    p.kv_splits = splits
+    return ia.load_library().ia_attention_workspace_size(ctypes.byref(p))
+
+
+def test_balanced_segments_need_no_clean_workspace():
+    """Balanced segments read only workspace entries written earlier in the
+    same call (a query tile covered whole by one segment writes the output
+    directly and marks its second partial empty), so a workspace of
+    arbitrary bytes, one of zeros, one of all-ones bytes (NaN floats) and one
+    reused call after call all give the same output, which meets the oracle."""
+    import int8_qk_quantized_gb300 as ia
+    Sq, Sk = 1100, 777  # ragged query rows (a last group of 12 rows) and keys
+    H = -(-_sms() // 5) + 1
+    wl = WORKLOADS["sdxl"].with_(H=H, Sq=Sq, Sk=Sk, granularity="token")
+    inp = make_inputs(wl, "cuda")
+    q8, qs, k8, ks = ia.quantize_qk(inp.q, inp.k, granularity="token")
+    args = dict(v_scale=inp.v_scale, granularity="token", return_lse=True, kv_splits=2)
+    ref_o, ref_l = ia.attention(q8, k8, qs, ks, inp.v, **args)
+    ia.device_status()
+    ro, rl = oracle_full(inp, wl)
+    assert_out_close(to_np(ref_o), ro)
+    assert_lse_close(to_np(ref_l), rl)
+    need = _workspace_bytes(wl, 2)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(11)
+    for fill in ("random", "zeros", "ones"):
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        if fill == "random":
+            ws.random_(0, 256, generator=gen)
+        else:
+            ws.fill_(0 if fill == "zeros" else 255)
+        for _ in range(3):
+            o, l = ia.attention(q8, k8, qs, ks, inp.v, workspace=ws, **args)
+            ia.device_status()
+            assert torch.equal(o, ref_o) and torch.equal(l, ref_l), fill
+
+
+def test_balanced_segments_in_a_replayed_cuda_graph():
+    """The balanced-segment call (attention launch + merge launch) captured
+    once in a CUDA graph: replays over changing inputs, copied into the
+    captured buffers, equal direct calls on the same inputs."""
+    import int8_qk_quantized_gb300 as ia
+    Sq, Sk = 1000, 1000
+    H = -(-_sms() // 4) + 1
+    wl = WORKLOADS["sdxl"].with_(H=H, Sq=Sq, Sk=Sk)
+    sets = []
+    for seed in (1, 2):
+        inp = make_inputs(wl.with_(seed=seed), "cuda")
+        q8, qs, k8, ks = ia.quantize_qk(inp.q, inp.k, granularity=wl.granularity)
+        sets.append((q8, k8, qs, ks, inp.v))
+    args = dict(granularity=wl.granularity, return_lse=True, kv_splits=2)
+    direct = [ia.attention(*t, **args) for t in sets]
+    ia.device_status()
+    bufs = [x.clone() for x in sets[0]]
+    ws = torch.empty(_workspace_bytes(wl, 2), dtype=torch.uint8, device="cuda")
+    ws.fill_(255)
+    out = torch.empty_like(direct[0][0])
+    lse = torch.empty_like(direct[0][1])
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):  # once outside the capture: function attributes set
+        ia.attention(*bufs, out=out, lse=lse, workspace=ws, **args)
+    torch.cuda.current_stream().wait_stream(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        ia.attention(*bufs, out=out, lse=lse, workspace=ws, **args)
+    for k in (1, 0, 1, 1, 0):
+        for dst, src in zip(bufs, sets[k]):
+            dst.copy_(src)
+        graph.replay()
+        torch.cuda.synchronize()
+        ia.device_status()
+        assert torch.equal(out, direct[k][0]) and torch.equal(lse, direct[k][1]), k
