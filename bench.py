@@ -307,6 +307,9 @@ def run_profile(args):
         "sparse": lambda: ia.attention(q8, k8, qs, ks, inp.v, block_mask=inp.block_mask,
                                        kv_valid=inp.kv_valid, out=out, lse=lse, return_lse=True),
     }
+    if name == "rowmask":  # the materialised bf16 [1,1,Q,K] mask of the skirt bias (per-row path)
+        m = inp.bias.to(torch.bfloat16).view(1, 1, 1, -1).expand(1, 1, wl.Sq, wl.Sk).contiguous()
+        fns["rowmask"] = lambda: ia.attention(q8, k8, qs, ks, inp.v, mask=m, out=out, kv_splits=1)
     fn = fns[name]
     for _ in range(args.warmup):
         fn()
@@ -417,7 +420,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip timing the other four workloads")
     ap.add_argument("--profile", default=None,
-                    choices=["attention", "attention_bias", "quantize", "merge", "sparse", "sdxl"],
+                    choices=["attention", "attention_bias", "quantize", "merge", "sparse", "sdxl", "rowmask"],
                     help="run one kernel alone, --steps times after --warmup (for ncu)")
     ap.add_argument("--heads", type=int, default=None, help="heads of the --profile case")
     args = ap.parse_args()
