@@ -170,6 +170,8 @@ struct Layout {
   static constexpr int SC = BN * 8 + 16;  // k scales, bias*log2e, flags
   // Per-row mask tile (ROWMASK): kM rows x BN keys as TMA boxes of 128-byte
   // rows with the 128-byte swizzle; 32 fp32, 64 16-bit or 128 bool keys per box.
+  // Sized for two fp32 boxes of one stage, or (QS == 2, masks of at most two
+  // bytes) one box per stage.
   static constexpr int MB = ROWMASK ? BN * 4 * kM : 0;
   static constexpr int OFF_QH = 0;
   static constexpr int OFF_KH = OFF_QH + QS * QH;
@@ -197,15 +199,14 @@ struct Layout {
                                    : TMEM_NEED <= 128 ? 128 : TMEM_NEED <= 256 ? 256 : 512;
   static constexpr int NWARPS = 4 * QS + 4;
   static constexpr int W_PROD = 4 * QS, W_MMA = 4 * QS + 1, W_CONV = 4 * QS + 2;
-  static_assert(PAIR || QS * QR <= VB, "int8 Q is staged in the first V buffer");
-  static_assert(PAIR || QS * QR * 2 <= NVS * VB, "16-bit Q is staged in the V buffers");
+  static_assert(PAIR || QS * QR <= NVS * VB, "int8 Q is staged in the V buffers");
   static_assert(TMEM_NEED <= 512, "TMEM budget");
   static_assert(OFF_QH % 1024 == 0 && OFF_KH % 1024 == 0 && OFF_V % 1024 == 0 &&
                     OFF_MK % 1024 == 0 && OFF_QST % 1024 == 0 && OFF_ONES % 1024 == 0,
                 "swizzle align");
   static_assert(!ONES || (VB == BN * 128 && (OFF_ONES - OFF_V) / 16 < (1 << 14)),
                 "one 64-column V block per buffer; the ones within the descriptor's reach");
-  static_assert(!ROWMASK || (QS == 1 && BN == 64 && !SPARSE), "row-mask shape");
+  static_assert(!ROWMASK || ((QS == 1 || QS == 2) && BN == 64 && !SPARSE), "row-mask shape");
   static_assert(!INPLACE || KR == BN * 128, "the int8 tile fills one 64-column fp16 block");
   // the pair's V half is one 64-column swizzle block; dense tiles only
   static_assert(!PAIR || (D == 128 && QS == 2 && BN == 128 && !SPARSE && !ROWMASK), "pair shape");
@@ -574,6 +575,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
   // measured slower)
   constexpr bool QSOFT = L::SEGOK && !QRAW && !KB;
   static_assert(!SEGM || (L::SEGOK && !QRAW), "segments: dense single-CTA head-dim-64, int8 Q");
+  static_assert(PAIR || !QRAW || QS * L::QR * 2 <= L::NVS * L::VB, "16-bit Q is staged in the V buffers");
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x;
@@ -792,7 +794,10 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
           tma_load_4d(kdst, &tm_k, bar(L::B_KRF + ks), 0, kt * BN + static_cast<int>(crank) * L::KROWS, h, b);
           kr_last[ks] = it;
           const int vs = it % L::NVS;
-          if (!PAIR && (it == 0 || (QRAW && it < L::NVS)))  // raw Q sits in V buffer 0 (all of them)
+          // Q sits in V buffer 0, or in all of them (16-bit Q, or int8 Q of two
+          // stages larger than one V buffer) until it has been widened
+          constexpr bool Q_ALL_V = QRAW || QS * L::QR > L::VB;
+          if (!PAIR && (it == 0 || (Q_ALL_V && it < L::NVS)))
             ok = wait_bar(bar(L::B_QCONV), 0, ctl, kErrProducer);
           else if (it >= L::NVS)
             ok = wait_bar(bar(L::B_VE + vs), ((it / L::NVS) - 1) & 1, ctl, kErrProducer);
@@ -804,13 +809,15 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
                         static_cast<int>(crank) * L::VCOLS + c * 64, kt * BN, h, b);
           v_last[vs] = it;
           if constexpr (ROWMASK) {  // the tile's mask rows, released with the tile's k scales
+            // boxes of stage s at (s * m_nbox + x) * kM * 128 (two stages: one box each)
             const int ms = it % L::NSC;
             if (it >= L::NSC) ok = wait_bar(bar(L::B_SCE + ms), ((it / L::NSC) - 1) & 1, ctl, kErrProducer);
             if (!ok) break;
-            mbar_arrive_expect_tx(bar(L::B_MF + ms), m_nbox * kM * 128);
-            for (int x = 0; x < m_nbox; ++x)
-              tma_load_4d(smem_u32(smem + L::OFF_MK + ms * L::MB + x * kM * 128), &tm_m,
-                          bar(L::B_MF + ms), kt * BN + x * m_kpb, q0, m_h, m_b);
+            mbar_arrive_expect_tx(bar(L::B_MF + ms), QS * m_nbox * kM * 128);
+            for (int s = 0; s < QS; ++s)
+              for (int x = 0; x < m_nbox; ++x)
+                tma_load_4d(smem_u32(smem + L::OFF_MK + ms * L::MB + (s * m_nbox + x) * kM * 128), &tm_m,
+                            bar(L::B_MF + ms), kt * BN + x * m_kpb, q0 + s * kM, m_h, m_b);
             m_last[ms] = it;
           }
         }
@@ -1274,6 +1281,12 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
                     unpack2(ffma2(fmul2(pack2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), pack2(k4.z, k4.w)),
                                   cq2o, pack2(b4.z, b4.w)), t[2], t[3]);
                   }
+                  if constexpr (ROWMASK) {  // this row's mask values (log2 units)
+                    float mk[4];
+                    row_mask4(smem + L::OFF_MK + ss * L::MB + s * (kM * 128), r, c, a.rm_dtype, mk);
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) t[e] = fmaf(mk[e], kLog2e, t[e]);
+                  }
                   const int q = (c >> 2) & 3;
                   mo[q] = fmax3(mo[q], fmaxf(t[0], t[1]), fmaxf(t[2], t[3]));
     #pragma unroll
@@ -1378,7 +1391,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
               }
               if constexpr (ROWMASK) {
                 float mk[4];
-                row_mask4(smem + L::OFF_MK + ss * L::MB, r, c, a.rm_dtype, mk);
+                row_mask4(smem + L::OFF_MK + ss * L::MB + s * (kM * 128), r, c, a.rm_dtype, mk);
     #pragma unroll
                 for (int e = 0; e < 4; ++e) f[e] = fmaf(mk[e], kLog2e, f[e]);
               }
@@ -1785,7 +1798,19 @@ template <bool QRAW>
 ia_status dispatch(const AttnLaunch& A, int num_sms, cudaStream_t st, const char** msg) {
   const ia_attn_params& p = A.p;
   const bool bf = p.v_dtype == IA_BF16;
-  if (A.row_mask) {  // one 128-row stage, 64-key tiles, mask tiles by TMA
+  if (A.row_mask) {  // 64-key tiles, mask tiles by TMA
+    // masks of at most two bytes per key with int8 Q: two 128-row stages, whose
+    // mask rows fit the ring; fp32 masks and 16-bit Q (which needs all of the
+    // V buffers per stage) take one stage
+    if constexpr (!QRAW) {
+      if (p.mask_dtype != IA_MASK_F32) {
+        if (p.D == 128)
+          return bf ? run<128, 2, 64, false, true, QRAW, true>(A, num_sms, st, msg)
+                    : run<128, 2, 64, false, false, QRAW, true>(A, num_sms, st, msg);
+        return bf ? run<64, 2, 64, false, true, QRAW, true>(A, num_sms, st, msg)
+                  : run<64, 2, 64, false, false, QRAW, true>(A, num_sms, st, msg);
+      }
+    }
     if (p.D == 128)
       return bf ? run<128, 1, 64, false, true, QRAW, true>(A, num_sms, st, msg)
                 : run<128, 1, 64, false, false, QRAW, true>(A, num_sms, st, msg);
