@@ -448,6 +448,46 @@ __device__ __forceinline__ void row_mask4(const uint8_t* buf, int r, int c, int 
   }
 }
 
+// The mask values of 16 consecutive keys of one row (bool and 16-bit masks),
+// held as raw 16-byte chunks: one load per 16 (bool) or 8 (16-bit) keys instead
+// of one per 4, and a quarter-warp's eight rows (r & 7 distinct) read eight
+// different bank groups of the swizzled rows. fp32 masks read per 4 keys.
+struct RowMask16 {
+  uint4 w0, w1;
+  __device__ __forceinline__ void load(const uint8_t* buf, int r, int c16, int dt) {
+    const uint8_t* row = buf + r * 128;
+    const int sw = r & 7;
+    if (dt == IA_MASK_BOOL) {
+      w0 = *reinterpret_cast<const uint4*>(row + (((c16 >> 4) ^ sw) << 4));
+    } else if (dt != IA_MASK_F32) {
+      w0 = *reinterpret_cast<const uint4*>(row + (((c16 >> 3) ^ sw) << 4));
+      w1 = *reinterpret_cast<const uint4*>(row + ((((c16 >> 3) + 1) ^ sw) << 4));
+    }
+  }
+  // keys c .. c+3 (c a multiple of 4, within the 16 loaded last)
+  __device__ __forceinline__ void get4(const uint8_t* buf, int r, int c, int dt, float out[4]) const {
+    if (dt == IA_MASK_F32) {
+      row_mask4(buf, r, c, dt, out);
+    } else if (dt == IA_MASK_BOOL) {
+      const int q = (c & 15) >> 2;
+      const uint32_t w = q == 0 ? w0.x : q == 1 ? w0.y : q == 2 ? w0.z : w0.w;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) out[e] = ((w >> (8 * e)) & 0xffu) ? 0.f : -INFINITY;
+    } else {
+      const uint4 v = (c & 8) ? w1 : w0;
+      const uint32_t x = (c & 4) ? v.z : v.x, y = (c & 4) ? v.w : v.y;
+      if (dt == IA_MASK_BF16) {
+        out[0] = __uint_as_float(x << 16), out[1] = __uint_as_float(x & 0xffff0000u);
+        out[2] = __uint_as_float(y << 16), out[3] = __uint_as_float(y & 0xffff0000u);
+      } else {
+        const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&x));
+        const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&y));
+        out[0] = lo.x, out[1] = lo.y, out[2] = hi.x, out[3] = hi.y;
+      }
+    }
+  }
+};
+
 // RMSNorm + RoPE of one raw 16-bit Q row in shared memory, in place, before
 // the fused quantization ("Feature Request: Direct int8 Q/K passthrough
 // between Comfy Kitchen and SageAttention", maintainer's reply: rms_rope /
@@ -1238,6 +1278,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
           tmem_wait_ld(sv);
           if (r == 0) IA_TRACE_POINT(2 + 4 * s, it);
           uint64_t lsum[2] = {pack2(0.f, 0.f), pack2(0.f, 0.f)};
+          RowMask16 rmk;  // ROWMASK: the current 16 keys' mask words
           // One pass (two query stages, a reference already set): P is taken
           // relative to the reference the previous tiles set (P may exceed 1: up to
           // 2^64 in bf16, 2^15 in fp16), the tile's maximum is taken in the same
@@ -1282,8 +1323,10 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
                                   cq2o, pack2(b4.z, b4.w)), t[2], t[3]);
                   }
                   if constexpr (ROWMASK) {  // this row's mask values (log2 units)
+                    const uint8_t* mb = smem + L::OFF_MK + ss * L::MB + s * (kM * 128);
+                    if ((c & 15) == 0) rmk.load(mb, r, c, a.rm_dtype);
                     float mk[4];
-                    row_mask4(smem + L::OFF_MK + ss * L::MB + s * (kM * 128), r, c, a.rm_dtype, mk);
+                    rmk.get4(mb, r, c, a.rm_dtype, mk);
     #pragma unroll
                     for (int e = 0; e < 4; ++e) t[e] = fmaf(mk[e], kLog2e, t[e]);
                   }
@@ -1390,8 +1433,10 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
                               cq2, pack2(b4.z, b4.w)), f[2], f[3]);
               }
               if constexpr (ROWMASK) {
+                const uint8_t* mb = smem + L::OFF_MK + ss * L::MB + s * (kM * 128);
+                if ((c & 15) == 0) rmk.load(mb, r, c, a.rm_dtype);
                 float mk[4];
-                row_mask4(smem + L::OFF_MK + ss * L::MB + s * (kM * 128), r, c, a.rm_dtype, mk);
+                rmk.get4(mb, r, c, a.rm_dtype, mk);
     #pragma unroll
                 for (int e = 0; e < 4; ++e) f[e] = fmaf(mk[e], kLog2e, f[e]);
               }
