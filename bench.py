@@ -216,6 +216,29 @@ def cpu_baseline(seconds_target=12.0):
                       f"quantise + fp64 attention with bias) in {dt:.1f} s"}
 
 
+def graph_ms(torch, fn, n=20, reps=3):
+    """ms per call of fn() captured n times in one CUDA graph and replayed reps
+    times (CUDA events around the replays, after one untimed replay)."""
+    fn()
+    torch.cuda.synchronize()
+    gs = torch.cuda.Stream()
+    gs.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gs):
+        for _ in range(n):
+            fn()
+    graph.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (n * reps)
+
+
 def time_workloads(ia, torch, names=("tiny", "sdxl", "anima4k", "anima9k", "sparse"), n=10):
     """Quantise and attention times of the other workloads (CUDA events,
     after 3 warm-up calls). TOPS use algorithmic ops (kept tiles for sparse)."""
@@ -250,6 +273,10 @@ def time_workloads(ia, torch, names=("tiny", "sdxl", "anima4k", "anima9k", "spar
                                  granularity=wl.granularity, out=out, lse=lse, return_lse=True)
 
         ms = {}
+        # device time alone: the same calls replayed from a CUDA graph, so that the
+        # host's per-call work (argument checks, output allocation) is not in it
+        ms["quantize_graph_ms"] = graph_ms(torch, tq)
+        ms["attention_graph_ms"] = graph_ms(torch, ta)
         for key, fn in (("quantize_ms", tq), ("attention_ms", ta), ("quantize_k_ms", tk),
                         ("fused_q_attention_ms", tf)):
             for _ in range(3):
