@@ -314,8 +314,9 @@ ia_status quantize(const void* q, const void* k, ia_dtype in_dtype, int B, int H
   ia_status s = check_device(&sms);
   if (s != IA_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ia::QuantArgs aq{}, ak{};
   if (q != nullptr) {
-    ia::QuantArgs a{};
+    ia::QuantArgs& a = aq;
     a.x = q;
     a.sb = q_strides[0];
     a.sh = q_strides[1];
@@ -331,11 +332,9 @@ ia_status quantize(const void* q, const void* k, ia_dtype in_dtype, int B, int H
     a.codes = q_i8;
     a.scales = q_scale;
     set_prologue(&a, pro, true);
-    cudaError_t e = ia::launch_quantize(a, sms, st);
-    if (e != cudaSuccess) return fail(IA_ERR_CUDA, "quantize(q): %s", cudaGetErrorString(e));
   }
   if (k != nullptr) {
-    ia::QuantArgs a{};
+    ia::QuantArgs& a = ak;
     a.x = k;
     a.sb = k_strides[0];
     a.sh = k_strides[1];
@@ -353,9 +352,11 @@ ia_status quantize(const void* q, const void* k, ia_dtype in_dtype, int B, int H
     a.codes = k_i8;
     a.scales = k_scale;
     set_prologue(&a, pro, false);
-    cudaError_t e = ia::launch_quantize(a, sms, st);
-    if (e != cudaSuccess) return fail(IA_ERR_CUDA, "quantize(k): %s", cudaGetErrorString(e));
   }
+  cudaError_t e = cudaSuccess;
+  if (q != nullptr && k != nullptr) e = ia::launch_quantize_qk(aq, ak, sms, st);
+  else e = ia::launch_quantize(q != nullptr ? aq : ak, sms, st);
+  if (e != cudaSuccess) return fail(IA_ERR_CUDA, "quantize: %s", cudaGetErrorString(e));
   return ok();
 }
 

@@ -222,26 +222,37 @@ __device__ __forceinline__ void lean_codes(const QuantArgs& a, const char* xb, i
   }
 }
 
-// grid: (chunks, H, B). Chunk c holds rows [c*chunk, min(S, (c+1)*chunk)).
-// With CLUSTER_MEAN the chunks of one head are one cluster and compute the mean;
-// MEAN_ONLY then stops once the mean is written to a.mean_out (codes_kernel
-// writes the codes in a second pass).
-template <int D, int DT, bool CLUSTER_MEAN, bool PRO, bool MEAN_ONLY = false>
-__global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a, int chunk) {
+// Shared memory of one quantize CTA.
+template <int D, bool CLUSTER_MEAN>
+struct QuantSmem {
+  static constexpr int RPP = kThreads / (D / 8);
+  __align__(16) float mu[D];
+  double red[CLUSTER_MEAN ? RPP : 1][CLUSTER_MEAN ? D : 1];
+  double part[CLUSTER_MEAN ? D : 1];
+  float wmax[kThreads / 32];
+  int count;
+};
+
+// Chunk cx of head (b, h): rows [cx*chunk, min(S, (cx+1)*chunk)). With
+// CLUSTER_MEAN and a.center the chunks of the head are one cluster (cx its
+// rank) and compute the mean; MEAN_ONLY then stops once the mean is written to
+// a.mean_out (codes_kernel writes the codes in a second pass).
+template <int D, int DT, bool CLUSTER_MEAN, bool PRO, bool MEAN_ONLY>
+__device__ __forceinline__ void quantize_chunk(const QuantArgs& a, int chunk, int b, int h, int cx,
+                                               QuantSmem<D, CLUSTER_MEAN>& sm) {
   constexpr int TPR = D / 8;            // threads per row, 8 elements each
   constexpr int RPP = kThreads / TPR;   // rows per pass
   static_assert(RPP * TPR == kThreads, "layout");
-  __shared__ __align__(16) float s_mu[D];
-  __shared__ double s_red[CLUSTER_MEAN ? RPP : 1][CLUSTER_MEAN ? D : 1];
-  __shared__ double s_part[CLUSTER_MEAN ? D : 1];
-  __shared__ float s_wmax[kThreads / 32];
-  __shared__ int s_count;
+  float* s_mu = sm.mu;
+  auto& s_red = sm.red;
+  double* s_part = sm.part;
+  float* s_wmax = sm.wmax;
+  int& s_count = sm.count;
 
   const int tid = threadIdx.x;
   const int tr = tid / TPR;
   const int tc = tid % TPR;
-  const int b = blockIdx.z, h = blockIdx.y;
-  const int r0 = blockIdx.x * chunk;
+  const int r0 = cx * chunk;
   const int r1 = min(a.S, r0 + chunk);
   const char* xb = static_cast<const char*>(a.x) + (static_cast<int64_t>(b) * a.sb +
                                                     static_cast<int64_t>(h) * a.sh) * 2;
@@ -303,7 +314,15 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a
       if (tid < D) {
         double tot = 0.0;
         const int nr = static_cast<int>(cluster.num_blocks());
-        for (int rk = 0; rk < nr; ++rk) tot += *cluster.map_shared_rank(&s_part[tid], rk);
+        // the partials in rank order; eight remote loads in flight at a time
+        for (int r0 = 0; r0 < nr; r0 += 8) {
+          double pv[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) pv[j] = r0 + j < nr ? *cluster.map_shared_rank(&s_part[tid], r0 + j) : 0.0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (r0 + j < nr) tot += pv[j];
+        }
         const int n = s_count > 0 ? s_count : 1;
         s_mu[tid] = static_cast<float>(tot / static_cast<double>(n));
         if (a.mean_out && cluster.block_rank() == 0) a.mean_out[bh * D + tid] = s_mu[tid];
@@ -313,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a
     } else {
       if (tid < D) {
         s_mu[tid] = __ldg(a.mean_in + bh * D + tid);
-        if (a.mean_out && blockIdx.x == 0) a.mean_out[bh * D + tid] = s_mu[tid];
+        if (a.mean_out && cx == 0) a.mean_out[bh * D + tid] = s_mu[tid];
       }
       __syncthreads();
     }
@@ -413,6 +432,28 @@ __global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a
     }
     if (tid == 0) sc[blk0 / kTile] = scale;
   }
+}
+
+// grid: (chunks, H, B); with CLUSTER_MEAN the chunks of a head are one cluster.
+template <int D, int DT, bool CLUSTER_MEAN, bool PRO, bool MEAN_ONLY = false>
+__global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantArgs a, int chunk) {
+  __shared__ QuantSmem<D, CLUSTER_MEAN> sm;
+  quantize_chunk<D, DT, CLUSTER_MEAN, PRO, MEAN_ONLY>(a, chunk, blockIdx.z, blockIdx.y, blockIdx.x, sm);
+}
+
+// Q and a centred K in one launch (a K small enough for the one-pass form):
+// grid (chunks, H, 2B) in clusters of `chunks` CTAs along x; z < B are K's
+// heads (cluster mean, then codes), z >= B are Q's (codes only, chunk_q rows
+// per CTA; the cluster is not used).
+template <int D, int DT, bool PRO>
+__global__ void __launch_bounds__(kThreads, 2)
+    quantize_qk_kernel(const QuantArgs aq, const QuantArgs ak, int chunk_q, int chunk_k) {
+  __shared__ QuantSmem<D, true> sm;
+  const int z = blockIdx.z;
+  if (z < ak.B)
+    quantize_chunk<D, DT, true, PRO, false>(ak, chunk_k, z, blockIdx.y, blockIdx.x, sm);
+  else
+    quantize_chunk<D, DT, true, PRO, false>(aq, chunk_q, z - ak.B, blockIdx.y, blockIdx.x, sm);
 }
 
 // Per-token codes without the prologue, the mean (if any) read from
@@ -517,7 +558,76 @@ cudaError_t launch_typed(const QuantArgs& a, int num_sms, cudaStream_t st) {
   return launch_codes<D, DT, PRO>(a, st);
 }
 
+// Q and K in one launch: K's clusters as in the one-pass form, sized so that the
+// two halves of the grid together fill two CTAs per SM in one wave where the
+// heads allow; Q's CTAs take the same number of chunks per head.
+template <int D, int DT, bool PRO>
+cudaError_t launch_qk_typed(const QuantArgs& aq, const QuantArgs& ak, int num_sms, cudaStream_t st) {
+  auto kern = quantize_qk_kernel<D, DT, PRO>;
+  static int max_cl = 0;
+  if (max_cl == 0) {
+    max_cl = 8;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+      cudaLaunchConfig_t q = {};
+      q.gridDim = dim3(16, 1, 1);
+      q.blockDim = dim3(kThreads);
+      int n = 0;
+      if (cudaOccupancyMaxPotentialClusterSize(&n, kern, &q) == cudaSuccess && n >= 8)
+        max_cl = n > 16 ? 16 : n;
+    }
+    cudaGetLastError();
+  }
+  const int BH = ak.B * ak.H;
+  int cl = num_sms / BH;
+  cl = cl < 1 ? 1 : (cl > max_cl ? max_cl : cl);
+  const int max_chunks = (ak.S + kTile - 1) / kTile;
+  if (cl > max_chunks) cl = max_chunks;
+  int chunk_k = (ak.S + cl - 1) / cl;
+  chunk_k = (chunk_k + kTile - 1) / kTile * kTile;
+  cl = (ak.S + chunk_k - 1) / chunk_k;
+  int chunk_q = (aq.S + cl - 1) / cl;
+  chunk_q = (chunk_q + kTile - 1) / kTile * kTile;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cl, ak.H, 2 * ak.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, aq, ak, chunk_q, chunk_k);
+}
+
+bool has_prologue(const QuantArgs& a) { return a.norm_w != nullptr || a.rope != IA_ROPE_NONE; }
+
 }  // namespace
+
+cudaError_t launch_quantize_qk(const QuantArgs& aq, const QuantArgs& ak, int num_sms, cudaStream_t st) {
+  const bool one = ak.center && ak.mean_in == nullptr && has_prologue(aq) == has_prologue(ak) &&
+                   aq.S > 0 && ak.S > 0 && ak.B > 0 && ak.H > 0 && 2 * static_cast<int64_t>(ak.B) <= 65535 &&
+                   static_cast<int64_t>(ak.B) * ak.H * ak.S * ak.D * 2 <= (int64_t{32} << 20);
+  if (!one) {
+    const cudaError_t e = launch_quantize(aq, num_sms, st);
+    return e != cudaSuccess ? e : launch_quantize(ak, num_sms, st);
+  }
+  const bool pro = has_prologue(ak);
+  if (ak.D == 128) {
+    if (pro)
+      return ak.dtype == IA_BF16 ? launch_qk_typed<128, IA_BF16, true>(aq, ak, num_sms, st)
+                                 : launch_qk_typed<128, IA_FP16, true>(aq, ak, num_sms, st);
+    return ak.dtype == IA_BF16 ? launch_qk_typed<128, IA_BF16, false>(aq, ak, num_sms, st)
+                               : launch_qk_typed<128, IA_FP16, false>(aq, ak, num_sms, st);
+  }
+  if (pro)
+    return ak.dtype == IA_BF16 ? launch_qk_typed<64, IA_BF16, true>(aq, ak, num_sms, st)
+                               : launch_qk_typed<64, IA_FP16, true>(aq, ak, num_sms, st);
+  return ak.dtype == IA_BF16 ? launch_qk_typed<64, IA_BF16, false>(aq, ak, num_sms, st)
+                             : launch_qk_typed<64, IA_FP16, false>(aq, ak, num_sms, st);
+}
 
 cudaError_t launch_quantize(const QuantArgs& a, int num_sms, cudaStream_t st) {
   if (a.S == 0 || a.B == 0 || a.H == 0) return cudaSuccess;
