@@ -139,10 +139,11 @@ typedef enum ia_mask_dtype {
  *               [B,H,ceil(S/64)] per block.
  *   k_mean_out  optional fp32 [B,H,D] output of the mean that was used. When
  *               the mean is computed, k_mean_out is given and K holds more
- *               than 32 MiB, the pass runs as two kernels: the K sum
+ *               than 64 MiB, the pass runs as two kernels: the K sum
  *               (clusters of CTAs per head, writing the mean here), then the
  *               codes. Otherwise one fused kernel sums and quantises each
- *               head. The results are the same bits; on a large K the
+ *               head (for a K of at most 64 MiB, with Q's codes in the same
+ *               launch). The results are the same bits; on a large K the
  *               two-kernel form is faster (K no longer fits in L2 for the
  *               fused kernel's second read, and its code pass is not held
  *               at a cluster barrier).

@@ -29,6 +29,9 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kTile = 64;
+// Largest centred K (bytes) that takes the one-pass cluster form: all heads are
+// read at once, and the code pass finds its chunk still in L2.
+constexpr int64_t kOnePassMaxBytes = int64_t{64} << 20;
 
 template <int DT>
 __device__ __forceinline__ void unpack8(const uint4 w, float (&v)[8]) {
@@ -505,13 +508,13 @@ cudaError_t launch_typed(const QuantArgs& a, int num_sms, cudaStream_t st) {
     // One cluster per head, sized so that the grid fills two CTAs per SM in
     // one wave where the heads allow (up to the largest cluster the device
     // can place; 16 needs the non-portable cluster size attribute).
-    // A K larger than ~1/4 of L2 is not there any more when the fused pass
-    // reads it the second time: then, with somewhere to put the mean, two
+    // A K above kOnePassMaxBytes (about half of L2) is not there any more when
+    // the fused pass reads it the second time: then, with somewhere to put the mean, two
     // passes (the clusters only sum K and write the mean, the code kernel
     // reads it), which keeps the code pass off the cluster barrier. A
     // smaller K stays in L2 and one fused pass saves a launch.
     const bool two_pass = a.mean_out != nullptr &&
-                          static_cast<int64_t>(BH) * a.S * D * 2 > (int64_t{32} << 20);
+                          static_cast<int64_t>(BH) * a.S * D * 2 > kOnePassMaxBytes;
     auto fused = quantize_kernel<D, DT, true, PRO, false>;
     auto mean_only = quantize_kernel<D, DT, true, PRO, true>;
     auto kern = two_pass ? mean_only : fused;
@@ -609,7 +612,7 @@ bool has_prologue(const QuantArgs& a) { return a.norm_w != nullptr || a.rope != 
 cudaError_t launch_quantize_qk(const QuantArgs& aq, const QuantArgs& ak, int num_sms, cudaStream_t st) {
   const bool one = ak.center && ak.mean_in == nullptr && has_prologue(aq) == has_prologue(ak) &&
                    aq.S > 0 && ak.S > 0 && ak.B > 0 && ak.H > 0 && 2 * static_cast<int64_t>(ak.B) <= 65535 &&
-                   static_cast<int64_t>(ak.B) * ak.H * ak.S * ak.D * 2 <= (int64_t{32} << 20);
+                   static_cast<int64_t>(ak.B) * ak.H * ak.S * ak.D * 2 <= kOnePassMaxBytes;
   if (!one) {
     const cudaError_t e = launch_quantize(aq, num_sms, st);
     return e != cudaSuccess ? e : launch_quantize(ak, num_sms, st);

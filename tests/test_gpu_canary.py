@@ -88,13 +88,16 @@ QUANT_CASES = [
 
 @pytest.mark.parametrize("with_mean", [True, False], ids=["mean_out", "no_mean_out"])
 @pytest.mark.parametrize("name,kw", QUANT_CASES + [
-    # K above 32 MiB: with a mean output, the mean kernel and the code kernel
+    # K between 32 and 64 MiB: one launch for Q and K (cluster mean, then codes)
     ("banded", dict(H=2, Sq=200, Sk=66001, skirt_width=600)),
     ("sparse", dict(H=1, Sq=135168, Sk=135168, band_tiles=4, random_tiles=2, granularity="block64")),
+    # K above 64 MiB: with a mean output, the mean kernel and the code kernel
+    ("banded", dict(H=4, Sq=200, Sk=66001, skirt_width=600)),
+    ("sparse", dict(H=2, Sq=135168, Sk=135168, band_tiles=4, random_tiles=2, granularity="block64")),
 ])
 def test_quantize_outputs_stay_in_bounds(name, kw, with_mean):
-    """A K above 32 MiB with a mean output runs the mean and code kernels;
-    otherwise the fused kernel."""
+    """A K above 64 MiB with a mean output runs the mean and code kernels;
+    otherwise Q and K go in one launch (the fused kernel for K)."""
     import int8_qk_quantized_gb300 as ia
     wl = WORKLOADS[name].with_(**kw)
     inp = make_inputs(wl, "cuda")

@@ -1,7 +1,7 @@
 """GPU quantiser against the oracle: codes, scales and the K mean bit for bit.
 
-Covers the fused kernel and, for a K above 32 MiB, the two-kernel path (mean
-pass, then codes), per-token and per-64-row-block scales, bf16 and fp16, D 64
+Covers the fused kernel (with Q in the same launch for a K of at most 64 MiB)
+and, for a larger K, the two-kernel path (mean pass, then codes), per-token and per-64-row-block scales, bf16 and fp16, D 64
 and 128,
 ragged tails, the validity vector, strided (BSHD-backed) inputs, an external
 mean, no centring, and the full-size K of the banded and block-sparse
@@ -75,12 +75,15 @@ def test_quantize_bit_exact(name, kw):
     assert_same(got, ref)
 
 
-# K above 32 MiB: with a mean buffer the library runs the mean kernel and the
-# code kernel, without one the fused kernel; both against the oracle (ragged
-# tail, validity vector, per-token and per-block scales)
+# A K between 32 and 64 MiB takes the one-pass cluster form with Q in the same
+# launch; above 64 MiB, with a mean buffer, the library runs the mean kernel and
+# the code kernel, without one the fused kernel. All against the oracle (ragged
+# tail, validity vector, per-token and per-block scales).
 LARGE = [
-    ("banded", dict(H=2, Sq=300, Sk=70001, skirt_width=600)),
+    ("banded", dict(H=2, Sq=300, Sk=70001, skirt_width=600)),   # 35.8 MB: one pass
     ("sparse", dict(H=1, Sq=140032, Sk=140032, band_tiles=8, random_tiles=4, granularity="block64")),
+    ("banded", dict(H=4, Sq=300, Sk=70001, skirt_width=600)),   # 71.7 MB: two kernels
+    ("sparse", dict(H=2, Sq=140032, Sk=140032, band_tiles=8, random_tiles=4, granularity="block64")),
 ]
 
 
