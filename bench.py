@@ -313,7 +313,7 @@ def run_profile(args):
     from workloads import WORKLOADS, make_inputs
 
     name = args.profile
-    wl = WORKLOADS[{"sparse": "sparse", "sdxl": "sdxl"}.get(name, "banded")]
+    wl = WORKLOADS[{"sparse": "sparse", "sparse_fused_q": "sparse", "sdxl": "sdxl"}.get(name, "banded")]
     if args.heads:
         wl = wl.with_(H=args.heads)
     inp = make_inputs(wl, "cuda")
@@ -334,6 +334,10 @@ def run_profile(args):
         "sparse": lambda: ia.attention(q8, k8, qs, ks, inp.v, block_mask=inp.block_mask,
                                        kv_valid=inp.kv_valid, out=out, lse=lse, return_lse=True),
     }
+    # the block-sparse call with Q quantized in the kernel (16-bit Q rows in)
+    fns["sparse_fused_q"] = lambda: ia.attention_quant_q(inp.q, k8, ks, inp.v, block_mask=inp.block_mask,
+                                                         kv_valid=inp.kv_valid, out=out, lse=lse,
+                                                         return_lse=True)
     if name == "rowmask":  # the materialised bf16 [1,1,Q,K] mask of the skirt bias (per-row path)
         m = inp.bias.to(torch.bfloat16).view(1, 1, 1, -1).expand(1, 1, wl.Sq, wl.Sk).contiguous()
         fns["rowmask"] = lambda: ia.attention(q8, k8, qs, ks, inp.v, mask=m, out=out, kv_splits=1)
@@ -447,7 +451,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip timing the other four workloads")
     ap.add_argument("--profile", default=None,
-                    choices=["attention", "attention_bias", "quantize", "merge", "sparse", "sdxl", "rowmask"],
+                    choices=["attention", "attention_bias", "quantize", "merge", "sparse", "sparse_fused_q", "sdxl",
+                             "rowmask"],
                     help="run one kernel alone, --steps times after --warmup (for ncu)")
     ap.add_argument("--heads", type=int, default=None, help="heads of the --profile case")
     args = ap.parse_args()
