@@ -142,11 +142,11 @@ typedef enum ia_mask_dtype {
  *               than 64 MiB, the pass runs as two kernels: the K sum
  *               (clusters of CTAs per head, writing the mean here), then the
  *               codes. Otherwise one fused kernel sums and quantises each
- *               head (for a K of at most 64 MiB, with Q's codes in the same
- *               launch). The results are the same bits; on a large K the
- *               two-kernel form is faster (K no longer fits in L2 for the
- *               fused kernel's second read, and its code pass is not held
- *               at a cluster barrier).
+ *               head (for a K of at most 64 MiB and a Q at most twice as
+ *               long, with Q's codes in the same launch). The results are the
+ *               same bits; on a large K the two-kernel form is faster (K no
+ *               longer fits in L2 for the fused kernel's second read, and its
+ *               code pass is not held at a cluster barrier).
  * Limits (IA_ERR_UNSUPPORTED): H <= 65535 and B <= 65535.
  */
 IA_API ia_status ia_quantize_qk(const void* q, const void* k, ia_dtype in_dtype, int B, int H,

@@ -33,8 +33,8 @@ struct QuantArgs {
 
 cudaError_t launch_quantize(const QuantArgs& a, int num_sms, cudaStream_t st);
 // Q (no centring) and K together: one launch when K takes the one-pass
-// cluster form (centred, no given mean, small enough to stay in L2), else the
-// two launches of launch_quantize, Q first.
+// cluster form (centred, no given mean, small enough to stay in L2) and Q is
+// at most twice as long as K, else the two launches of launch_quantize, Q first.
 cudaError_t launch_quantize_qk(const QuantArgs& aq, const QuantArgs& ak, int num_sms, cudaStream_t st);
 
 struct MergeArgs {

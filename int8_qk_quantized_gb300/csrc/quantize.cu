@@ -610,8 +610,11 @@ bool has_prologue(const QuantArgs& a) { return a.norm_w != nullptr || a.rope != 
 }  // namespace
 
 cudaError_t launch_quantize_qk(const QuantArgs& aq, const QuantArgs& ak, int num_sms, cudaStream_t st) {
+  // (Q's CTAs take as many chunks per head as K's cluster: a Q much longer
+  // than K is better served by its own code kernel)
   const bool one = ak.center && ak.mean_in == nullptr && has_prologue(aq) == has_prologue(ak) &&
-                   aq.S > 0 && ak.S > 0 && ak.B > 0 && ak.H > 0 && 2 * static_cast<int64_t>(ak.B) <= 65535 &&
+                   aq.S > 0 && ak.S > 0 && aq.S <= 2 * static_cast<int64_t>(ak.S) && ak.B > 0 && ak.H > 0 &&
+                   2 * static_cast<int64_t>(ak.B) <= 65535 &&
                    static_cast<int64_t>(ak.B) * ak.H * ak.S * ak.D * 2 <= kOnePassMaxBytes;
   if (!one) {
     const cudaError_t e = launch_quantize(aq, num_sms, st);

@@ -63,6 +63,10 @@ SMALL = [
     ("banded", dict(H=2, Sq=300, Sk=3000, skirt_width=600)),
     ("sparse", dict(H=2, Sq=2048, Sk=2048, band_tiles=8, random_tiles=4)),
     ("sparse", dict(H=2, Sq=2048, Sk=2048, band_tiles=8, random_tiles=4, granularity="block64")),
+    # a Q more than twice as long as K: Q's code kernel and K's cluster kernel
+    # run as two launches (in one launch Q would get only K's chunk count)
+    ("anima4k", dict(H=2, Sq=5000, Sk=700)),
+    ("anima4k", dict(H=2, Sq=3001, Sk=640, granularity="block64", dtype="fp16")),
 ]
 
 
