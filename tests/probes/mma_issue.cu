@@ -7,9 +7,10 @@
 // or, for the "mix" cases, 4 SS MMAs and 8 TS MMAs (M = 128, N = 64: the
 // head-dim-64 P V shape), each followed by a commit. Between groups a case
 // adds nothing, a fence, or a wait on an mbarrier phase that has already
-// completed (so the wait returns at once). The two-issuer case runs the mix
-// with waits from one thread in each of two warps (disjoint accumulators)
-// and prints cycles per group of the two together.
+// completed (so the wait returns at once), or a poll of a shared-memory word
+// that is already set (an acquire load, or a volatile one). The two-issuer case
+// runs the mix with waits from one thread in each of two warps (disjoint
+// accumulators) and prints cycles per group of the two together.
 //
 // Operand values do not affect the time: shared memory holds zeros, the TMEM A
 // operand whatever the allocation held. Every wait is bounded.
@@ -20,6 +21,24 @@
 #include <cstdlib>
 
 #include "../../int8_qk_quantized_gb300/csrc/ptx.cuh"
+
+__device__ __forceinline__ uint32_t ld_acq(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared.u32 %0, [%1];"
+               : "=r"(v)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p)))
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_vol(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.volatile.shared.u32 %0, [%1];"
+               : "=r"(v)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p)))
+               : "memory");
+  return v;
+}
+
 using namespace ia;
 
 namespace {
@@ -32,9 +51,17 @@ __device__ __forceinline__ void wait_done(uint32_t bar) {
   }
 }
 
+template <bool ACQ>
+__device__ __forceinline__ void poll_flag(const uint32_t* f) {
+  for (int g = 0; g < 1000; ++g)
+    if ((ACQ ? ld_acq(f) : ld_vol(f)) == 1u) break;
+}
+
 // CASE 0: 4 SS; 1: + commit + fence::after_thread_sync; 2: + commit + wait;
 // 3: + commit + wait + fence; 4: mix without waits; 5: mix with a wait (and
-// fence) after each commit; 6: case 5 on two issuers.
+// fence) after each commit; 6: case 5 on two issuers; 7, 8: case 3 with an
+// acquire / volatile poll of a set word instead of the wait; 9, 10: case 5
+// likewise.
 template <int CASE>
 __global__ void __launch_bounds__(128) probe(unsigned long long* out) {
   extern __shared__ __align__(1024) uint8_t smraw[];
@@ -59,6 +86,7 @@ __global__ void __launch_bounds__(128) probe(unsigned long long* out) {
   tc_fence_after();
   const uint32_t pre = bars + 32;
   if (tid == 0) mbar_arrive(pre);  // phase 0 of `pre` completes here
+  if (tid == 0) slot[1] = 1u;      // the flag the poll cases read
   __syncthreads();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(slot);
   const int who = (CASE == 6) ? (lane == 0 && warp < 2 ? warp : -1) : (tid == 0 ? 0 : -1);
@@ -77,15 +105,21 @@ __global__ void __launch_bounds__(128) probe(unsigned long long* out) {
       for (int kk = 0; kk < 4; ++kk)
         mma_ss(dq, ad + ((kk * 32) >> 4), bd + ((kk * 32) >> 4), idq, (r | kk) ? 1u : 0u);
       if constexpr (CASE >= 1) mma_commit(cbar);
-      if constexpr (CASE == 2 || CASE == 3 || CASE >= 5) wait_done(pre);
+      if constexpr (CASE == 2 || CASE == 3 || (CASE >= 5 && CASE <= 6)) wait_done(pre);
+      if constexpr (CASE == 7 || CASE == 9) poll_flag<true>(slot + 1);
+      if constexpr (CASE == 8 || CASE == 10) poll_flag<false>(slot + 1);
       if constexpr (CASE == 1 || CASE == 3 || CASE >= 5) tc_fence_after();
-      if constexpr (CASE >= 4) {
+      if constexpr (CASE == 4 || CASE == 5 || CASE == 6 || CASE >= 9) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ts(dv, pa + kk * 8, vd + ((kk * 16 * 128) >> 4), idv, (r | kk) ? 1u : 0u);
         mma_commit(cbar);
-        if constexpr (CASE >= 5) {
+        if constexpr (CASE == 5 || CASE == 6) {
           wait_done(pre);
+          tc_fence_after();
+        }
+        if constexpr (CASE >= 9) {
+          poll_flag<CASE == 9>(slot + 1);
           tc_fence_after();
         }
       }
@@ -135,5 +169,9 @@ int main() {
   run<4>(d, "mix");
   run<5>(d, "mix+waits");
   run<6>(d, "mix+waits,two-issuers");
+  run<7>(d, "4SS+commit+acquire-poll+fence");
+  run<8>(d, "4SS+commit+volatile-poll+fence");
+  run<9>(d, "mix+acquire-polls");
+  run<10>(d, "mix+volatile-polls");
   return 0;
 }
