@@ -615,7 +615,13 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
   // measured slower)
   constexpr bool QSOFT = L::SEGOK && !QRAW && !KB;
   static_assert(!SEGM || (L::SEGOK && !QRAW), "segments: dense single-CTA head-dim-64, int8 Q");
-  static_assert(PAIR || !QRAW || QS * L::QR * 2 <= L::NVS * L::VB, "16-bit Q is staged in the V buffers");
+  // Where Q lands before it is widened or quantized: the V buffers, or (16-bit Q
+  // rows of two stages with a per-row mask, 64 KB at head dim 128) the mask ring,
+  // whose first tiles are copied only once Q has been quantized
+  constexpr bool Q_IN_MK = QRAW && ROWMASK && QS == 2;
+  constexpr int OFF_QIN = Q_IN_MK ? L::OFF_MK : L::OFF_QIN;
+  static_assert(PAIR || !QRAW || QS * L::QR * 2 <= (Q_IN_MK ? L::NSC * L::MB : L::NVS * L::VB),
+                "16-bit Q fits its staging area");
   extern __shared__ __align__(1024) uint8_t smem[];
 
   const int tid = threadIdx.x;
@@ -810,7 +816,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         // int8 Q codes, or 16-bit Q rows that the softmax warps quantize; either
         // way they are staged in the V buffers until converted
         constexpr int QB = QRAW ? 2 : 1;
-        const uint32_t sm_qin = smem_u32(smem + L::OFF_QIN);
+        const uint32_t sm_qin = smem_u32(smem + OFF_QIN);
         mbar_arrive_expect_tx(bar(L::B_QFULL), QS * kM * D * QB);
         IA_TRACE_POINT(14, 2);
         for (int s = 0; s < QS; ++s)
@@ -837,7 +843,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
           // Q sits in V buffer 0, or in all of them (16-bit Q, or int8 Q of two
           // stages larger than one V buffer) until it has been widened
           constexpr bool Q_ALL_V = QRAW || QS * L::QR > L::VB;
-          if (!PAIR && (it == 0 || (Q_ALL_V && it < L::NVS)))
+          if (!PAIR && !Q_IN_MK && (it == 0 || (Q_ALL_V && it < L::NVS)))
             ok = wait_bar(bar(L::B_QCONV), 0, ctl, kErrProducer);
           else if (it >= L::NVS)
             ok = wait_bar(bar(L::B_VE + vs), ((it / L::NVS) - 1) & 1, ctl, kErrProducer);
@@ -851,7 +857,10 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
           if constexpr (ROWMASK) {  // the tile's mask rows, released with the tile's k scales
             // boxes of stage s at (s * m_nbox + x) * kM * 128 (two stages: one box each)
             const int ms = it % L::NSC;
-            if (it >= L::NSC) ok = wait_bar(bar(L::B_SCE + ms), ((it / L::NSC) - 1) & 1, ctl, kErrProducer);
+            if (Q_IN_MK && it < L::NSC)  // the ring still holds the 16-bit Q rows
+              ok = wait_bar(bar(L::B_QCONV), 0, ctl, kErrProducer);
+            else if (it >= L::NSC)
+              ok = wait_bar(bar(L::B_SCE + ms), ((it / L::NSC) - 1) & 1, ctl, kErrProducer);
             if (!ok) break;
             mbar_arrive_expect_tx(bar(L::B_MF + ms), QS * m_nbox * kM * 128);
             for (int s = 0; s < QS; ++s)
@@ -1024,7 +1033,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
       if (ct == 0) IA_TRACE_POINT(14, 3);
       if (ok && !QRAW && !QSOFT) {
         for (int s = 0; s < QS; ++s)
-          widen_tile<D, kM, false>(smem + L::OFF_QIN + s * L::QR, smem + L::OFF_QH + s * L::QH, ct);
+          widen_tile<D, kM, false>(smem + OFF_QIN + s * L::QR, smem + L::OFF_QH + s * L::QH, ct);
         fence_proxy_async_smem();
         mbar_arrive(bar(L::B_QCONV));
         if (ct == 0) IA_TRACE_POINT(14, 4);
@@ -1146,7 +1155,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         // block's two warps also scans the other warp's rows; without the
         // prologue those rows are not modified, so no barrier is needed).
         ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_QFULL), 0, ctl, kErrSoftmax));
-        uint8_t* raw = smem + L::OFF_QIN + static_cast<size_t>(s * kM) * D * 2;
+        uint8_t* raw = smem + OFF_QIN + static_cast<size_t>(s * kM) * D * 2;
         auto quantized = [&](int rr) {  // row rr of this stage: real and not padding
           const int gr = q0 + s * kM + rr;
           return gr < a.Sq && !(a.pad_query && (gr & 63) >= __ldg(a.kv_valid + (gr >> 6)));
@@ -1178,7 +1187,7 @@ __global__ void __launch_bounds__(32 * (4 * QS + 4), SPARSE ? 2 : 1)
         if constexpr (QSOFT) {  // this thread widens its own Q row
           ok = __all_sync(0xffffffffu, wait_bar(bar(L::B_QFULL), 0, ctl, kErrSoftmax));
           if (ok) {
-            widen_row<D>(smem + L::OFF_QIN + s * L::QR + r * D, smem + L::OFF_QH + s * L::QH, r);
+            widen_row<D>(smem + OFF_QIN + s * L::QR + r * D, smem + L::OFF_QH + s * L::QH, r);
             fence_proxy_async_smem();
             mbar_arrive(bar(L::B_QCONV));
           }
@@ -1844,17 +1853,15 @@ ia_status dispatch(const AttnLaunch& A, int num_sms, cudaStream_t st, const char
   const ia_attn_params& p = A.p;
   const bool bf = p.v_dtype == IA_BF16;
   if (A.row_mask) {  // 64-key tiles, mask tiles by TMA
-    // masks of at most two bytes per key with int8 Q: two 128-row stages, whose
-    // mask rows fit the ring; fp32 masks and 16-bit Q (which needs all of the
-    // V buffers per stage) take one stage
-    if constexpr (!QRAW) {
-      if (p.mask_dtype != IA_MASK_F32) {
-        if (p.D == 128)
-          return bf ? run<128, 2, 64, false, true, QRAW, true>(A, num_sms, st, msg)
-                    : run<128, 2, 64, false, false, QRAW, true>(A, num_sms, st, msg);
-        return bf ? run<64, 2, 64, false, true, QRAW, true>(A, num_sms, st, msg)
-                  : run<64, 2, 64, false, false, QRAW, true>(A, num_sms, st, msg);
-      }
+    // masks of at most two bytes per key: two 128-row stages, whose mask rows
+    // fit the ring (16-bit Q rows are staged in that ring until quantized);
+    // fp32 masks take one stage
+    if (p.mask_dtype != IA_MASK_F32) {
+      if (p.D == 128)
+        return bf ? run<128, 2, 64, false, true, QRAW, true>(A, num_sms, st, msg)
+                  : run<128, 2, 64, false, false, QRAW, true>(A, num_sms, st, msg);
+      return bf ? run<64, 2, 64, false, true, QRAW, true>(A, num_sms, st, msg)
+                : run<64, 2, 64, false, false, QRAW, true>(A, num_sms, st, msg);
     }
     if (p.D == 128)
       return bf ? run<128, 1, 64, false, true, QRAW, true>(A, num_sms, st, msg)
