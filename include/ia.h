@@ -222,9 +222,9 @@ typedef struct ia_attn_params {
                                    of a bias. q != 0 (a row per query) is read by TMA into
                                    shared memory per key tile: base and the b, h, q strides
                                    16-byte aligned; not combinable with a block mask. With
-                                   int8 Q and a mask of at most two bytes per key the CTA
-                                   runs two 128-row stages (~2.3x unmasked); fp32 masks and
-                                   ia_attention_fwd_quant_q run one (~3.5x). */
+                                   a mask of at most two bytes per key the CTA runs two
+                                   128-row stages (~2.3x unmasked, in both entry points);
+                                   fp32 masks run one (~3.5x). */
   const ia_qk_prologue* q_prologue; /* ia_attention_fwd_quant_q only: RMSNorm + RoPE of
                                    the Q rows before the in-kernel quantization (its q_*
                                    fields, eps, rope tables); NULL for none */
