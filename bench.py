@@ -40,8 +40,8 @@ PAGE_SPLIT_MS = 11.05
 # unmasked), recorded with the SHA-256 of the kernel sources it was taken on. A launch's traffic is scaled
 # from it per head, with the key-proportional part scaled by the keys of the
 # launch. When the kernel sources change, the figure no longer applies.
-ATTN_TRAFFIC = {"source_sha256": "b7e248c28fa1a7edb9ecd62320bbf5fefb97e3f3db5d99006111c4066c7fa880",
-                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 244961024.0}
+ATTN_TRAFFIC = {"source_sha256": "955c2c8ac1c2a758f6f496fa873c80ed14e2036a0a7a925829e0902873be4bd5",
+                "heads": 16, "sq": 4096, "sk": 33600, "d": 128, "bytes": 245499648.0}
 
 
 def attn_source_sha():
