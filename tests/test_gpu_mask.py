@@ -176,6 +176,18 @@ def test_mask_errors():
         ia.attention(q8, k8, qs, ks, inp.v, mask=m, bias=torch.zeros(256, device="cuda"))
 
 
+@pytest.mark.parametrize("kind,D", [("bf16", 128), ("bool", 64)])
+def test_per_row_mask_single_partial_key_tile(kind, D):
+    """Fewer keys than one 64-key tile (48): the mask boxes and the K and V
+    tiles run past Sk in both query stages, for both entry points."""
+    wl = BASE.with_(Sq=300, Sk=48, D=D, v_scale=False)
+    inp = make_inputs(wl, "cuda")
+    m = make_mask((1, 1, wl.Sq, wl.Sk), kind, 9)
+    o1, l1 = run_and_check(wl, inp, m)
+    o2, l2 = run_and_check(wl, inp, m, quant_q=True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 def test_per_row_mask_full_size_equals_broadcast():
     """The banded workload at full size (56 heads, 4096 x 33600 x 128) with the
     skirt bias as a bf16 mask: materialised with a row per query (the two-stage
